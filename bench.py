@@ -1,0 +1,512 @@
+#!/usr/bin/env python3
+"""Throughput of the GPT-2 pre-norm forward on GB300 through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--seed S]
+
+A step is one pass of the whole forward path of the workload over one batch of
+synthetic, seeded input already resident in device memory: the block
+(LN1, c_attn, causal attention, c_proj + residual, LN2, c_fc + GELU, mlp
+c_proj + residual), the full model (embedding, L blocks, ln_f, tied head) or
+one cached decode step.  The default workload is the GPT-2-small block
+(d=768, 12 heads, B=8, T=1024, bf16 storage, fp32 accumulate).
+
+Timing: W untimed warm-up steps, then K steps each bracketed by CUDA events
+on the launching stream, with L2 flushed (a 256 MiB device write) between
+steps; a barrier and a device synchronize bracket the K steps; the per-step
+time is the maximum over ranks.  Under torchrun each rank runs an independent
+replica of the workload (the forward has no cross-sequence exchange), so the
+whole-job value is the sum of the ranks' tokens over the slowest rank's time.
+
+One JSON line is printed by rank 0.  Beside the device-timed value it carries:
+  e2e         the same metric through the C ABI with pinned host buffers, the
+              host->device copy of the inputs and the device->host copy of the
+              result inside each timed step;
+  roofline    the dominant kernel's achieved rate (its algorithmic flops or
+              bytes per launch over its CUDA-event duration, measured in a
+              second, profiled pass of K steps) against the measured peak;
+  cpu_baseline  the fp64 oracle timed on the host cores on a bounded sample;
+  clocks      SM clocks and throttle reasons sampled during the timed steps.
+--impl reference times the oracle itself as the reference arm.
+"""
+from __future__ import annotations
+
+import os
+
+# The oracle's matrix products use numpy's BLAS: give it every host core
+# (set before numpy is first imported).
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
+
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from gpt_pre_norm_gb300 import synthetic as S  # noqa: E402
+
+METRIC = "GPT-2 block/full-forward tokens/s at 1 GB300; achieved TFLOP/s vs bf16 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+TENSOR_KINDS = {"gemm_c_attn", "gemm_c_proj", "gemm_c_fc", "gemm_mlp_c_proj", "gemm_lm_head",
+                "gemm_other", "attention_prefill"}
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ------------------------------------------------------------------ helpers --
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def source_digest(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+KERNEL_SOURCES = {
+    "gemm": ["gpt_pre_norm_gb300/csrc/gemm_tc.cu", "gpt_pre_norm_gb300/csrc/device.cuh"],
+    "attention": ["gpt_pre_norm_gb300/csrc/attention.cu", "gpt_pre_norm_gb300/csrc/device.cuh"],
+    "row": ["gpt_pre_norm_gb300/csrc/rowwise.cu", "gpt_pre_norm_gb300/csrc/device.cuh"],
+}
+
+
+def kernel_family(kind: str) -> str:
+    if kind.startswith("gemm"):
+        return "gemm"
+    if kind.startswith("attention"):
+        return "attention"
+    return "row"
+
+
+def ncu_traffic(kind: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel's sources changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    digest = source_digest(KERNEL_SOURCES[kernel_family(kind)])
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) == 4 and not line.startswith("#") and parts[0] == kind \
+                    and parts[1] == workload and parts[3] == digest:
+                return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, v in enumerate(flags)
+                          if v.lower() == "active"})
+        mx = max(r[1] for r in rows)
+        loaded = [r[0] for r in rows if r[0] > 0.5 * mx] or [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- workloads --
+def workload_flops(w: S.Workload) -> float:
+    """Algorithmic flops of one step (dense products; causal attention pairs)."""
+    d, B, T = w.d, w.B, w.T
+    tp = w.t_past
+    gemm = 2.0 * B * T * (3 * d * d + d * d + 4 * d * d + 4 * d * d)
+    pairs = T * tp + 0.5 * T * (T + 1)
+    attn = 4.0 * B * w.n_head * pairs * w.d_h
+    per_layer = gemm + attn
+    if w.kind == "block":
+        return per_layer
+    return w.n_layer * per_layer + 2.0 * B * T * d * w.n_vocab
+
+
+def to_dev_bf16(a: np.ndarray, torch, device):
+    bits = S.bf16_bits(a).view(np.int16)
+    return torch.from_numpy(bits).to(device).view(torch.bfloat16)
+
+
+class Runner:
+    """Builds one workload's device state and exposes step functions."""
+
+    def __init__(self, w: S.Workload, seed: int, device):
+        import torch
+        from gpt_pre_norm_gb300 import binding as G
+        self.G, self.torch, self.w, self.device = G, torch, w, device
+        mode = G.GPT2_BF16 if w.dtype == "bf16" else G.GPT2_FP32
+        dt = torch.bfloat16 if mode == G.GPT2_BF16 else torch.float32
+
+        def todev(a):
+            return to_dev_bf16(a, torch, device) if mode == G.GPT2_BF16 else \
+                torch.from_numpy(a).to(device)
+
+        T_ctx = w.T
+        self.ctx = G.Context(w.n_vocab, w.n_ctx, w.d, w.n_head, w.n_layer, mode, w.B, T_ctx)
+        if w.kind == "block":
+            p = S.block_params(w, seed)
+            self.params = {k: todev(v) for k, v in p.items()}
+            x = S.block_input(w, seed)
+            self.x = todev(x)
+            self.out = torch.empty_like(self.x)
+            self.x_host = self.x.cpu().pin_memory()
+            self.out_host = torch.empty(self.out.shape, dtype=dt).pin_memory()
+            self.tokens = w.B * w.T
+        else:
+            p = S.model_params(w, seed)
+            tp = {k: todev(p[k]) for k in ("wte", "wpe", "lnf_g", "lnf_b")}
+            tp["blocks"] = [{k: todev(v) for k, v in b.items()} for b in p["blocks"]]
+            self.mp = G.ModelParams(tp)
+            ids = S.token_ids(w, seed)
+            self.ids = torch.from_numpy(ids).to(device)
+            self.ids_host = self.ids.cpu().pin_memory()
+            self.logits = torch.empty((w.B, w.T, w.n_vocab), dtype=torch.float32, device=device)
+            self.logits_host = torch.empty(self.logits.shape, dtype=torch.float32).pin_memory()
+            self.tokens = w.B * w.T
+            self.cache = None
+            if w.kind == "decode":
+                shape = (w.B, w.n_layer, 2, w.n_head, w.n_ctx, w.d_h)
+                host = torch.empty(shape, dtype=torch.int16).pin_memory()
+                hv = host.numpy()
+                for b in range(w.B):
+                    for layer in range(w.n_layer):
+                        pk = S.past_kv(w, seed, b, layer)
+                        hv[b, layer, :, :, :w.t_past] = S.bf16_bits(pk).view(np.int16)
+                self.cache = G.KV(host.to(device).view(torch.bfloat16), w.t_past)
+        self.graph = None
+
+    # One step, inputs resident on the device.
+    def step(self):
+        G, w = self.G, self.w
+        if w.kind == "block":
+            G.gpt2_block_forward(self.ctx, self.x, self.params, w.B, w.T, w.d, w.n_head,
+                                 out=self.out)
+        elif w.kind == "forward":
+            G.gpt2_forward(self.ctx, self.ids, self.mp, w.B, w.T, logits=self.logits)
+        else:
+            self.cache.T_len = w.t_past
+            G.gpt2_forward(self.ctx, self.ids, self.mp, w.B, w.T, past=self.cache,
+                           present=self.cache, logits=self.logits)
+
+    def capture_graph(self):
+        torch = self.torch
+        self.step()  # first call outside capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step()
+        self.graph = g
+
+    def run(self):
+        if self.graph is not None:
+            self.graph.replay()
+        else:
+            self.step()
+
+    # One step end to end: pinned host inputs in, result back to pinned host.
+    def step_e2e(self):
+        w = self.w
+        if w.kind == "block":
+            self.x.copy_(self.x_host, non_blocking=True)
+            self.run()
+            self.out_host.copy_(self.out, non_blocking=True)
+        else:
+            self.ids.copy_(self.ids_host, non_blocking=True)
+            self.run()
+            self.logits_host.copy_(self.logits, non_blocking=True)
+
+    def e2e_bytes(self):
+        if self.w.kind == "block":
+            n = self.x.numel() * self.x.element_size()
+            return n, n
+        return self.ids.numel() * 4, self.logits.numel() * 4
+
+
+def timed_steps(fn, K, flush, barrier, torch):
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        starts[i].record()
+        fn()
+        ends[i].record()
+    torch.cuda.synchronize()
+    barrier()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+# -------------------------------------------------------------- CPU oracle --
+def oracle_sample(w: S.Workload, seed: int, T_sample: int):
+    """A bounded sample of the workload for the fp64 oracle: one sequence of
+    T_sample new tokens (block / forward), or one sequence's decode step.
+    Returns (callable, tokens)."""
+    from oracle import gpt2_oracle as O
+    if w.kind == "block":
+        p = S.block_params(w, seed)
+        x = S.block_input(w, seed)[:1, :T_sample]
+        return (lambda: O.block_forward(x, p, w.n_head)), T_sample
+    p = S.model_params(w, seed)
+    ids = S.token_ids(w, seed)[:1]
+    if w.kind == "forward":
+        ids = ids[:, :T_sample]
+        return (lambda: O.forward(ids, p, w.n_head)), T_sample
+    past = np.stack([S.past_kv(w, seed, 0, layer) for layer in range(w.n_layer)])[None]
+    return (lambda: O.forward(ids, p, w.n_head, past=past)), 1
+
+
+def time_oracle(w, seed, budget_s=15.0):
+    T_sample = w.T
+    fn, tokens = oracle_sample(w, seed, T_sample)
+    t0 = time.perf_counter()
+    fn()
+    one = time.perf_counter() - t0
+    reps = max(1, min(20, int(budget_s / max(one, 1e-3))))
+    if reps > 1:
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        one = (time.perf_counter() - t0) / reps
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+    sample = (f"1 sequence x {tokens} token(s) of {w.name}"
+              + (f" with a {w.t_past}-position cache" if w.kind == "decode" else "")
+              + f", {reps} repetition(s), fp64 numpy")
+    return {"value": tokens / one, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": sample}
+
+
+def reference_arm(args, w):
+    """The oracle as the reference arm: K timed steps of a bounded sample."""
+    T_s = w.T if w.kind != "decode" else 1
+    fn, tokens = oracle_sample(w, args.seed, T_s)
+    t0 = time.perf_counter()
+    fn()
+    one = time.perf_counter() - t0
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    if w.kind != "decode" and one > budget:
+        T_s = max(16, int(w.T * budget / one))
+        fn, tokens = oracle_sample(w, args.seed, T_s)
+    for _ in range(max(0, args.warmup - 1)):
+        fn()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        fn()
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = tokens / (ms / 1e3)
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
+    sample = f"1 sequence x {tokens} token(s) of {w.name} per step, fp64 numpy"
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, args),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def workload_config(w, args):
+    cfg = {"workload": w.name, "kind": w.kind, "d": w.d, "n_head": w.n_head, "B": w.B, "T": w.T,
+           "seed": args.seed, "l2": "flushed between steps (256 MiB device write)",
+           "parallelism": f"replicas x{args.gpus}"}
+    if w.kind != "block":
+        cfg.update(n_layer=w.n_layer, n_vocab=w.n_vocab)
+    if w.kind == "decode":
+        cfg.update(t_past=w.t_past, cuda_graph=True)
+    return cfg
+
+
+# --------------------------------------------------------------------- main --
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="block_bf16_d768", choices=sorted(S.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = S.WORKLOADS[args.workload]
+    ws, rank, local = dist_env()
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(reference_arm(args, w)), flush=True)
+        return 0
+
+    import torch
+    if args.warmup < 3:
+        args.warmup = 3
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    barrier = lambda: None  # noqa: E731
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+        barrier = lambda: dist.barrier()  # noqa: E731
+
+    from gpt_pre_norm_gb300 import binding as G
+    r = Runner(w, args.seed + rank, device)
+    if w.kind == "decode":
+        r.capture_graph()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    for _ in range(args.warmup):
+        r.run()
+    torch.cuda.synchronize()
+    st = G.gpt2_sync_status(r.ctx)
+    if st != G.GPT2_OK:
+        raise SystemExit(f"device error after warm-up: {G.status_string(st)}")
+
+    # Timed region: device-resident inputs.
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        times = timed_steps(r.run, args.steps, flush, barrier, torch)
+    ms = sum(times) / len(times)
+
+    # End to end through the C ABI: pinned host buffers, copies inside the step.
+    times_e2e = timed_steps(r.step_e2e, args.steps, flush, barrier, torch)
+    ms_e2e = sum(times_e2e) / len(times_e2e)
+
+    # Profiled pass: every kernel launch bracketed by events on its stream.
+    G.gpt2_profile_enable(r.ctx, True)
+    G.gpt2_profile_reset(r.ctx)
+    timed_steps(r.step, args.steps, flush, barrier, torch)
+    prof = G.gpt2_profile_read(r.ctx)
+    G.gpt2_profile_enable(r.ctx, False)
+    st = G.gpt2_sync_status(r.ctx)
+    if st != G.GPT2_OK:
+        raise SystemExit(f"device error in the timed region: {G.status_string(st)}")
+
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms, ms_e2e], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, ms_e2e = float(t[0]), float(t[1])
+    if rank != 0:
+        return 0
+
+    peaks = load_peaks()
+    tokens = r.tokens * ws
+    value = tokens / (ms / 1e3)
+    flops = workload_flops(w)
+    kernels = {}
+    for kind, rec in prof.items():
+        n = rec["launches"]
+        avg_s = rec["ms"] / 1e3 / n
+        entry = {"launches_per_step": n / args.steps, "ms_per_launch": rec["ms"] / n,
+                 "share": rec["ms"] / sum(x["ms"] for x in prof.values())}
+        if kind in TENSOR_KINDS and rec["flops"] > 0:
+            ach = rec["flops"] / n / avg_s / 1e12
+            entry.update(tflops=ach, frac=ach / peaks["bf16_tflops"])
+        elif rec["bytes"] > 0:
+            ach = rec["bytes"] / n / avg_s / 1e9
+            entry.update(gbs=ach, frac=ach / peaks["hbm_gbs"])
+        kernels[kind] = entry
+    top = max(prof, key=lambda k: prof[k]["ms"])
+    rec = prof[top]
+    n = rec["launches"]
+    avg_s = rec["ms"] / 1e3 / n
+    if top in TENSOR_KINDS:
+        achieved = rec["flops"] / n / avg_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    else:
+        achieved = rec["bytes"] / n / avg_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = top
+    roof["peak_source"] = peaks["source"]
+    roof["traffic"] = ncu_traffic(top, w.name)
+    roof["algorithmic_per_launch"] = rec["flops"] / n if top in TENSOR_KINDS else rec["bytes"] / n
+
+    h2d, d2h = r.e2e_bytes()
+    launches = sum(v["launches"] for v in prof.values())
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": workload_config(w, args),
+        "tflops": flops * ws / (ms / 1e3) / 1e12,
+        "tflops_frac_of_bf16_peak": flops * ws / (ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+        "roofline": roof,
+        "e2e": {"value": tokens / (ms_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(round(launches)),
+        "clocks": clk.summary(),
+        "kernels": kernels,
+    }
+    if not args.no_cpu_baseline and ws == 1:
+        line["cpu_baseline"] = time_oracle(w, args.seed)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,497 @@
+// attention.cu -- causal multi-head attention kernels.
+//
+// Computes, per sequence b and head, o_i = sum_{j <= p_i} softmax_j(q_i . k_j /
+// sqrt(d_h)) v_j with p_i = T_past + i the query's absolute position ("GPT-2
+// Block - TorchCode", "Reference Solution": scores, upper-triangular -inf
+// mask, softmax over keys, weights @ v; "GPT-2 Full Forward Pass", "How it
+// works": cached keys/values come first on the sequence axis).  Keys and
+// values are read from the KV cache the c_attn epilogue wrote; the output is
+// written with heads merged, [B, T, h * d_h].
+//
+//   attn_prefill_bf16   d_h = 64.  One CTA per (128-query tile, sequence x
+//                       head), 8 warps of 16 query rows.  Key/value tiles of 64
+//                       stream through a cp.async double buffer; S = Q K^T and
+//                       O += P V run on the tensor cores (mma.sync m16n8k16,
+//                       bf16 in, fp32 accumulate); softmax is online in
+//                       registers with exp2; tiles entirely above the diagonal
+//                       are never loaded, and the tiles with the most keys are
+//                       scheduled first.
+//   attn_decode_bf16    one new token: split over keys, 8 warps per CTA, each
+//                       8-lane group streams one key per step with 16-byte
+//                       loads; partial (max, sum, o) merged in shared memory,
+//                       and across CTAs by attn_decode_combine.
+//   attn_fp32           fp32 storage, any d_h <= 256, one warp per query.
+#include <math.h>
+
+#include <algorithm>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace gpt2 {
+
+namespace {
+
+constexpr int kDh = 64;
+constexpr int kQTile = 128;
+constexpr int kKTile = 64;
+constexpr int kAttnThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Byte offset of 16-byte chunk c of row r in a [rows x 64] bf16 tile whose
+// chunks are XOR-swizzled by the row's low three bits (conflict-free ldmatrix).
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 2)
+    attn_prefill_bf16(const bf16* __restrict__ q, const bf16* __restrict__ kv, long long s_batch,
+                      long long s_kv, long long s_head, int h, int T, int t_past,
+                      bf16* __restrict__ out, int n_qtiles) {
+  __shared__ __align__(128) uint8_t sQ[kQTile * 128];
+  __shared__ __align__(128) uint8_t sK[2][kKTile * 128];
+  __shared__ __align__(128) uint8_t sV[2][kKTile * 128];
+
+  const int bh = blockIdx.x;
+  const int qt = n_qtiles - 1 - static_cast<int>(blockIdx.y);  // most keys first
+  const int b = bh / h, head = bh - b * h;
+  const int q0 = qt * kQTile;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t_all = t_past + T;
+
+  const bf16* Qg = q + static_cast<size_t>(bh) * T * kDh;
+  const bf16* Kg = kv + b * s_batch + head * s_head;
+  const bf16* Vg = Kg + s_kv;
+
+  // Keys this tile needs: up to the last query row's position.
+  const int q_last = min(q0 + kQTile, T) - 1;
+  const int kv_len = t_past + q_last + 1;
+  const int n_kt = (kv_len + kKTile - 1) / kKTile;
+
+  const uint32_t sQa = smem_u32(sQ);
+  const uint32_t sKa[2] = {smem_u32(sK[0]), smem_u32(sK[1])};
+  const uint32_t sVa[2] = {smem_u32(sV[0]), smem_u32(sV[1])};
+
+  // Q tile: 128 rows x 8 chunks.
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int idx = tid + i * kAttnThreads;
+    const int r = idx >> 3, c = idx & 7;
+    const bool valid = q0 + r < T;
+    const bf16* src = Qg + static_cast<size_t>(valid ? q0 + r : 0) * kDh + c * 8;
+    cp_async_16(sQa + swz(r, c), src, valid);
+  }
+  auto load_kv = [&](int j, int buf) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int idx = tid + i * kAttnThreads;
+      const int r = idx >> 3, c = idx & 7;
+      const int key = j * kKTile + r;
+      const bool valid = key < t_all;
+      const size_t off = static_cast<size_t>(valid ? key : 0) * kDh + c * 8;
+      cp_async_16(sKa[buf] + swz(r, c), Kg + off, valid);
+      cp_async_16(sVa[buf] + swz(r, c), Vg + off, valid);
+    }
+  };
+  load_kv(0, 0);
+  cp_async_commit();
+
+  const int g = lane >> 2, tq = lane & 3;
+  const int row_lo = 16 * warp;                   // warp's first row in the tile
+  const int pos_lo = t_past + q0 + row_lo;        // its absolute position
+  const int pos_a = pos_lo + g, pos_b = pos_a + 8;
+  const float sl2 = 0.125f * kLog2e;              // 1/sqrt(64) in log2 units
+
+  uint32_t qf[4][4];
+  float o[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[i][j] = 0.f;
+  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+
+  for (int j = 0; j < n_kt; ++j) {
+    if (j + 1 < n_kt) load_kv(j + 1, (j + 1) & 1);
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();
+    if (j == 0) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        ldmatrix_x4(qf[kk], sQa + swz(row_lo + (lane & 15), 2 * kk + (lane >> 4)));
+    }
+    const int kbase = j * kKTile;
+    const int buf = j & 1;
+    if (kbase <= pos_lo + 15) {  // some key of this tile is visible to the warp
+      float s[8][4];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[i][e] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+        for (int np = 0; np < 4; ++np) {
+          uint32_t r[4];
+          ldmatrix_x4(r, sKa[buf] + swz(16 * np + ((lane >> 4) << 3) + (lane & 7),
+                                        2 * kk + ((lane >> 3) & 1)));
+          mma_bf16_16816(s[2 * np], qf[kk], r[0], r[1]);
+          mma_bf16_16816(s[2 * np + 1], qf[kk], r[2], r[3]);
+        }
+      }
+      if (kbase + kKTile - 1 > pos_lo) {  // the tile crosses this warp's diagonal
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+          const int key = kbase + 8 * nt + 2 * tq;
+          if (key > pos_a) s[nt][0] = -INFINITY;
+          if (key + 1 > pos_a) s[nt][1] = -INFINITY;
+          if (key > pos_b) s[nt][2] = -INFINITY;
+          if (key + 1 > pos_b) s[nt][3] = -INFINITY;
+        }
+      }
+      float mx_a = -INFINITY, mx_b = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        mx_a = fmaxf(mx_a, fmaxf(s[nt][0], s[nt][1]));
+        mx_b = fmaxf(mx_b, fmaxf(s[nt][2], s[nt][3]));
+      }
+      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+      const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+      const float base_a = (mn_a == -INFINITY) ? 0.f : mn_a * sl2;
+      const float base_b = (mn_b == -INFINITY) ? 0.f : mn_b * sl2;
+      const float alpha_a = ex2(m_a * sl2 - base_a), alpha_b = ex2(m_b * sl2 - base_b);
+      m_a = mn_a;
+      m_b = mn_b;
+      float sum_a = 0.f, sum_b = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        s[nt][0] = ex2(fmaf(s[nt][0], sl2, -base_a));
+        s[nt][1] = ex2(fmaf(s[nt][1], sl2, -base_a));
+        s[nt][2] = ex2(fmaf(s[nt][2], sl2, -base_b));
+        s[nt][3] = ex2(fmaf(s[nt][3], sl2, -base_b));
+        sum_a += s[nt][0] + s[nt][1];
+        sum_b += s[nt][2] + s[nt][3];
+      }
+      l_a = l_a * alpha_a + sum_a;
+      l_b = l_b * alpha_b + sum_b;
+#pragma unroll
+      for (int nd = 0; nd < 8; ++nd) {
+        o[nd][0] *= alpha_a;
+        o[nd][1] *= alpha_a;
+        o[nd][2] *= alpha_b;
+        o[nd][3] *= alpha_b;
+      }
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        uint32_t pa[4];
+        pa[0] = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
+        pa[1] = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
+        pa[2] = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+        pa[3] = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+#pragma unroll
+        for (int dp = 0; dp < 4; ++dp) {
+          uint32_t r[4];
+          ldmatrix_x4_trans(r, sVa[buf] + swz(16 * kk + (((lane >> 3) & 1) << 3) + (lane & 7),
+                                              2 * dp + (lane >> 4)));
+          mma_bf16_16816(o[2 * dp], pa, r[0], r[1]);
+          mma_bf16_16816(o[2 * dp + 1], pa, r[2], r[3]);
+        }
+      }
+    }
+    __syncthreads();  // buffer `buf` is refilled two iterations later
+  }
+  cp_async_wait<0>();
+
+  l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+  l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+  l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+  l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+  const float inv_a = 1.f / l_a, inv_b = 1.f / l_b;
+  const int d = h * kDh;
+  const int ra = q0 + row_lo + g, rb = ra + 8;
+  bf16* outb = out + static_cast<size_t>(b) * T * d + head * kDh + 2 * tq;
+#pragma unroll
+  for (int nd = 0; nd < 8; ++nd) {
+    if (ra < T)
+      *reinterpret_cast<uint32_t*>(outb + static_cast<size_t>(ra) * d + 8 * nd) =
+          pack_bf16x2(o[nd][0] * inv_a, o[nd][1] * inv_a);
+    if (rb < T)
+      *reinterpret_cast<uint32_t*>(outb + static_cast<size_t>(rb) * d + 8 * nd) =
+          pack_bf16x2(o[nd][2] * inv_b, o[nd][3] * inv_b);
+  }
+}
+
+// ------------------------------------------------------------------ decode --
+constexpr int kDecThreads = 256;
+constexpr int kDecWarps = kDecThreads / 32;
+constexpr int kPartialStride = kDh + 2;  // o[64], m, l
+
+__global__ void __launch_bounds__(kDecThreads)
+    attn_decode_bf16(const bf16* __restrict__ q, const bf16* __restrict__ kv, long long s_batch,
+                     long long s_kv, long long s_head, int h, int t_len, int chunk,
+                     bf16* __restrict__ out, float* __restrict__ partials) {
+  __shared__ float s_m[kDecWarps], s_l[kDecWarps];
+  __shared__ float s_o[kDecWarps][kDh];
+
+  const int split = blockIdx.x, splits = gridDim.x;
+  const int bh = blockIdx.y;
+  const int b = bh / h, head = bh - b * h;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = lane >> 3, sub = lane & 7;  // 4 groups of 8 lanes; 8 dims per lane
+
+  const int k_begin = split * chunk;
+  const int k_end = min(t_len, k_begin + chunk);
+  const int per_warp = (k_end - k_begin + kDecWarps - 1) / kDecWarps;
+  const int w_begin = k_begin + warp * per_warp;
+  const int w_end = min(k_end, w_begin + per_warp);
+
+  const bf16* Kg = kv + b * s_batch + head * s_head;
+  const bf16* Vg = Kg + s_kv;
+  const float sl2 = 0.125f * kLog2e;
+
+  float qv[8];
+  {
+    const uint4 qq = *reinterpret_cast<const uint4*>(q + static_cast<size_t>(bh) * kDh + sub * 8);
+    const uint32_t w[4] = {qq.x, qq.y, qq.z, qq.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      qv[2 * i] = bf16_lo(w[i]) * sl2;
+      qv[2 * i + 1] = bf16_hi(w[i]) * sl2;
+    }
+  }
+  float m = -INFINITY, l = 0.f, o[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i] = 0.f;
+
+  constexpr int kUnroll = 4;  // keys per group per step
+  for (int k0 = w_begin; k0 < w_end; k0 += 4 * kUnroll) {
+    uint4 kr[kUnroll], vr[kUnroll];
+    bool ok[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int key = k0 + u * 4 + grp;
+      ok[u] = key < w_end;
+      const size_t off = static_cast<size_t>(ok[u] ? key : w_begin) * kDh + sub * 8;
+      kr[u] = *reinterpret_cast<const uint4*>(Kg + off);
+      vr[u] = *reinterpret_cast<const uint4*>(Vg + off);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t kw[4] = {kr[u].x, kr[u].y, kr[u].z, kr[u].w};
+      float sc = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        sc = fmaf(qv[2 * i], bf16_lo(kw[i]), sc);
+        sc = fmaf(qv[2 * i + 1], bf16_hi(kw[i]), sc);
+      }
+      sc += __shfl_xor_sync(0xffffffffu, sc, 1);
+      sc += __shfl_xor_sync(0xffffffffu, sc, 2);
+      sc += __shfl_xor_sync(0xffffffffu, sc, 4);
+      if (!ok[u]) continue;
+      const float mn = fmaxf(m, sc);
+      const float alpha = ex2(m - mn);
+      const float p = ex2(sc - mn);
+      m = mn;
+      l = l * alpha + p;
+      const uint32_t vw[4] = {vr[u].x, vr[u].y, vr[u].z, vr[u].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        o[2 * i] = fmaf(p, bf16_lo(vw[i]), o[2 * i] * alpha);
+        o[2 * i + 1] = fmaf(p, bf16_hi(vw[i]), o[2 * i + 1] * alpha);
+      }
+    }
+  }
+  // Merge the four key groups of the warp (lanes sub, sub+8, sub+16, sub+24).
+#pragma unroll
+  for (int off = 8; off < 32; off <<= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+    const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
+    const float mn = fmaxf(m, m2);
+    const float a1 = (m == -INFINITY) ? 0.f : ex2(m - mn);
+    const float a2 = (m2 == -INFINITY) ? 0.f : ex2(m2 - mn);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float o2 = __shfl_xor_sync(0xffffffffu, o[i], off);
+      o[i] = o[i] * a1 + o2 * a2;
+    }
+    l = l * a1 + l2 * a2;
+    m = mn;
+  }
+  if (grp == 0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s_o[warp][sub * 8 + i] = o[i];
+    if (sub == 0) {
+      s_m[warp] = m;
+      s_l[warp] = l;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // Lane t owns dims 2t, 2t+1.
+    float mx = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) mx = fmaxf(mx, s_m[w]);
+    float lsum = 0.f, o0 = 0.f, o1 = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) {
+      const float a = (s_m[w] == -INFINITY) ? 0.f : ex2(s_m[w] - mx);
+      lsum += s_l[w] * a;
+      o0 += s_o[w][2 * lane] * a;
+      o1 += s_o[w][2 * lane + 1] * a;
+    }
+    if (splits == 1) {
+      const float inv = 1.f / lsum;
+      *reinterpret_cast<uint32_t*>(out + static_cast<size_t>(bh) * kDh + 2 * lane) =
+          pack_bf16x2(o0 * inv, o1 * inv);
+    } else {
+      float* pp = partials + (static_cast<size_t>(bh) * splits + split) * kPartialStride;
+      pp[2 * lane] = o0;
+      pp[2 * lane + 1] = o1;
+      if (lane == 0) {
+        pp[kDh] = mx;
+        pp[kDh + 1] = lsum;
+      }
+    }
+  }
+}
+
+// One warp per (sequence, head): merges the splits' partial results.
+__global__ void attn_decode_combine(const float* __restrict__ partials, int n_bh, int splits,
+                                    bf16* __restrict__ out) {
+  const int bh = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (bh >= n_bh) return;
+  const float* pp = partials + static_cast<size_t>(bh) * splits * kPartialStride;
+  float mx = -INFINITY;
+  for (int s = 0; s < splits; ++s) mx = fmaxf(mx, pp[s * kPartialStride + kDh]);
+  float lsum = 0.f, o0 = 0.f, o1 = 0.f;
+  for (int s = 0; s < splits; ++s) {
+    const float ms = pp[s * kPartialStride + kDh];
+    const float a = (ms == -INFINITY) ? 0.f : ex2(ms - mx);
+    lsum += pp[s * kPartialStride + kDh + 1] * a;
+    o0 += pp[s * kPartialStride + 2 * lane] * a;
+    o1 += pp[s * kPartialStride + 2 * lane + 1] * a;
+  }
+  const float inv = 1.f / lsum;
+  *reinterpret_cast<uint32_t*>(out + static_cast<size_t>(bh) * kDh + 2 * lane) =
+      pack_bf16x2(o0 * inv, o1 * inv);
+}
+
+// -------------------------------------------------------------------- fp32 --
+constexpr int kF32MaxPerLane = 8;  // d_h <= 256
+
+__global__ void attn_fp32(const float* __restrict__ q, const float* __restrict__ kv,
+                          long long s_batch, long long s_kv, long long s_head, int B, int h,
+                          int T, int t_past, int dh, float* __restrict__ out) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);  // (b, head, i)
+  const int lane = threadIdx.x & 31;
+  if (row >= B * h * T) return;
+  const int i = row % T;
+  const int bh = row / T;
+  const int b = bh / h, head = bh - b * h;
+  const float* qr = q + static_cast<size_t>(row) * dh;
+  const float* Kg = kv + b * s_batch + head * s_head;
+  const float* Vg = Kg + s_kv;
+  const float scale = 1.0f / sqrtf(static_cast<float>(dh));
+  float qv[kF32MaxPerLane], o[kF32MaxPerLane];
+#pragma unroll
+  for (int u = 0; u < kF32MaxPerLane; ++u) {
+    const int c = lane + 32 * u;
+    qv[u] = c < dh ? qr[c] : 0.f;
+    o[u] = 0.f;
+  }
+  float m = -INFINITY, l = 0.f;
+  const int p = t_past + i;
+  for (int j = 0; j <= p; ++j) {
+    float sc = 0.f;
+#pragma unroll
+    for (int u = 0; u < kF32MaxPerLane; ++u) {
+      const int c = lane + 32 * u;
+      if (c < dh) sc = fmaf(qv[u], Kg[static_cast<size_t>(j) * dh + c], sc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, off);
+    sc *= scale;
+    const float mn = fmaxf(m, sc);
+    const float alpha = expf(m - mn);
+    const float pj = expf(sc - mn);
+    l = l * alpha + pj;
+#pragma unroll
+    for (int u = 0; u < kF32MaxPerLane; ++u) {
+      const int c = lane + 32 * u;
+      if (c < dh) o[u] = o[u] * alpha + pj * Vg[static_cast<size_t>(j) * dh + c];
+    }
+    m = mn;
+  }
+  const int d = h * dh;
+  float* orow = out + (static_cast<size_t>(b) * T + i) * d + head * dh;
+#pragma unroll
+  for (int u = 0; u < kF32MaxPerLane; ++u) {
+    const int c = lane + 32 * u;
+    if (c < dh) orow[c] = o[u] / l;
+  }
+}
+
+}  // namespace
+
+int launch_attention_bf16(const bf16* q, const bf16* kv, long long s_batch, long long s_kv,
+                          long long s_head, int B, int h, int T, int t_past, bf16* out,
+                          cudaStream_t stream) {
+  if (B <= 0 || h <= 0 || T <= 0 || t_past < 0) return GPT2_ERR_INVALID_ARG;
+  const int n_qtiles = (T + kQTile - 1) / kQTile;
+  if (n_qtiles > 65535) return GPT2_ERR_UNSUPPORTED;
+  dim3 grid(B * h, n_qtiles);
+  attn_prefill_bf16<<<grid, kAttnThreads, 0, stream>>>(q, kv, s_batch, s_kv, s_head, h, T, t_past,
+                                                       out, n_qtiles);
+  return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+}
+
+size_t decode_partials_floats(int B, int h, int splits) {
+  return static_cast<size_t>(B) * h * splits * kPartialStride;
+}
+
+int decode_splits(int B, int h, int t_len, int num_sms) {
+  const int bh = B * h;
+  int splits = (2 * num_sms + bh - 1) / bh;         // about two CTAs per SM
+  splits = std::min(splits, (t_len + 255) / 256);   // at least 256 keys per split
+  return std::max(1, std::min(splits, 64));
+}
+
+int launch_decode_attention_bf16(const bf16* q, const bf16* kv, long long s_batch, long long s_kv,
+                                 long long s_head, int B, int h, int t_len, bf16* out,
+                                 float* partials, int splits, cudaStream_t stream,
+                                 int* launches) {
+  if (B <= 0 || h <= 0 || t_len <= 0 || splits <= 0 || splits > 65535) return GPT2_ERR_INVALID_ARG;
+  if (splits > 1 && partials == nullptr) return GPT2_ERR_INVALID_ARG;
+  const int chunk = (t_len + splits - 1) / splits;
+  dim3 grid(splits, B * h);
+  attn_decode_bf16<<<grid, kDecThreads, 0, stream>>>(q, kv, s_batch, s_kv, s_head, h, t_len, chunk,
+                                                     out, partials);
+  int n = 1;
+  if (splits > 1) {
+    const int n_bh = B * h;
+    attn_decode_combine<<<(n_bh + 7) / 8, 256, 0, stream>>>(partials, n_bh, splits, out);
+    ++n;
+  }
+  if (launches) *launches = n;
+  return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+}
+
+int launch_attention_fp32(const float* q, const float* kv, long long s_batch, long long s_kv,
+                          long long s_head, int B, int h, int T, int t_past, int d_h, float* out,
+                          cudaStream_t stream) {
+  if (B <= 0 || h <= 0 || T <= 0 || t_past < 0 || d_h <= 0 || d_h > 32 * kF32MaxPerLane)
+    return GPT2_ERR_INVALID_ARG;
+  const long long rows = static_cast<long long>(B) * h * T;
+  const int warps_per_block = 8;
+  const long long blocks = (rows + warps_per_block - 1) / warps_per_block;
+  if (blocks > 0x7fffffffLL) return GPT2_ERR_UNSUPPORTED;
+  attn_fp32<<<static_cast<unsigned>(blocks), 32 * warps_per_block, 0, stream>>>(
+      q, kv, s_batch, s_kv, s_head, B, h, T, t_past, d_h, out);
+  return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+}
+
+}  // namespace gpt2

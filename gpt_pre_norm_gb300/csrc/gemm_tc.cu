@@ -1,0 +1,409 @@
+// gemm_tc.cu -- tensor-core GEMM for sm_103a: C[M,N] = A[M,K] * W[N,K]^T,
+// bf16 operands, fp32 accumulation in tensor memory, fused epilogues.
+//
+// It computes the five Linear products of the GPT-2 forward ("GPT-2 Full
+// Forward Pass", "How it works": fused c_attn d->3d, attention c_proj, c_fc
+// d->4d, mlp c_proj, and the tied head LN_f(H) W_e^T), with the epilogues the
+// block needs: bias; bias + GELU (tanh form); bias + residual add ("GPT-2
+// Decoder Block", "How it works": x <- x + a, x <- x + m); the QKV split into
+// heads with the keys/values written straight into the KV cache; and fp32
+// logits with a ragged vocabulary tail.
+//
+// Design (one CTA per SM, persistent over output tiles of 128 x BN):
+//   warp 0      TMA producer: 128x64 A and BNx64 W boxes, 128-byte swizzle,
+//               into a ring of `stages` shared-memory slots (mbarrier pairs).
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=BN,
+//               K=16) x4 per slot into one of two TMEM accumulators.
+//   warp 2      allocates / frees 512 TMEM columns.
+//   warps 4-7   epilogue: tcgen05.ld of their 32 TMEM lanes, a transpose
+//               through shared memory so each warp stores whole row segments,
+//               then bias / GELU / residual / scatter and global stores.
+// Two accumulators let the epilogue of tile i overlap the mainloop of i+1.
+// Every mbarrier wait is bounded; a wait that runs out raises the context's
+// error word and the CTA drains its copies, frees TMEM and returns.
+#include <algorithm>
+#include <cstdio>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace gpt2 {
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;                       // one 128-byte swizzle row of bf16
+constexpr int kThreads = 256;
+constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB per A slot
+constexpr int kStageLd = 65;                  // epilogue staging row stride (floats)
+constexpr int kEpiStageFloats = 4 * 32 * kStageLd;
+constexpr int kMaxStages = 8;
+constexpr uint32_t kTmemCols = 512;           // two accumulators of up to 256 columns
+constexpr int kSmemLimit = 232448;            // 227 KB opt-in per CTA
+
+struct GemmArgs {
+  int M, N, K;
+  int BN;
+  int stages;
+  int num_m_blocks;
+  int num_tiles;
+  unsigned* err;
+  EpiParams ep;
+};
+
+__host__ __device__ inline size_t smem_bytes_for(int BN, int stages) {
+  return 1024 /* alignment slack */ + static_cast<size_t>(stages) * (kABytes + BN * kBK * 2) +
+         kEpiStageFloats * sizeof(float) + (2 * stages + 5) * sizeof(uint64_t) + 16;
+}
+
+template <int KIND>
+__device__ __forceinline__ void epilogue_chunk(const float* st, int row0, int M, int col0,
+                                               int lane, const GemmArgs& a) {
+  const EpiParams& ep = a.ep;
+  const int N = a.N;
+  if constexpr (KIND == kEpiLogits) {
+    float* out = static_cast<float*>(ep.out);
+    const int c0 = col0 + lane, c1 = col0 + 32 + lane;
+    const bool ok0 = c0 < N, ok1 = c1 < N;
+#pragma unroll 4
+    for (int r = 0; r < 32; ++r) {
+      const int row = row0 + r;
+      if (row >= M) break;
+      float* o = out + static_cast<size_t>(row) * ep.ldo;
+      if (ok0) o[c0] = st[r * kStageLd + lane];
+      if (ok1) o[c1] = st[r * kStageLd + 32 + lane];
+    }
+  } else {
+    // Two adjacent columns per lane; N is even for every bf16 product here.
+    const int n = col0 + 2 * lane;
+    const bool ok = n < N;
+    float b0 = 0.f, b1 = 0.f;
+    if (ok) {
+      const uint32_t bb = *reinterpret_cast<const uint32_t*>(static_cast<const bf16*>(ep.bias) + n);
+      b0 = bf16_lo(bb);
+      b1 = bf16_hi(bb);
+    }
+    if constexpr (KIND == kEpiQkv) {
+      // The whole 64-column chunk belongs to one of Q/K/V and one head.
+      const int which = col0 / ep.d;
+      const int head = (col0 - which * ep.d) >> 6;
+      const int h = ep.d >> 6;
+#pragma unroll 4
+      for (int r = 0; r < 32; ++r) {
+        const int row = row0 + r;
+        if (row >= M) break;
+        const int bi = row / ep.T, t = row - bi * ep.T;
+        bf16* dst;
+        if (which == 0) {
+          dst = static_cast<bf16*>(ep.q) + ((static_cast<size_t>(bi) * h + head) * ep.T + t) * 64;
+        } else {
+          dst = static_cast<bf16*>(ep.kv.base) + bi * ep.kv.s_batch + (which - 1) * ep.kv.s_kv +
+                head * ep.kv.s_head + static_cast<long long>(ep.kv.t_past + t) * 64;
+        }
+        const float v0 = st[r * kStageLd + 2 * lane] + b0;
+        const float v1 = st[r * kStageLd + 2 * lane + 1] + b1;
+        *reinterpret_cast<uint32_t*>(dst + 2 * lane) = pack_bf16x2(v0, v1);
+      }
+    } else {
+#pragma unroll 4
+      for (int r = 0; r < 32; ++r) {
+        const int row = row0 + r;
+        if (row >= M) break;
+        if (!ok) continue;
+        float v0 = st[r * kStageLd + 2 * lane] + b0;
+        float v1 = st[r * kStageLd + 2 * lane + 1] + b1;
+        const size_t off = static_cast<size_t>(row) * ep.ldo + n;
+        if constexpr (KIND == kEpiBias) {
+          *reinterpret_cast<uint32_t*>(static_cast<bf16*>(ep.out) + off) = pack_bf16x2(v0, v1);
+        } else if constexpr (KIND == kEpiGelu) {
+          *reinterpret_cast<uint32_t*>(static_cast<bf16*>(ep.out) + off) =
+              pack_bf16x2(gelu_tanh_approx(v0), gelu_tanh_approx(v1));
+        } else if constexpr (KIND == kEpiResidF32) {
+          const float2 rr = *reinterpret_cast<const float2*>(static_cast<const float*>(ep.resid) + off);
+          *reinterpret_cast<float2*>(static_cast<float*>(ep.out) + off) =
+              make_float2(rr.x + v0, rr.y + v1);
+        } else if constexpr (KIND == kEpiResidBf16In) {
+          const uint32_t rr = *reinterpret_cast<const uint32_t*>(static_cast<const bf16*>(ep.resid) + off);
+          *reinterpret_cast<float2*>(static_cast<float*>(ep.out) + off) =
+              make_float2(bf16_lo(rr) + v0, bf16_hi(rr) + v1);
+        } else if constexpr (KIND == kEpiResidBf16Out) {
+          const float2 rr = *reinterpret_cast<const float2*>(static_cast<const float*>(ep.resid) + off);
+          *reinterpret_cast<uint32_t*>(static_cast<bf16*>(ep.out) + off) =
+              pack_bf16x2(rr.x + v0, rr.y + v1);
+        }
+      }
+    }
+  }
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int BN = args.BN, S = args.stages;
+  const uint32_t b_bytes = static_cast<uint32_t>(BN) * kBK * 2;
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + static_cast<size_t>(S) * kABytes;
+  float* ep_stage = reinterpret_cast<float*>(sB + static_cast<size_t>(S) * b_bytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ep_stage + kEpiStageFloats);
+  uint64_t* full = bars;                 // [S]   TMA landed
+  uint64_t* empty = bars + S;            // [S]   slot consumed by the MMAs
+  uint64_t* tfull = bars + 2 * S;        // [2]   accumulator ready
+  uint64_t* tempty = bars + 2 * S + 2;   // [2]   accumulator drained
+  uint64_t* mma_done = bars + 2 * S + 4; // [1]   every issued MMA retired
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int KB = (args.K + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 4);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------- producer --
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    int last_parity[kMaxStages];
+    for (int s = 0; s < kMaxStages; ++s) last_parity[s] = -1;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
+      const int m_blk = tile % args.num_m_blocks, n_blk = tile / args.num_m_blocks;
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.err)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[stage], kABytes + b_bytes);
+        tma_load_2d(sA + static_cast<size_t>(stage) * kABytes, &tmA, &full[stage], kb * kBK,
+                    m_blk * kBM);
+        tma_load_2d(sB + static_cast<size_t>(stage) * b_bytes, &tmB, &full[stage], kb * kBK,
+                    n_blk * BN);
+        last_parity[stage] = static_cast<int>(phase);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok) {
+      // Drain: every copy already issued must land before the CTA exits.
+      for (int s = 0; s < S; ++s)
+        if (last_parity[s] >= 0)
+          mbar_wait_bounded(&full[s], static_cast<uint32_t>(last_parity[s]), nullptr, args.err);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------- MMA issuer --
+    const uint32_t idesc = umma_idesc_bf16(kBM, BN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t acc_par = static_cast<uint32_t>((it >> 1) & 1);
+      if (!mbar_wait_bounded(&tempty[acc], acc_par ^ 1u, abort_flag, args.err)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 256);
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t a_desc = sdesc_k_sw128(smem_u32(sA + static_cast<size_t>(stage) * kABytes));
+        const uint64_t b_desc = sdesc_k_sw128(smem_u32(sB + static_cast<size_t>(stage) * b_bytes));
+#pragma unroll
+        for (int k = 0; k < kBK / 16; ++k) {
+          // +32 bytes per 16-element K slice: +2 in the descriptor's address field.
+          umma_bf16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+        }
+        umma_commit(&empty[stage]);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (ok) umma_commit(&tfull[acc]);
+    }
+    // Every MMA issued above must retire before TMEM is freed.
+    umma_commit(mma_done);
+    mbar_wait_bounded(mma_done, 0, nullptr, args.err);
+  } else if (warp >= 4) {
+    // --------------------------------------------------------- epilogue --
+    const int ew = warp - 4;
+    float* st = ep_stage + ew * 32 * kStageLd;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t acc_par = static_cast<uint32_t>((it >> 1) & 1);
+      if (!mbar_wait_bounded(&tfull[acc], acc_par, abort_flag, args.err)) break;
+      tc_fence_after();
+      const int m_blk = tile % args.num_m_blocks, n_blk = tile / args.num_m_blocks;
+      const int row0 = m_blk * kBM + ew * 32;
+      const int n0 = n_blk * BN;
+      for (int c = 0; c < BN; c += 64) {
+        if (n0 + c >= args.N) break;
+        uint32_t r0[32], r1[32];
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
+                               static_cast<uint32_t>(acc * 256 + c);
+        tmem_ld_32x32b_x32(taddr, r0);
+        tmem_ld_32x32b_x32(taddr + 32, r1);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          st[lane * kStageLd + j] = __uint_as_float(r0[j]);
+          st[lane * kStageLd + 32 + j] = __uint_as_float(r1[j]);
+        }
+        __syncwarp();
+        epilogue_chunk<KIND>(st, row0, args.M, n0 + c, lane, args);
+        __syncwarp();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+template <int KIND>
+void* kernel_ptr() {
+  return reinterpret_cast<void*>(&gemm_tc_kernel<KIND>);
+}
+
+void* kernel_for(int kind) {
+  switch (kind) {
+    case kEpiBias: return kernel_ptr<kEpiBias>();
+    case kEpiGelu: return kernel_ptr<kEpiGelu>();
+    case kEpiResidF32: return kernel_ptr<kEpiResidF32>();
+    case kEpiResidBf16In: return kernel_ptr<kEpiResidBf16In>();
+    case kEpiResidBf16Out: return kernel_ptr<kEpiResidBf16Out>();
+    case kEpiLogits: return kernel_ptr<kEpiLogits>();
+    case kEpiQkv: return kernel_ptr<kEpiQkv>();
+    default: return nullptr;
+  }
+}
+
+bool encode_kmajor_bf16(const LaunchEnv& env, CUtensorMap* map, const void* base, int rows,
+                        int K, int box_rows) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = env.encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Tile width: the candidate minimising waves x (BN + 32): the busiest SM's
+// share of the work plus a per-tile cost (operand reloads, epilogue start),
+// preferring wider tiles on ties.
+int choose_bn(int M, int N, int num_sms) {
+  const int m_blocks = (M + kBM - 1) / kBM;
+  int best = 256;
+  long long best_cost = -1;
+  for (int bn : {256, 192, 128, 64}) {
+    const long long tiles = static_cast<long long>(m_blocks) * ((N + bn - 1) / bn);
+    const long long waves = (tiles + num_sms - 1) / num_sms;
+    const long long cost = waves * (bn + 32);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+}  // namespace
+
+int launch_gemm_tc(const LaunchEnv& env, int kind, const bf16* A, const bf16* W, int M, int N,
+                   int K, const EpiParams& ep, cudaStream_t stream, double* flops, double* bytes) {
+  void* fn = kernel_for(kind);
+  if (!fn) return GPT2_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0) return GPT2_ERR_INVALID_ARG;
+  if (K % 8 != 0) return GPT2_ERR_UNSUPPORTED;
+  if (kind != kEpiLogits && (N % 2 != 0)) return GPT2_ERR_UNSUPPORTED;
+  if (kind == kEpiQkv && (ep.d % 64 != 0 || N != 3 * ep.d)) return GPT2_ERR_UNSUPPORTED;
+
+  const int BN = choose_bn(M, N, env.num_sms);
+  int stages = kMaxStages;
+  while (stages > 2 && smem_bytes_for(BN, stages) > static_cast<size_t>(kSmemLimit)) --stages;
+  const size_t smem = smem_bytes_for(BN, stages);
+
+  CUtensorMap tmA, tmB;
+  if (!encode_kmajor_bf16(env, &tmA, A, M, K, kBM)) return GPT2_ERR_CUDA;
+  if (!encode_kmajor_bf16(env, &tmB, W, N, K, BN)) return GPT2_ERR_CUDA;
+
+  GemmArgs args;
+  args.M = M;
+  args.N = N;
+  args.K = K;
+  args.BN = BN;
+  args.stages = stages;
+  args.num_m_blocks = (M + kBM - 1) / kBM;
+  args.num_tiles = args.num_m_blocks * ((N + BN - 1) / BN);
+  args.err = env.err;
+  args.ep = ep;
+
+  // Set once per process (the opt-in limit does not depend on the call), so
+  // later calls make no non-stream CUDA call (safe under stream capture).
+  static bool attr_set[kEpiCount] = {};
+  if (!attr_set[kind]) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) !=
+        cudaSuccess)
+      return GPT2_ERR_CUDA;
+    attr_set[kind] = true;
+  }
+  const int grid = std::min(args.num_tiles, env.num_sms);
+  void* params[] = {&tmA, &tmB, &args};
+  if (cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), params, smem, stream) != cudaSuccess)
+    return GPT2_ERR_CUDA;
+
+  if (flops) *flops = 2.0 * M * N * static_cast<double>(K);
+  if (bytes) {
+    double b = 2.0 * (static_cast<double>(M) * K + static_cast<double>(N) * K);
+    const double mn = static_cast<double>(M) * N;
+    switch (kind) {
+      case kEpiBias: case kEpiGelu: case kEpiQkv: b += 2.0 * mn + 2.0 * N; break;
+      case kEpiResidF32: b += 8.0 * mn + 2.0 * N; break;
+      case kEpiResidBf16In: b += 6.0 * mn + 2.0 * N; break;
+      case kEpiResidBf16Out: b += 6.0 * mn + 2.0 * N; break;
+      case kEpiLogits: b += 4.0 * mn; break;
+    }
+    *bytes = b;
+  }
+  return GPT2_OK;
+}
+
+}  // namespace gpt2

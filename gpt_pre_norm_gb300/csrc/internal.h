@@ -1,0 +1,115 @@
+// internal.h -- declarations shared by the host orchestrator (gpt2_api.cu)
+// and the kernel launchers (gemm_tc.cu, attention.cu, rowwise.cu, simt_fp32.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gpt2.h"
+
+namespace gpt2 {
+
+typedef __nv_bfloat16 bf16;
+
+// Profiled kernel kinds (names returned by gpt2_profile_read).
+enum KernelKind : int {
+  kKindEmbed = 0,
+  kKindLayerNorm,
+  kKindGemmQkv,
+  kKindAttention,
+  kKindGemmProj,
+  kKindGemmFc,
+  kKindGemmMlpProj,
+  kKindGemmLogits,
+  kKindGemmOther,
+  kKindDecodeAttention,
+  kKindDecodeCombine,
+  kKindSimtFp32,
+  kKindCount
+};
+
+// Epilogues of the tensor-core GEMM.
+enum EpiKind : int {
+  kEpiBias = 0,       // out_bf16 = acc + bias
+  kEpiGelu,           // out_bf16 = gelu_tanh(acc + bias)
+  kEpiResidF32,       // out_f32  = resid_f32 + acc + bias
+  kEpiResidBf16In,    // out_f32  = resid_bf16 + acc + bias
+  kEpiResidBf16Out,   // out_bf16 = resid_f32 + acc + bias
+  kEpiLogits,         // out_f32  = acc (no bias, N tail masked)
+  kEpiQkv,            // acc + bias scattered to Q [B,h,T,64] and the K/V cache
+  kEpiCount
+};
+
+// Where c_attn's keys and values go: a cache laid out [.., 2, h, T_cap, 64]
+// with the element strides below (token stride = d_h).
+struct KvDst {
+  void* base;
+  long long s_batch;  // elements between sequences
+  long long s_kv;     // elements between the K and V halves
+  long long s_head;   // elements between heads (= T_cap * d_h)
+  int t_past;         // first position written
+};
+
+struct EpiParams {
+  const void* bias;         // [N], mode dtype
+  const void* resid;        // [M, ldo] (fp32 or bf16 by kind)
+  void* out;                // [M, ldo] (fp32 or bf16 by kind)
+  int ldo;                  // row stride of resid and out, elements
+  void* q;                  // Q destination [B, h, T, d_h] (kEpiQkv)
+  KvDst kv;                 // K/V destination (kEpiQkv)
+  int T;                    // tokens per sequence (kEpiQkv)
+  int d;                    // model width (kEpiQkv)
+};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// Per-device launch environment.
+struct LaunchEnv {
+  int num_sms;
+  unsigned* err;          // device error word
+  EncodeTiledFn encode;   // cuTensorMapEncodeTiled
+};
+
+// Tensor-core GEMM (bf16 in, fp32 accumulate in TMEM): C = A[M,K] W[N,K]^T
+// with epilogue `kind`.  Returns a gpt2_status.
+int launch_gemm_tc(const LaunchEnv& env, int kind, const bf16* A, const bf16* W, int M, int N,
+                   int K, const EpiParams& ep, cudaStream_t stream, double* flops, double* bytes);
+
+// fp32 SIMT GEMM with the same epilogues (fp32 storage throughout).
+int launch_gemm_fp32(const LaunchEnv& env, int kind, const float* A, const float* W, int M, int N,
+                     int K, const EpiParams& ep, int d_h, cudaStream_t stream);
+
+// LayerNorm rows of d: x fp32 or bf16 -> y bf16 (mode BF16) or fp32 (mode FP32).
+int launch_layer_norm(int mode, const void* x, int x_dtype, const void* g, const void* b, int rows,
+                      int d, void* y, cudaStream_t stream);
+
+// H[b,t,:] = wte[ids[b,t]] + wpe[t_past + t] -> fp32.
+int launch_embed(int mode, const int32_t* ids, const void* wte, const void* wpe, int B, int T,
+                 int t_past, int d, int n_vocab, float* H, unsigned* err, cudaStream_t stream);
+
+// Causal prefill attention, bf16, d_h = 64 (tensor cores).
+int launch_attention_bf16(const bf16* q, const bf16* kv, long long kv_s_batch, long long kv_s_kv,
+                          long long kv_s_head, int B, int h, int T, int t_past, bf16* out,
+                          cudaStream_t stream);
+
+// Single-token decode attention, bf16, d_h = 64: split over keys, partial
+// results combined through `partials` (floats, see decode_partials_floats).
+int launch_decode_attention_bf16(const bf16* q, const bf16* kv, long long kv_s_batch,
+                                 long long kv_s_kv, long long kv_s_head, int B, int h, int t_len,
+                                 bf16* out, float* partials, int splits, cudaStream_t stream,
+                                 int* launches);
+size_t decode_partials_floats(int B, int h, int splits);
+int decode_splits(int B, int h, int t_len, int num_sms);
+
+// fp32 attention (any d_h <= 256), with cache offset.
+int launch_attention_fp32(const float* q, const float* kv, long long kv_s_batch, long long kv_s_kv,
+                          long long kv_s_head, int B, int h, int T, int t_past, int d_h,
+                          float* out, cudaStream_t stream);
+
+}  // namespace gpt2

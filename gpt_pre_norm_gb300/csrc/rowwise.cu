@@ -1,0 +1,233 @@
+// rowwise.cu -- the memory-bound row kernels: LayerNorm (fused with the cast
+// of its output) and the embedding gather + position add.
+//
+// LayerNorm follows the openai/gpt-2 ``norm`` excerpt on the "GPT-2
+// Transformer block" page: over the feature axis u = mean(x), s = mean((x -
+// u)^2) (biased), y = (x - u) * rsqrt(s + eps) * g + b with eps = 1e-5 ("GPT-2
+// Decoder Block", "How it works").  One warp owns one row, keeps it in
+// registers, and reduces with shuffles: one read of x, one write of y.
+//
+// The embedding follows "GPT-2 Full Forward Pass", "How it works":
+// H0[b, t] = wte[ids[b, t]] + wpe[T_past + t], written in fp32 (the residual
+// stream).  One warp per token, 16-byte loads.
+#include "device.cuh"
+#include "internal.h"
+
+namespace gpt2 {
+
+namespace {
+
+constexpr float kLnEps = 1e-5f;
+constexpr int kRowThreads = 256;
+constexpr int kRowsPerBlock = kRowThreads / 32;
+
+__device__ __forceinline__ void load2(const float* p, float& a, float& b) {
+  const float2 v = *reinterpret_cast<const float2*>(p);
+  a = v.x;
+  b = v.y;
+}
+__device__ __forceinline__ void load2(const bf16* p, float& a, float& b) {
+  const uint32_t v = *reinterpret_cast<const uint32_t*>(p);
+  a = bf16_lo(v);
+  b = bf16_hi(v);
+}
+__device__ __forceinline__ void store2(float* p, float a, float b) {
+  *reinterpret_cast<float2*>(p) = make_float2(a, b);
+}
+__device__ __forceinline__ void store2(bf16* p, float a, float b) {
+  *reinterpret_cast<uint32_t*>(p) = pack_bf16x2(a, b);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// Row held in registers: NP pairs per lane, d <= 64 * NP, d even.
+template <typename TX, typename TY, int NP>
+__global__ void __launch_bounds__(kRowThreads)
+    layer_norm_reg(const TX* __restrict__ x, const TY* __restrict__ g, const TY* __restrict__ b,
+                   int rows, int d, TY* __restrict__ y) {
+  const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const TX* xr = x + static_cast<size_t>(row) * d;
+  float v[2 * NP];
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < NP; ++i) {
+    const int c = 2 * (lane + 32 * i);
+    if (c < d) {
+      load2(xr + c, v[2 * i], v[2 * i + 1]);
+    } else {
+      v[2 * i] = v[2 * i + 1] = 0.f;
+    }
+    sum += v[2 * i] + v[2 * i + 1];
+  }
+  const float inv_d = 1.0f / static_cast<float>(d);
+  const float u = warp_sum(sum) * inv_d;
+  float sq = 0.f;
+#pragma unroll
+  for (int i = 0; i < NP; ++i) {
+    const int c = 2 * (lane + 32 * i);
+    if (c < d) {
+      const float a0 = v[2 * i] - u, a1 = v[2 * i + 1] - u;
+      sq = fmaf(a0, a0, fmaf(a1, a1, sq));
+    }
+  }
+  const float s = warp_sum(sq) * inv_d;
+  const float rstd = rsqrtf(s + kLnEps);
+  TY* yr = y + static_cast<size_t>(row) * d;
+#pragma unroll
+  for (int i = 0; i < NP; ++i) {
+    const int c = 2 * (lane + 32 * i);
+    if (c < d) {
+      float g0, g1, b0, b1;
+      load2(g + c, g0, g1);
+      load2(b + c, b0, b1);
+      store2(yr + c, (v[2 * i] - u) * rstd * g0 + b0, (v[2 * i + 1] - u) * rstd * g1 + b1);
+    }
+  }
+}
+
+__device__ __forceinline__ float ld1(const float* p) { return *p; }
+__device__ __forceinline__ float ld1(const bf16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void st1(float* p, float v) { *p = v; }
+__device__ __forceinline__ void st1(bf16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+// Any d: three passes over the row in global memory.
+template <typename TX, typename TY>
+__global__ void __launch_bounds__(kRowThreads)
+    layer_norm_any(const TX* __restrict__ x, const TY* __restrict__ g, const TY* __restrict__ b,
+                   int rows, int d, TY* __restrict__ y) {
+  const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const TX* xr = x + static_cast<size_t>(row) * d;
+  float sum = 0.f;
+  for (int c = lane; c < d; c += 32) sum += ld1(xr + c);
+  const float u = warp_sum(sum) / static_cast<float>(d);
+  float sq = 0.f;
+  for (int c = lane; c < d; c += 32) {
+    const float a = ld1(xr + c) - u;
+    sq = fmaf(a, a, sq);
+  }
+  const float rstd = rsqrtf(warp_sum(sq) / static_cast<float>(d) + kLnEps);
+  TY* yr = y + static_cast<size_t>(row) * d;
+  for (int c = lane; c < d; c += 32) st1(yr + c, (ld1(xr + c) - u) * rstd * ld1(g + c) + ld1(b + c));
+}
+
+template <typename TX, typename TY>
+int ln_dispatch(const TX* x, const TY* g, const TY* b, int rows, int d, TY* y, cudaStream_t s) {
+  const unsigned blocks = static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock);
+  if (d % 2 == 0 && d <= 64 * 4) {
+    layer_norm_reg<TX, TY, 4><<<blocks, kRowThreads, 0, s>>>(x, g, b, rows, d, y);
+  } else if (d % 2 == 0 && d <= 64 * 12) {
+    layer_norm_reg<TX, TY, 12><<<blocks, kRowThreads, 0, s>>>(x, g, b, rows, d, y);
+  } else if (d % 2 == 0 && d <= 64 * 16) {
+    layer_norm_reg<TX, TY, 16><<<blocks, kRowThreads, 0, s>>>(x, g, b, rows, d, y);
+  } else if (d % 2 == 0 && d <= 64 * 25) {
+    layer_norm_reg<TX, TY, 25><<<blocks, kRowThreads, 0, s>>>(x, g, b, rows, d, y);
+  } else {
+    layer_norm_any<TX, TY><<<blocks, kRowThreads, 0, s>>>(x, g, b, rows, d, y);
+  }
+  return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- embed ----
+__device__ __forceinline__ int checked_id(const int32_t* ids, size_t i, int n_vocab, unsigned* err) {
+  int id = ids[i];
+  if (id < 0 || id >= n_vocab) {
+    raise_error(err, kErrBadToken);
+    id = id < 0 ? 0 : n_vocab - 1;
+  }
+  return id;
+}
+
+__global__ void __launch_bounds__(kRowThreads)
+    embed_bf16(const int32_t* __restrict__ ids, const bf16* __restrict__ wte,
+               const bf16* __restrict__ wpe, int rows, int T, int t_past, int d, int n_vocab,
+               float* __restrict__ H, unsigned* err) {
+  const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const int id = checked_id(ids, row, n_vocab, err);
+  const int pos = t_past + row % T;
+  const bf16* e = wte + static_cast<size_t>(id) * d;
+  const bf16* p = wpe + static_cast<size_t>(pos) * d;
+  float* h = H + static_cast<size_t>(row) * d;
+  for (int c = lane * 8; c < d; c += 32 * 8) {  // d % 8 == 0
+    const uint4 ev = *reinterpret_cast<const uint4*>(e + c);
+    const uint4 pv = *reinterpret_cast<const uint4*>(p + c);
+    const uint32_t ew[4] = {ev.x, ev.y, ev.z, ev.w};
+    const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
+    float4 lo, hi;
+    lo.x = bf16_lo(ew[0]) + bf16_lo(pw[0]);
+    lo.y = bf16_hi(ew[0]) + bf16_hi(pw[0]);
+    lo.z = bf16_lo(ew[1]) + bf16_lo(pw[1]);
+    lo.w = bf16_hi(ew[1]) + bf16_hi(pw[1]);
+    hi.x = bf16_lo(ew[2]) + bf16_lo(pw[2]);
+    hi.y = bf16_hi(ew[2]) + bf16_hi(pw[2]);
+    hi.z = bf16_lo(ew[3]) + bf16_lo(pw[3]);
+    hi.w = bf16_hi(ew[3]) + bf16_hi(pw[3]);
+    *reinterpret_cast<float4*>(h + c) = lo;
+    *reinterpret_cast<float4*>(h + c + 4) = hi;
+  }
+}
+
+__global__ void __launch_bounds__(kRowThreads)
+    embed_fp32(const int32_t* __restrict__ ids, const float* __restrict__ wte,
+               const float* __restrict__ wpe, int rows, int T, int t_past, int d, int n_vocab,
+               float* __restrict__ H, unsigned* err) {
+  const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const int id = checked_id(ids, row, n_vocab, err);
+  const int pos = t_past + row % T;
+  const float* e = wte + static_cast<size_t>(id) * d;
+  const float* p = wpe + static_cast<size_t>(pos) * d;
+  float* h = H + static_cast<size_t>(row) * d;
+  for (int c = lane; c < d; c += 32) h[c] = e[c] + p[c];
+}
+
+}  // namespace
+
+int launch_layer_norm(int mode, const void* x, int x_dtype, const void* g, const void* b, int rows,
+                      int d, void* y, cudaStream_t stream) {
+  if (rows <= 0 || d <= 0) return GPT2_ERR_INVALID_ARG;
+  if (mode == GPT2_BF16) {
+    if (d % 2 != 0) return GPT2_ERR_UNSUPPORTED;
+    if (x_dtype == GPT2_FP32)
+      return ln_dispatch(static_cast<const float*>(x), static_cast<const bf16*>(g),
+                         static_cast<const bf16*>(b), rows, d, static_cast<bf16*>(y), stream);
+    if (x_dtype == GPT2_BF16)
+      return ln_dispatch(static_cast<const bf16*>(x), static_cast<const bf16*>(g),
+                         static_cast<const bf16*>(b), rows, d, static_cast<bf16*>(y), stream);
+    return GPT2_ERR_INVALID_ARG;
+  }
+  if (mode == GPT2_FP32 && x_dtype == GPT2_FP32)
+    return ln_dispatch(static_cast<const float*>(x), static_cast<const float*>(g),
+                       static_cast<const float*>(b), rows, d, static_cast<float*>(y), stream);
+  return GPT2_ERR_INVALID_ARG;
+}
+
+int launch_embed(int mode, const int32_t* ids, const void* wte, const void* wpe, int B, int T,
+                 int t_past, int d, int n_vocab, float* H, unsigned* err, cudaStream_t stream) {
+  if (B <= 0 || T <= 0 || d <= 0 || n_vocab <= 0) return GPT2_ERR_INVALID_ARG;
+  const int rows = B * T;
+  const unsigned blocks = static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock);
+  if (mode == GPT2_BF16) {
+    if (d % 8 != 0) return GPT2_ERR_UNSUPPORTED;
+    embed_bf16<<<blocks, kRowThreads, 0, stream>>>(ids, static_cast<const bf16*>(wte),
+                                                   static_cast<const bf16*>(wpe), rows, T, t_past,
+                                                   d, n_vocab, H, err);
+  } else {
+    embed_fp32<<<blocks, kRowThreads, 0, stream>>>(ids, static_cast<const float*>(wte),
+                                                   static_cast<const float*>(wpe), rows, T, t_past,
+                                                   d, n_vocab, H, err);
+  }
+  return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+}
+
+}  // namespace gpt2

@@ -1,0 +1,227 @@
+/*
+ * gpt2.h -- C ABI of the GB300 (sm_103a) GPT-2 pre-norm forward library.
+ *
+ * The library computes the GPT-2 pre-norm decoder block, the full uncached
+ * forward (embedding, L blocks, final LayerNorm, tied head) and cached decode,
+ * with hand-written CUDA kernels.  Every function takes plain pointers and
+ * sizes; device pointers are CUDA device addresses owned by the caller.
+ *
+ * Sources (web pages, by title and section):
+ *   "GPT-2 Decoder Block" (AI Engineer Exhaustive), "How it works": the block
+ *       a = Attn(LN1(x)); x += a; m = MLP(LN2(x)); x += m, LN eps 1e-5,
+ *       n_head heads of width d/n_head, a 4d GELU MLP, present returned.
+ *   "GPT-2 Full Forward Pass" (AI Engineer Exhaustive), "How it works":
+ *       H0 = gather(W_e, X) + gather(W_p, pos(X, l_past)); L blocks; ln_f;
+ *       logits = LN_f(H) W_e^T; fused c_attn to 3d; past [B, 2, h, T_past,
+ *       d_h] per layer concatenated on the sequence axis; present stacked as
+ *       [B, L, 2, h, T, d_h]; positions stay below n_ctx.
+ *   "GPT-2 Transformer block" (open-model-atlas), openai/gpt-2 ``norm``
+ *       excerpt: u = mean(x), s = mean((x-u)^2), (x-u) rsqrt(s+eps) g + b.
+ *   "GPT-2 Block - TorchCode", "Reference Solution": scores q k^T/sqrt(d_k),
+ *       upper-triangular -inf mask, softmax over keys, weights @ v.
+ *   "Decoder-only" (CodeBlanks): pre-LN loop and the tied head.
+ *
+ * Conventions common to every entry point:
+ *   - Return value: a gpt2_status.  On any validation error nothing is
+ *     launched and no memory is touched.  Errors raised inside a kernel
+ *     (a bounded wait that ran out) surface at gpt2_sync_status.
+ *   - Asynchrony: work is enqueued on `stream` (a cudaStream_t value; NULL is
+ *     the legacy default stream) and the call returns before it completes.
+ *   - Dtypes: in GPT2_BF16 mode activations, parameters and the KV cache are
+ *     bf16 (stored as 16-bit words) and every product accumulates in fp32; in
+ *     GPT2_FP32 mode they are fp32.  Logits are always fp32.  Token ids are
+ *     int32.  The residual stream inside gpt2_forward is fp32 in both modes.
+ *   - Layouts are dense row-major C order.  Linear weights are [out, in]
+ *     (the nn.Linear convention); c_attn rows are Q | K | V, head j taking
+ *     rows [j*d_h, (j+1)*d_h) of each block.
+ *   - Alignment: every device pointer must be 16-byte aligned.
+ *   - Shapes: BF16 mode needs d_h = d / n_head = 64; FP32 mode needs only
+ *     d % n_head == 0 and d_h <= 256.  T_past + T <= n_ctx.
+ *   - Ownership: the caller owns every buffer, including the workspace it
+ *     hands to gpt2_ctx_create; the library frees nothing it did not create.
+ */
+#ifndef GPT2_H
+#define GPT2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GPT2_OK = 0,
+  GPT2_ERR_INVALID_ARG = 1,    /* null pointer, non-positive size, bad enum */
+  GPT2_ERR_UNSUPPORTED = 2,    /* shape the chosen mode does not implement */
+  GPT2_ERR_CTX_OVERFLOW = 3,   /* T_past + T > n_ctx, or a cache too small */
+  GPT2_ERR_ALIGNMENT = 4,      /* a device pointer not 16-byte aligned */
+  GPT2_ERR_CUDA = 5,           /* a CUDA runtime call failed */
+  GPT2_ERR_DEVICE_TIMEOUT = 6, /* a kernel's bounded wait ran out */
+  GPT2_ERR_WORKSPACE = 7,      /* workspace too small for the request */
+  GPT2_ERR_NO_DEVICE = 8       /* no sm_100-family GPU is current */
+} gpt2_status;
+
+typedef enum { GPT2_BF16 = 0, GPT2_FP32 = 1 } gpt2_dtype;
+
+/* Model hyper-parameters (default_hparams of the official code, as the Full
+ * Forward Pass page names them).  dtype is a gpt2_dtype. */
+typedef struct {
+  int n_vocab, n_ctx, n_embd, n_head, n_layer;
+  int dtype;
+} gpt2_hparams;
+
+/* One block's parameters, device pointers in the mode's dtype:
+ *   ln1_g, ln1_b, ln2_g, ln2_b   [d]
+ *   attn_w [3d, d], attn_b [3d]   c_attn (Q | K | V)
+ *   proj_w [d, d],  proj_b [d]    attention c_proj
+ *   fc_w   [4d, d], fc_b   [4d]   mlp c_fc
+ *   mlp_proj_w [d, 4d], mlp_proj_b [d]   mlp c_proj                       */
+typedef struct {
+  const void *ln1_g, *ln1_b, *attn_w, *attn_b, *proj_w, *proj_b;
+  const void *ln2_g, *ln2_b, *fc_w, *fc_b, *mlp_proj_w, *mlp_proj_b;
+} gpt2_block_params;
+
+/* Whole-model parameters: wte [n_vocab, d], wpe [n_ctx, d], lnf_g/lnf_b [d]
+ * (device, mode dtype); blocks is a HOST array of n_layer block records.   */
+typedef struct {
+  const void *wte, *wpe, *lnf_g, *lnf_b;
+  const gpt2_block_params *blocks;
+} gpt2_params;
+
+/* A KV cache.  data is device memory of shape
+ *   [B, L, 2, h, T_cap, d_h]  for gpt2_forward (L = n_layer), or
+ *   [B, 2, h, T_cap, d_h]     for gpt2_block_forward,
+ * index 0 of the "2" axis holding keys and 1 values.  Positions
+ * [0, T_len) are valid.  This is the pages' past/present layout with the
+ * sequence axis allocated to a capacity T_cap >= T_len.                   */
+typedef struct {
+  void *data;
+  int T_cap;
+  int T_len;
+} gpt2_kv;
+
+typedef struct gpt2_ctx gpt2_ctx;
+
+/* ------------------------------------------------------------ context ---- */
+
+/* Bytes of device workspace a context needs for batches of up to max_B
+ * sequences of up to max_T new tokens with hyper-parameters *hp.          */
+int gpt2_workspace_bytes(const gpt2_hparams *hp, int max_B, int max_T, size_t *bytes);
+
+/* Creates a context on the current CUDA device.  workspace: caller-owned
+ * device memory of at least gpt2_workspace_bytes bytes, 256-byte aligned,
+ * which the context uses for intermediates and its device error word until
+ * it is destroyed.  *out receives the context (host memory the library owns).
+ * Errors: INVALID_ARG, UNSUPPORTED (shape the dtype cannot run),
+ * WORKSPACE (too small), NO_DEVICE, CUDA.                                   */
+int gpt2_ctx_create(const gpt2_hparams *hp, int max_B, int max_T, void *workspace,
+                    size_t workspace_bytes, gpt2_ctx **out);
+
+/* Releases the context's host state and CUDA events.  The workspace stays
+ * the caller's.  NULL is accepted.                                         */
+void gpt2_ctx_destroy(gpt2_ctx *ctx);
+
+/* Waits for `stream`, then reads and clears the context's device error
+ * word: GPT2_OK, GPT2_ERR_DEVICE_TIMEOUT, or GPT2_ERR_CUDA for a failed
+ * launch or an asynchronous CUDA error.                                    */
+int gpt2_sync_status(gpt2_ctx *ctx, void *stream);
+
+/* Static description of a status code. */
+const char *gpt2_status_string(int status);
+
+/* ------------------------------------------------------------ forward ---- */
+
+/* One pre-norm decoder block ("GPT-2 Decoder Block", "How it works"):
+ *   a = c_proj(causal_MHA(c_attn(LN1(x)))); x += a;
+ *   m = mlp_proj(GELU_tanh(c_fc(LN2(x)))); out = x + m.
+ * x, out: device [B, T, d] in the mode dtype (out may equal x).
+ * params: host pointer to device parameter pointers.  d, n_head must equal
+ * the context's n_embd, n_head.
+ * past: NULL (no cache) or a [B, 2, h, T_cap, d_h] cache holding T_past =
+ * past->T_len positions; the queries sit at positions T_past .. T_past+T-1
+ * and see every cached and new key at or before their own position.
+ * present: NULL (keys/values are not returned) or a cache that receives all
+ * T_past + T positions; present->T_len is set to T_past + T when the call is
+ * enqueued.  present->data == past->data appends in place; otherwise the
+ * past positions are copied into present first.
+ * Errors: INVALID_ARG, UNSUPPORTED, CTX_OVERFLOW (T_past + T > n_ctx or
+ * > present->T_cap), ALIGNMENT, WORKSPACE (B*T beyond the context's sizing),
+ * CUDA.                                                                    */
+int gpt2_block_forward(gpt2_ctx *ctx, const void *x, const gpt2_block_params *params, int B, int T,
+                       int d, int n_head, const gpt2_kv *past, gpt2_kv *present, void *out,
+                       void *stream);
+
+/* The full forward ("GPT-2 Full Forward Pass", "How it works"):
+ * H = wte[ids] + wpe[T_past + t]; L blocks; logits = LN_f(H) wte^T.
+ * ids: device int32 [B, T], each in [0, n_vocab).
+ * params: host pointer; L must equal the context's n_layer.
+ * past / present: NULL or [B, L, 2, h, T_cap, d_h] caches as above.
+ * logits: device fp32 [B, T, n_vocab] (exactly n_vocab columns, no bias).
+ * Out-of-range token ids are clamped into range on the device and reported
+ * as GPT2_ERR_INVALID_ARG by gpt2_sync_status.
+ * Errors: as gpt2_block_forward.                                            */
+int gpt2_forward(gpt2_ctx *ctx, const int32_t *ids, int B, int T, const gpt2_params *params, int L,
+                 const gpt2_kv *past, gpt2_kv *present, float *logits, void *stream);
+
+/* ------------------------------------------------- single operations ---- */
+/* The steps of the forward, exposed one by one so each kernel can be checked
+ * and timed alone.  All pointers are device pointers.                      */
+
+/* LayerNorm over the last axis (openai/gpt-2 ``norm`` excerpt, eps 1e-5,
+ * biased variance): y = (x - u) rsqrt(s + eps) g + b for `rows` rows of d.
+ * x_dtype: dtype of x (GPT2_FP32 or GPT2_BF16); g, b, y: mode dtype.      */
+int gpt2_layer_norm(int mode, const void *x, int x_dtype, const void *g, const void *b, int rows,
+                    int d, void *y, void *stream);
+
+typedef enum {
+  GPT2_EPI_BIAS = 0,       /* out = A W^T + bias                     (mode dtype) */
+  GPT2_EPI_BIAS_GELU = 1,  /* out = gelu_tanh(A W^T + bias)          (mode dtype) */
+  GPT2_EPI_BIAS_RESID = 2, /* out = resid + A W^T + bias             (fp32 resid/out) */
+  GPT2_EPI_LOGITS = 3      /* out = A W^T, no bias                   (fp32 out) */
+} gpt2_epilogue;
+
+/* Linear layer C[M, N] = A[M, K] W[N, K]^T with a fused epilogue (the c_attn
+ * / c_proj / c_fc / mlp c_proj / tied-head products of the Full Forward Pass
+ * page).  A, W: mode dtype.  bias [N] (ignored for LOGITS).  resid and out
+ * are [M, N]; resid may equal out.  K must be a multiple of 8.            */
+int gpt2_linear(gpt2_ctx *ctx, int epilogue, const void *A, const void *W, const void *bias,
+                const float *resid, void *out, int M, int N, int K, void *stream);
+
+/* Causal multi-head attention ("GPT-2 Block - TorchCode", "Reference
+ * Solution", with the cache offset of the Full Forward Pass page).
+ * q: [B, h, T, d_h]; kv: [B, 2, h, T_cap, d_h] holding T_past + T valid
+ * positions (the new keys/values already appended); out: [B, T, h*d_h]
+ * (heads merged).  Mode dtype throughout.  T == 1 with T_past > 0 takes the
+ * split-KV decode kernel.                                                 */
+int gpt2_attention(gpt2_ctx *ctx, const void *q, const void *kv, int B, int n_head, int T,
+                   int T_past, int T_cap, int d_h, void *out, void *stream);
+
+/* Embedding: H[b, t] = wte[ids[b, t]] + wpe[T_past + t] (fp32 out [B, T, d]).
+ * wte [n_vocab, d], wpe [n_ctx, d] in the mode dtype.                      */
+int gpt2_embed(gpt2_ctx *ctx, const int32_t *ids, const void *wte, const void *wpe, int B, int T,
+               int T_past, float *H, void *stream);
+
+/* ---------------------------------------------------------- profiling ---- */
+
+/* When enabled, every kernel launch the context makes is bracketed by CUDA
+ * events on its stream; the per-kernel totals accumulate until read.      */
+int gpt2_profile_enable(gpt2_ctx *ctx, int enable);
+
+/* Number of kernel kinds the profiler distinguishes. */
+int gpt2_profile_kinds(void);
+
+/* Waits for the recorded events and returns, for kernel kind `kind`, its
+ * name, the number of launches, their summed duration in ms and the summed
+ * algorithmic flops and bytes of those launches.                          */
+int gpt2_profile_read(gpt2_ctx *ctx, int kind, const char **name, long long *launches,
+                      double *total_ms, double *flops, double *bytes);
+
+/* Clears the accumulated profile. */
+int gpt2_profile_reset(gpt2_ctx *ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GPT2_H */

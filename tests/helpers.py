@@ -1,0 +1,60 @@
+"""Shared helpers of the GPU parity tests: device transfer and the tolerances.
+
+Tolerances (fixed for the whole suite):
+  fp32 mode  max |gpu - oracle| <= 1e-4 * max(1, |oracle|), element-wise;
+  bf16 mode  relative L2 error ||gpu - oracle|| / ||oracle|| <= 1e-2 per output
+             tensor, and for full-model logits the argmax agrees at >= 99% of
+             positions.
+"""
+import numpy as np
+import torch
+
+FP32_TOL = 1e-4
+BF16_REL_L2 = 1e-2
+ARGMAX_AGREE = 0.99
+
+
+def dev(a: np.ndarray, dtype=torch.bfloat16) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a)).to("cuda", dtype)
+
+
+def host(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def rel_l2(got, ref) -> float:
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+def assert_bf16_close(got, ref, tol=BF16_REL_L2, what=""):
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    e = rel_l2(got, ref)
+    assert e <= tol, f"{what}: relative L2 error {e:.3e} > {tol:.1e}"
+    return e
+
+
+def assert_fp32_close(got, ref, tol=FP32_TOL, what=""):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.abs(got - ref) / np.maximum(1.0, np.abs(ref))
+    assert float(err.max()) <= tol, f"{what}: max scaled error {float(err.max()):.3e} > {tol:.1e}"
+    return float(err.max())
+
+
+def argmax_agreement(got_logits, ref_logits) -> float:
+    g = np.argmax(np.asarray(got_logits), axis=-1)
+    r = np.argmax(np.asarray(ref_logits), axis=-1)
+    return float(np.mean(g == r))
+
+
+def block_to_device(p: dict, dtype=torch.bfloat16) -> dict:
+    return {k: dev(v, dtype) for k, v in p.items()}
+
+
+def model_to_device(p: dict, dtype=torch.bfloat16) -> dict:
+    out = {k: dev(p[k], dtype) for k in ("wte", "wpe", "lnf_g", "lnf_b")}
+    out["blocks"] = [block_to_device(b, dtype) for b in p["blocks"]]
+    return out

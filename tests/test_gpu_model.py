@@ -1,0 +1,180 @@
+"""Block, full forward and cached decode through the C ABI vs the fp64 oracle
+(small, fast cases: several tiles and ragged tails; error paths)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import gpt2_oracle as O
+from gpt_pre_norm_gb300 import synthetic as S
+from tests.helpers import (ARGMAX_AGREE, argmax_agreement, assert_bf16_close, assert_fp32_close,
+                           block_to_device, dev, host, model_to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def G():
+    from gpt_pre_norm_gb300 import build
+    build.build()
+    from gpt_pre_norm_gb300 import binding
+    return binding
+
+
+def _kv(G, B, h, t_cap, dh, dtype, L=None):
+    shape = (B, 2, h, t_cap, dh) if L is None else (B, L, 2, h, t_cap, dh)
+    return G.KV(torch.zeros(shape, dtype=dtype, device="cuda"))
+
+
+# ------------------------------------------------------------------ block ----
+def test_block_fp32_debug_shape(G):
+    """The TorchCode debug block: d=64, 4 heads, x [2, 8, 64], fp32."""
+    w = S.WORKLOADS["block_fp32_d64"]
+    for seed in (0, 1, 2):
+        p = S.block_params(w, seed)
+        x = S.block_input(w, seed)
+        ctx = G.Context(50257, 1024, w.d, w.n_head, 1, G.GPT2_FP32, w.B, w.T)
+        present = _kv(G, w.B, w.n_head, 16, w.d_h, torch.float32)
+        out = G.gpt2_block_forward(ctx, dev(x, torch.float32), block_to_device(p, torch.float32),
+                                   w.B, w.T, w.d, w.n_head, present=present)
+        assert G.gpt2_sync_status(ctx) == 0
+        assert tuple(out.shape) == (2, 8, 64)
+        ref, ref_present = O.block_forward(x, p, w.n_head)
+        assert_fp32_close(host(out), ref, what="fp32 block")
+        assert present.T_len == w.T
+        assert_fp32_close(host(present.data)[:, :, :, :w.T], ref_present, what="fp32 present")
+
+
+@pytest.mark.parametrize("name,B,T", [("block_bf16_d768", 2, 300), ("block_bf16_d1600", 1, 130),
+                                      ("block_bf16_d768", 3, 1)])
+def test_block_bf16(G, name, B, T):
+    w = S.WORKLOADS[name]
+    p = S.block_params(w, seed=1)
+    x = S.block_input(w, seed=1, B=B, T=T)
+    ctx = G.Context(50257, 1024, w.d, w.n_head, 1, G.GPT2_BF16, B, T)
+    present = _kv(G, B, w.n_head, T + 5, w.d_h, torch.bfloat16)
+    out = G.gpt2_block_forward(ctx, dev(x), block_to_device(p), B, T, w.d, w.n_head,
+                               present=present)
+    assert G.gpt2_sync_status(ctx) == 0
+    ref, ref_present = O.block_forward(x, p, w.n_head)
+    assert_bf16_close(host(out), ref, what="block out")
+    # The residual branch alone (out - x) is the part the kernels compute.
+    assert_bf16_close(host(out) - x, ref - x, tol=2e-2, what="block branch")
+    got_present = host(present.data)[:, :, :, :T]
+    assert_bf16_close(got_present[:, 0], ref_present[:, 0], what="present K")
+    assert_bf16_close(got_present[:, 1], ref_present[:, 1], what="present V")
+
+
+@pytest.mark.parametrize("mode", ["in_place", "copy", "no_present"])
+def test_block_with_cache_equals_uncached(G, mode):
+    w = S.WORKLOADS["block_bf16_d768"]
+    B, T0, T1 = 2, 100, 70
+    p = S.block_params(w, seed=2)
+    x = S.block_input(w, seed=2, B=B, T=T0 + T1)
+    pd = block_to_device(p)
+    ctx = G.Context(50257, 1024, w.d, w.n_head, 1, G.GPT2_BF16, B, T0 + T1)
+    cache = _kv(G, B, w.n_head, 256, w.d_h, torch.bfloat16)
+    G.gpt2_block_forward(ctx, dev(x[:, :T0]), pd, B, T0, w.d, w.n_head, present=cache)
+    if mode == "in_place":
+        present = cache
+    elif mode == "copy":
+        present = _kv(G, B, w.n_head, 200, w.d_h, torch.bfloat16)
+    else:
+        present = None
+    out = G.gpt2_block_forward(ctx, dev(x[:, T0:]), pd, B, T1, w.d, w.n_head, past=cache,
+                               present=present)
+    assert G.gpt2_sync_status(ctx) == 0
+    ref, ref_present = O.block_forward(x, p, w.n_head)
+    assert_bf16_close(host(out), ref[:, T0:], what="cached block out")
+    if present is not None:
+        assert present.T_len == T0 + T1
+        got = host(present.data)[:, :, :, :T0 + T1]
+        assert_bf16_close(got, ref_present, what="present after append")
+
+
+# ----------------------------------------------------------- full forward ----
+def _small_model(n_layer=2, d=768, h=12, V=50257):
+    return S.Workload("small", "forward", "bf16", d=d, n_head=h, B=2, T=130, n_layer=n_layer,
+                      n_vocab=V, resid_scale_layers=n_layer)
+
+
+def test_forward_bf16_small(G):
+    w = _small_model()
+    p = S.model_params(w, seed=3)
+    ids = S.token_ids(w, seed=3)
+    ctx = G.Context(w.n_vocab, w.n_ctx, w.d, w.n_head, w.n_layer, G.GPT2_BF16, w.B, w.T)
+    mp = G.ModelParams(model_to_device(p))
+    present = _kv(G, w.B, w.n_head, w.n_ctx, w.d_h, torch.bfloat16, L=w.n_layer)
+    logits = G.gpt2_forward(ctx, dev(ids, torch.int32), mp, w.B, w.T, present=present)
+    assert G.gpt2_sync_status(ctx) == 0
+    ref, ref_present = O.forward(ids, p, w.n_head)
+    got = host(logits)
+    assert got.shape == (w.B, w.T, w.n_vocab)
+    assert_bf16_close(got, ref, what="logits")
+    assert argmax_agreement(got, ref) >= ARGMAX_AGREE
+    assert_bf16_close(host(present.data)[..., :w.T, :], ref_present, what="present")
+
+
+def test_forward_fp32_tiny(G):
+    w = S.Workload("tiny32", "forward", "fp32", d=64, n_head=4, B=2, T=9, n_layer=2, n_vocab=300,
+                   n_ctx=32, w_std=0.1)
+    p = S.model_params(w, seed=4)
+    ids = S.token_ids(w, seed=4)
+    ctx = G.Context(w.n_vocab, w.n_ctx, w.d, w.n_head, w.n_layer, G.GPT2_FP32, w.B, w.T)
+    mp = G.ModelParams(model_to_device(p, torch.float32))
+    logits = G.gpt2_forward(ctx, dev(ids, torch.int32), mp, w.B, w.T)
+    assert G.gpt2_sync_status(ctx) == 0
+    ref, _ = O.forward(ids, p, w.n_head)
+    assert_fp32_close(host(logits), ref, what="fp32 logits")
+
+
+def test_decode_equals_uncached(G):
+    """Prefill 40 tokens with a cache, then 3 one-token steps: the step logits
+    match the uncached pass (GPU and oracle) at those positions."""
+    w = _small_model(n_layer=3)
+    p = S.model_params(w, seed=5)
+    ids = S.token_ids(w, seed=5, T=43)
+    ctx = G.Context(w.n_vocab, w.n_ctx, w.d, w.n_head, w.n_layer, G.GPT2_BF16, w.B, 43)
+    mp = G.ModelParams(model_to_device(p))
+    ids_d = dev(ids, torch.int32)
+    cache = _kv(G, w.B, w.n_head, 64, w.d_h, torch.bfloat16, L=w.n_layer)
+    G.gpt2_forward(ctx, ids_d[:, :40].contiguous(), mp, w.B, 40, present=cache)
+    steps = []
+    for t in range(40, 43):
+        steps.append(host(G.gpt2_forward(ctx, ids_d[:, t:t + 1].contiguous(), mp, w.B, 1,
+                                         past=cache, present=cache)))
+    full = host(G.gpt2_forward(ctx, ids_d, mp, w.B, 43))
+    assert G.gpt2_sync_status(ctx) == 0
+    assert cache.T_len == 43
+    got = np.concatenate(steps, axis=1)
+    ref, _ = O.forward(ids, p, w.n_head, positions=[40, 41, 42])
+    assert_bf16_close(got, ref, what="decode vs oracle")
+    assert_bf16_close(got, full[:, 40:], what="decode vs gpu uncached")
+    assert argmax_agreement(got, ref) >= ARGMAX_AGREE
+
+
+# ----------------------------------------------------------- error paths ----
+def test_errors_are_reported_before_launch(G):
+    w = S.WORKLOADS["block_bf16_d768"]
+    p = block_to_device(S.block_params(w, seed=0))
+    ctx = G.Context(50257, 1024, w.d, w.n_head, 1, G.GPT2_BF16, 2, 64)
+    x = dev(S.block_input(w, 0, B=2, T=64))
+    with pytest.raises(G.Gpt2Error) as e:  # B*T beyond the context's sizing
+        G.gpt2_block_forward(ctx, dev(S.block_input(w, 0, B=3, T=64)), p, 3, 64, w.d, w.n_head)
+    assert e.value.status == G.GPT2_ERR_WORKSPACE
+    past = _kv(G, 2, w.n_head, 1024, w.d_h, torch.bfloat16)
+    past.T_len = 1000
+    with pytest.raises(G.Gpt2Error) as e:  # 1000 + 64 > n_ctx
+        G.gpt2_block_forward(ctx, x, p, 2, 64, w.d, w.n_head, past=past, present=past)
+    assert e.value.status == G.GPT2_ERR_CTX_OVERFLOW
+    small = _kv(G, 2, w.n_head, 32, w.d_h, torch.bfloat16)
+    with pytest.raises(G.Gpt2Error) as e:  # present too small
+        G.gpt2_block_forward(ctx, x, p, 2, 64, w.d, w.n_head, present=small)
+    assert e.value.status == G.GPT2_ERR_CTX_OVERFLOW
+    with pytest.raises(G.Gpt2Error) as e:
+        G.gpt2_block_forward(ctx, x, p, 2, 64, w.d, 16)  # n_head differs from the context
+    assert e.value.status == G.GPT2_ERR_INVALID_ARG
+    xm = torch.empty(2 * 64 * w.d + 8, dtype=torch.bfloat16, device="cuda")[8:].view(2, 64, w.d)
+    with pytest.raises(G.Gpt2Error) as e:
+        G.gpt2_block_forward(ctx, xm, p, 2, 64, w.d, w.n_head)
+    assert e.value.status == G.GPT2_ERR_ALIGNMENT
+    assert G.gpt2_sync_status(ctx) == 0

@@ -1,0 +1,213 @@
+"""Kernel-by-kernel parity with the fp64 oracle, through the C ABI.
+
+Sizes span several tiles and a ragged tail (128-row GEMM tiles, 64-column
+chunks, 128-query / 64-key attention tiles, split-KV chunks)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import gpt2_oracle as O
+from gpt_pre_norm_gb300 import synthetic as S
+from tests.helpers import assert_bf16_close, assert_fp32_close, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def G():
+    from gpt_pre_norm_gb300 import build
+    build.build()
+    from gpt_pre_norm_gb300 import binding
+    return binding
+
+
+def _ctx(G, mode, d=768, h=12, B=8, T=1024, V=50257, L=1):
+    return G.Context(V, 1024, d, h, L, mode, B, T)
+
+
+def _rand(rng, shape, std=1.0, bf16=True):
+    a = std * rng.standard_normal(shape)
+    return S.round_to_bf16(a) if bf16 else a.astype(np.float32)
+
+
+# ------------------------------------------------------------- LayerNorm ----
+@pytest.mark.parametrize("d", [64, 768, 1024, 1600, 100])
+@pytest.mark.parametrize("x_fp32", [True, False])
+def test_layer_norm_bf16(G, d, x_fp32):
+    rng = np.random.default_rng(d)
+    rows = 1000
+    x = _rand(rng, (rows, d), 2.0, bf16=not x_fp32) + 0.5
+    g = _rand(rng, (d,), 0.1) + 1.0
+    g = S.round_to_bf16(g)
+    b = _rand(rng, (d,), 0.1)
+    y = G.gpt2_layer_norm(G.GPT2_BF16, dev(x, torch.float32 if x_fp32 else torch.bfloat16),
+                          dev(g), dev(b))
+    torch.cuda.synchronize()
+    ref = O.layer_norm(x.astype(np.float64), g, b)
+    got = host(y)
+    assert_bf16_close(got, ref, what=f"LN d={d}")
+    # bf16 output: each element within a few bf16 ulps of the exact value.
+    assert np.max(np.abs(got - ref) / (np.abs(ref) + 1e-2)) < 2 ** -7
+
+
+@pytest.mark.parametrize("d", [64, 15, 768])
+def test_layer_norm_fp32(G, d):
+    rng = np.random.default_rng(7 + d)
+    x = _rand(rng, (37, d), 3.0, bf16=False) - 1.0
+    g = _rand(rng, (d,), 0.2, bf16=False) + 1.0
+    b = _rand(rng, (d,), 0.2, bf16=False)
+    y = G.gpt2_layer_norm(G.GPT2_FP32, dev(x, torch.float32), dev(g, torch.float32),
+                          dev(b, torch.float32))
+    torch.cuda.synchronize()
+    assert_fp32_close(host(y), O.layer_norm(x, g, b), what=f"LN fp32 d={d}")
+
+
+# ----------------------------------------------------------------- GEMMs ----
+GEMM_SHAPES = [(128, 256, 64), (300, 200, 768), (1000, 768, 768), (129, 2304, 768),
+               (77, 3072, 200), (1, 64, 64), (32, 1024, 1024), (640, 768, 3072)]
+
+
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+def test_linear_bias_resid_bf16(G, M, N, K):
+    rng = np.random.default_rng(M * 7 + N + K)
+    ctx = _ctx(G, G.GPT2_BF16)
+    A = _rand(rng, (M, K))
+    W = _rand(rng, (N, K), 0.05)
+    bias = _rand(rng, (N,), 0.1)
+    resid = rng.standard_normal((M, N)).astype(np.float32)
+    Ad, Wd, bd = dev(A), dev(W), dev(bias)
+    ref = O.linear(A, W, bias)
+    out = G.gpt2_linear(ctx, G.GPT2_EPI_BIAS_RESID, Ad, Wd, bd, dev(resid, torch.float32))
+    out_b = G.gpt2_linear(ctx, G.GPT2_EPI_BIAS, Ad, Wd, bd)
+    assert G.gpt2_sync_status(ctx) == 0
+    # fp32 output: only the fp32 accumulation order differs from the exact value.
+    assert_fp32_close(host(out), ref + resid, tol=2e-5, what="linear+resid")
+    assert_bf16_close(host(out_b), ref, what="linear+bias")
+    assert np.max(np.abs(host(out_b) - ref)) <= 2 ** -7 * np.max(np.abs(ref)) + 1e-3
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 3072, 768), (128, 256, 1600)])
+def test_linear_gelu_bf16(G, M, N, K):
+    rng = np.random.default_rng(11)
+    ctx = _ctx(G, G.GPT2_BF16)
+    A = _rand(rng, (M, K))
+    W = _rand(rng, (N, K), 0.05)
+    bias = _rand(rng, (N,), 0.5)
+    out = G.gpt2_linear(ctx, G.GPT2_EPI_BIAS_GELU, dev(A), dev(W), dev(bias))
+    assert G.gpt2_sync_status(ctx) == 0
+    assert_bf16_close(host(out), O.gelu(O.linear(A, W, bias)), what="linear+gelu")
+
+
+@pytest.mark.parametrize("M,V", [(130, 50257), (1, 50257), (256, 1000)])
+def test_tied_head_logits(G, M, V):
+    rng = np.random.default_rng(M + V)
+    ctx = _ctx(G, G.GPT2_BF16, V=V)
+    A = _rand(rng, (M, 768))
+    W = _rand(rng, (V, 768), 0.02)
+    out = G.gpt2_linear(ctx, G.GPT2_EPI_LOGITS, dev(A), dev(W))
+    assert G.gpt2_sync_status(ctx) == 0
+    assert out.shape == (M, V)
+    assert_fp32_close(host(out), O.linear(A, W, None), tol=2e-5, what="logits")
+
+
+def test_linear_fp32(G):
+    rng = np.random.default_rng(3)
+    ctx = _ctx(G, G.GPT2_FP32, d=64, h=4)
+    M, N, K = 70, 130, 66
+    A = _rand(rng, (M, K), bf16=False)
+    W = _rand(rng, (N, K), 0.1, bf16=False)
+    bias = _rand(rng, (N,), 0.1, bf16=False)
+    resid = _rand(rng, (M, N), bf16=False)
+    f = lambda a: dev(a, torch.float32)  # noqa: E731
+    o1 = G.gpt2_linear(ctx, G.GPT2_EPI_BIAS, f(A), f(W), f(bias))
+    o2 = G.gpt2_linear(ctx, G.GPT2_EPI_BIAS_GELU, f(A), f(W), f(bias))
+    o3 = G.gpt2_linear(ctx, G.GPT2_EPI_BIAS_RESID, f(A), f(W), f(bias), f(resid))
+    o4 = G.gpt2_linear(ctx, G.GPT2_EPI_LOGITS, f(A), f(W))
+    assert G.gpt2_sync_status(ctx) == 0
+    ref = O.linear(A, W, bias)
+    assert_fp32_close(host(o1), ref)
+    assert_fp32_close(host(o2), O.gelu(ref))
+    assert_fp32_close(host(o3), ref + resid)
+    assert_fp32_close(host(o4), O.linear(A, W, None))
+
+
+# ------------------------------------------------------------- attention ----
+def _attn_case(rng, B, h, T, t_past, t_cap, dh=64, bf16=True):
+    q = _rand(rng, (B, h, T, dh), bf16=bf16)
+    kv = np.zeros((B, 2, h, t_cap, dh), np.float32)
+    kv[:, :, :, :t_past + T] = _rand(rng, (B, 2, h, t_past + T, dh), bf16=bf16)
+    # Poison the unused capacity: the kernels must never read it.
+    kv[:, :, :, t_past + T:] = np.nan
+    return q, kv
+
+
+@pytest.mark.parametrize("B,h,T,t_past", [(2, 3, 1, 0), (2, 3, 2, 0), (1, 2, 127, 0),
+                                          (2, 3, 129, 0), (1, 12, 300, 0), (2, 2, 70, 5),
+                                          (1, 2, 200, 130), (1, 1, 1024, 0)])
+def test_attention_prefill_bf16(G, B, h, T, t_past):
+    rng = np.random.default_rng(B * 1000 + T + t_past)
+    ctx = _ctx(G, G.GPT2_BF16)
+    t_cap = t_past + T + 3
+    q, kv = _attn_case(rng, B, h, T, t_past, t_cap)
+    out = G.gpt2_attention(ctx, dev(q), dev(kv), t_past)
+    assert G.gpt2_sync_status(ctx) == 0
+    k = kv[:, 0, :, :t_past + T].astype(np.float64)
+    v = kv[:, 1, :, :t_past + T].astype(np.float64)
+    ref = O.merge_heads(O.causal_attention(q.astype(np.float64), k, v))
+    got = host(out)
+    assert_bf16_close(got, ref, what="prefill attention")
+    assert np.max(np.abs(got - ref)) < 3e-2
+
+
+@pytest.mark.parametrize("B,h,t_past", [(32, 16, 1023), (1, 2, 1), (2, 3, 100), (1, 4, 1000),
+                                        (3, 1, 5000 // 5)])
+def test_attention_decode_bf16(G, B, h, t_past):
+    rng = np.random.default_rng(B + h + t_past)
+    ctx = _ctx(G, G.GPT2_BF16, d=1024, h=16, B=max(B, 8))
+    t_cap = t_past + 1 + 1
+    q, kv = _attn_case(rng, B, h, 1, t_past, t_cap)
+    out = G.gpt2_attention(ctx, dev(q), dev(kv), t_past)
+    assert G.gpt2_sync_status(ctx) == 0
+    k = kv[:, 0, :, :t_past + 1].astype(np.float64)
+    v = kv[:, 1, :, :t_past + 1].astype(np.float64)
+    ref = O.merge_heads(O.causal_attention(q.astype(np.float64), k, v))
+    got = host(out)
+    assert_bf16_close(got, ref, what="decode attention")
+    assert np.max(np.abs(got - ref)) < 3e-2
+
+
+@pytest.mark.parametrize("dh,T,t_past", [(16, 8, 0), (64, 33, 4), (24, 5, 0), (256, 3, 2)])
+def test_attention_fp32(G, dh, T, t_past):
+    rng = np.random.default_rng(dh + T)
+    h = 3
+    ctx = G.Context(100, 1024, dh * h, h, 1, G.GPT2_FP32, 2, 64)
+    q, kv = _attn_case(rng, 2, h, T, t_past, t_past + T, dh=dh, bf16=False)
+    out = G.gpt2_attention(ctx, dev(q, torch.float32), dev(kv, torch.float32), t_past)
+    assert G.gpt2_sync_status(ctx) == 0
+    ref = O.merge_heads(O.causal_attention(q.astype(np.float64), kv[:, 0].astype(np.float64),
+                                           kv[:, 1].astype(np.float64)))
+    assert_fp32_close(host(out), ref, what="fp32 attention")
+
+
+# ----------------------------------------------------------------- embed ----
+@pytest.mark.parametrize("t_past", [0, 17])
+def test_embed_bf16(G, t_past):
+    w = S.WORKLOADS["forward_bf16_gpt2_small"]
+    rng = np.random.default_rng(5)
+    emb = S.embeddings(w, seed=1)
+    ids = rng.integers(0, w.n_vocab, size=(3, 50)).astype(np.int32)
+    ctx = _ctx(G, G.GPT2_BF16)
+    H = G.gpt2_embed(ctx, dev(ids, torch.int32), dev(emb["wte"]), dev(emb["wpe"]), t_past)
+    assert G.gpt2_sync_status(ctx) == 0
+    ref = O.embed(ids, emb["wte"], emb["wpe"], t_past)
+    np.testing.assert_array_equal(host(H), ref)  # one fp32 add of two bf16 values is exact
+
+
+def test_embed_rejects_bad_token_on_device(G):
+    w = S.WORKLOADS["forward_bf16_gpt2_small"]
+    emb = S.embeddings(w, seed=1)
+    ids = np.array([[0, w.n_vocab, 5]], np.int32)
+    ctx = _ctx(G, G.GPT2_BF16)
+    G.gpt2_embed(ctx, dev(ids, torch.int32), dev(emb["wte"]), dev(emb["wpe"]))
+    assert G.gpt2_sync_status(ctx) == G.GPT2_ERR_INVALID_ARG
+    assert G.gpt2_sync_status(ctx) == G.GPT2_OK  # the error word was cleared
