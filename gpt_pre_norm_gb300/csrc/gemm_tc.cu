@@ -33,10 +33,11 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;                       // one 128-byte swizzle row of bf16
-constexpr int kThreads = 256;
+constexpr int kEpiWarps = 8;                  // two per TMEM lane quarter
+constexpr int kThreads = 128 + 32 * kEpiWarps;
 constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB per A slot
-constexpr int kStageLd = 65;                  // epilogue staging row stride (floats)
-constexpr int kEpiStageFloats = 4 * 32 * kStageLd;
+constexpr int kStageLd = 33;                  // logits transpose row stride (floats)
+constexpr int kEpiStageFloats = kEpiWarps * 32 * kStageLd;
 constexpr int kMaxStages = 8;
 constexpr uint32_t kTmemCols = 512;           // two accumulators of up to 256 columns
 constexpr int kSmemLimit = 232448;            // 227 KB opt-in per CTA
@@ -47,6 +48,7 @@ struct GemmArgs {
   int stages;
   int num_m_blocks;
   int num_tiles;
+  int vec_ok;        // row stride allows 16-byte vector access of out / resid
   unsigned* err;
   EpiParams ep;
 };
@@ -56,80 +58,152 @@ __host__ __device__ inline size_t smem_bytes_for(int BN, int stages) {
          kEpiStageFloats * sizeof(float) + (2 * stages + 5) * sizeof(uint64_t) + 16;
 }
 
+__device__ __forceinline__ void unpack8(const uint4 v, float* f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = bf16_lo(w[i]);
+    f[2 * i + 1] = bf16_hi(w[i]);
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const float* f) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+__device__ __forceinline__ void store32_bf16(bf16* dst, const float (&v)[32]) {
+  uint4* p = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = pack8(v + 8 * i);
+}
+
+// Epilogue of one warp's share of a tile: rows row0 .. row0+31 (this thread:
+// row0 + lane), columns ncol0 .. ncol0+ncols-1, accumulator at TMEM tbase.
 template <int KIND>
-__device__ __forceinline__ void epilogue_chunk(const float* st, int row0, int M, int col0,
-                                               int lane, const GemmArgs& a) {
+__device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol0, int ncols,
+                                              int lane, float* st, const GemmArgs& a) {
   const EpiParams& ep = a.ep;
-  const int N = a.N;
-  if constexpr (KIND == kEpiLogits) {
-    float* out = static_cast<float*>(ep.out);
-    const int c0 = col0 + lane, c1 = col0 + 32 + lane;
-    const bool ok0 = c0 < N, ok1 = c1 < N;
-#pragma unroll 4
-    for (int r = 0; r < 32; ++r) {
-      const int row = row0 + r;
-      if (row >= M) break;
-      float* o = out + static_cast<size_t>(row) * ep.ldo;
-      if (ok0) o[c0] = st[r * kStageLd + lane];
-      if (ok1) o[c1] = st[r * kStageLd + 32 + lane];
-    }
-  } else {
-    // Two adjacent columns per lane; N is even for every bf16 product here.
-    const int n = col0 + 2 * lane;
-    const bool ok = n < N;
-    float b0 = 0.f, b1 = 0.f;
-    if (ok) {
-      const uint32_t bb = *reinterpret_cast<const uint32_t*>(static_cast<const bf16*>(ep.bias) + n);
-      b0 = bf16_lo(bb);
-      b1 = bf16_hi(bb);
-    }
-    if constexpr (KIND == kEpiQkv) {
-      // The whole 64-column chunk belongs to one of Q/K/V and one head.
-      const int which = col0 / ep.d;
-      const int head = (col0 - which * ep.d) >> 6;
-      const int h = ep.d >> 6;
-#pragma unroll 4
-      for (int r = 0; r < 32; ++r) {
-        const int row = row0 + r;
-        if (row >= M) break;
-        const int bi = row / ep.T, t = row - bi * ep.T;
+  const int M = a.M, N = a.N;
+  const int row = row0 + lane;
+  const bool row_ok = row < M;
+  // Per-row destination of the QKV split (fixed for the whole tile).
+  int qkv_b = 0, qkv_t = 0;
+  if constexpr (KIND == kEpiQkv) {
+    qkv_b = row / ep.T;
+    qkv_t = row - qkv_b * ep.T;
+  }
+  for (int c = 0; c < ncols; c += 32) {
+    const int col = ncol0 + c;
+    if (col >= N) break;  // warp-uniform
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), r);
+    const bool full = (col + 32 <= N) && a.vec_ok;
+    const size_t off = static_cast<size_t>(row) * ep.ldo + col;
+
+    if constexpr (KIND == kEpiLogits) {
+      tmem_ld_wait();
+      // Rows of the fp32 logits are only 4-byte aligned: transpose through
+      // shared memory so each store instruction writes one row's 32 columns.
+#pragma unroll
+      for (int j = 0; j < 32; ++j) st[lane * kStageLd + j] = __uint_as_float(r[j]);
+      __syncwarp();
+      float* out = static_cast<float*>(ep.out);
+      const int ccol = col + lane;
+      if (ccol < N) {
+#pragma unroll 8
+        for (int rr = 0; rr < 32; ++rr) {
+          const int rrow = row0 + rr;
+          if (rrow < M) out[static_cast<size_t>(rrow) * ep.ldo + ccol] = st[rr * kStageLd + lane];
+        }
+      }
+      __syncwarp();
+    } else {
+      // Residual prefetch, issued before the TMEM load completes.
+      float rv[32];
+      if constexpr (KIND == kEpiResidF32 || KIND == kEpiResidBf16Out) {
+        const float* rp = static_cast<const float*>(ep.resid) + off;
+        if (full && row_ok) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 v = reinterpret_cast<const float4*>(rp)[i];
+            rv[4 * i] = v.x; rv[4 * i + 1] = v.y; rv[4 * i + 2] = v.z; rv[4 * i + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) rv[j] = (row_ok && col + j < N) ? rp[j] : 0.f;
+        }
+      } else if constexpr (KIND == kEpiResidBf16In) {
+        const bf16* rp = static_cast<const bf16*>(ep.resid) + off;
+        if (full && row_ok) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) unpack8(reinterpret_cast<const uint4*>(rp)[i], rv + 8 * i);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            rv[j] = (row_ok && col + j < N) ? __bfloat162float(rp[j]) : 0.f;
+        }
+      }
+      float bv[32];
+      {
+        const bf16* bp = static_cast<const bf16*>(ep.bias) + col;
+        if (col + 32 <= N) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) unpack8(reinterpret_cast<const uint4*>(bp)[i], bv + 8 * i);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) bv[j] = col + j < N ? __bfloat162float(bp[j]) : 0.f;
+        }
+      }
+      tmem_ld_wait();
+      float v[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) + bv[j];
+
+      if constexpr (KIND == kEpiQkv) {
+        // 64-column chunks of c_attn's output are one of Q/K/V and one head.
+        const int which = col / ep.d;
+        const int head = (col - which * ep.d) >> 6;
+        const int dim0 = col & 63;
         bf16* dst;
         if (which == 0) {
-          dst = static_cast<bf16*>(ep.q) + ((static_cast<size_t>(bi) * h + head) * ep.T + t) * 64;
+          dst = static_cast<bf16*>(ep.q) +
+                ((static_cast<size_t>(qkv_b) * (ep.d >> 6) + head) * ep.T + qkv_t) * 64 + dim0;
         } else {
-          dst = static_cast<bf16*>(ep.kv.base) + bi * ep.kv.s_batch + (which - 1) * ep.kv.s_kv +
-                head * ep.kv.s_head + static_cast<long long>(ep.kv.t_past + t) * 64;
+          dst = static_cast<bf16*>(ep.kv.base) + qkv_b * ep.kv.s_batch + (which - 1) * ep.kv.s_kv +
+                head * ep.kv.s_head + static_cast<long long>(ep.kv.t_past + qkv_t) * 64 + dim0;
         }
-        const float v0 = st[r * kStageLd + 2 * lane] + b0;
-        const float v1 = st[r * kStageLd + 2 * lane + 1] + b1;
-        *reinterpret_cast<uint32_t*>(dst + 2 * lane) = pack_bf16x2(v0, v1);
-      }
-    } else {
-#pragma unroll 4
-      for (int r = 0; r < 32; ++r) {
-        const int row = row0 + r;
-        if (row >= M) break;
-        if (!ok) continue;
-        float v0 = st[r * kStageLd + 2 * lane] + b0;
-        float v1 = st[r * kStageLd + 2 * lane + 1] + b1;
-        const size_t off = static_cast<size_t>(row) * ep.ldo + n;
-        if constexpr (KIND == kEpiBias) {
-          *reinterpret_cast<uint32_t*>(static_cast<bf16*>(ep.out) + off) = pack_bf16x2(v0, v1);
-        } else if constexpr (KIND == kEpiGelu) {
-          *reinterpret_cast<uint32_t*>(static_cast<bf16*>(ep.out) + off) =
-              pack_bf16x2(gelu_tanh_approx(v0), gelu_tanh_approx(v1));
-        } else if constexpr (KIND == kEpiResidF32) {
-          const float2 rr = *reinterpret_cast<const float2*>(static_cast<const float*>(ep.resid) + off);
-          *reinterpret_cast<float2*>(static_cast<float*>(ep.out) + off) =
-              make_float2(rr.x + v0, rr.y + v1);
-        } else if constexpr (KIND == kEpiResidBf16In) {
-          const uint32_t rr = *reinterpret_cast<const uint32_t*>(static_cast<const bf16*>(ep.resid) + off);
-          *reinterpret_cast<float2*>(static_cast<float*>(ep.out) + off) =
-              make_float2(bf16_lo(rr) + v0, bf16_hi(rr) + v1);
-        } else if constexpr (KIND == kEpiResidBf16Out) {
-          const float2 rr = *reinterpret_cast<const float2*>(static_cast<const float*>(ep.resid) + off);
-          *reinterpret_cast<uint32_t*>(static_cast<bf16*>(ep.out) + off) =
-              pack_bf16x2(rr.x + v0, rr.y + v1);
+        if (row_ok) store32_bf16(dst, v);
+      } else if constexpr (KIND == kEpiBias || KIND == kEpiGelu || KIND == kEpiResidBf16Out) {
+        if constexpr (KIND == kEpiGelu) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = gelu_tanh_approx(v[j]);
+        }
+        if constexpr (KIND == kEpiResidBf16Out) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] += rv[j];
+        }
+        bf16* o = static_cast<bf16*>(ep.out) + off;
+        if (full && row_ok) {
+          store32_bf16(o, v);
+        } else if (row_ok) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (col + j < N) o[j] = __float2bfloat16_rn(v[j]);
+        }
+      } else {  // fp32 out = resid + acc + bias
+        float* o = static_cast<float*>(ep.out) + off;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += rv[j];
+        if (full && row_ok) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            reinterpret_cast<float4*>(o)[i] =
+                make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        } else if (row_ok) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (col + j < N) o[j] = v[j];
         }
       }
     }
@@ -167,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4);
+      mbar_init(&tempty[i], kEpiWarps);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -255,8 +329,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait_bounded(mma_done, 0, nullptr, args.err);
   } else if (warp >= 4) {
     // --------------------------------------------------------- epilogue --
-    const int ew = warp - 4;
-    float* st = ep_stage + ew * 32 * kStageLd;
+    // Warp w may read TMEM lanes 32*(w%4) .. +31; the two warps of a lane
+    // quarter split the tile's columns in halves.
+    const int e = warp - 4;
+    const int quarter = warp & 3;
+    const int half = e >> 2;
+    const int ncols = BN / 2;
+    float* st = ep_stage + e * 32 * kStageLd;
     int it = 0;
     for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x, ++it) {
       const int acc = it & 1;
@@ -264,25 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_bounded(&tfull[acc], acc_par, abort_flag, args.err)) break;
       tc_fence_after();
       const int m_blk = tile % args.num_m_blocks, n_blk = tile / args.num_m_blocks;
-      const int row0 = m_blk * kBM + ew * 32;
-      const int n0 = n_blk * BN;
-      for (int c = 0; c < BN; c += 64) {
-        if (n0 + c >= args.N) break;
-        uint32_t r0[32], r1[32];
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
-                               static_cast<uint32_t>(acc * 256 + c);
-        tmem_ld_32x32b_x32(taddr, r0);
-        tmem_ld_32x32b_x32(taddr + 32, r1);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          st[lane * kStageLd + j] = __uint_as_float(r0[j]);
-          st[lane * kStageLd + 32 + j] = __uint_as_float(r1[j]);
-        }
-        __syncwarp();
-        epilogue_chunk<KIND>(st, row0, args.M, n0 + c, lane, args);
-        __syncwarp();
-      }
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(acc * 256 + half * ncols);
+      epilogue_tile<KIND>(tbase, m_blk * kBM + quarter * 32, n_blk * BN + half * ncols, ncols,
+                          lane, st, args);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -373,6 +437,8 @@ int launch_gemm_tc(const LaunchEnv& env, int kind, const bf16* A, const bf16* W,
   args.stages = stages;
   args.num_m_blocks = (M + kBM - 1) / kBM;
   args.num_tiles = args.num_m_blocks * ((N + BN - 1) / BN);
+  args.vec_ok = (kind == kEpiResidF32 || kind == kEpiResidBf16In) ? (ep.ldo % 4 == 0)
+                                                                  : (ep.ldo % 8 == 0);
   args.err = env.err;
   args.ep = ep;
 

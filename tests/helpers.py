@@ -44,6 +44,22 @@ def assert_fp32_close(got, ref, tol=FP32_TOL, what=""):
     return float(err.max())
 
 
+def assert_gemm_f32_close(got, ref, A, W, what=""):
+    """fp32-output tensor-core product of bf16 operands: every product is exact
+    in fp32 and the error comes from the fp32 accumulation alone.  Bound per
+    element: (sqrt(K/16) + 2) * 2^-22 * sum_k |a_k w_k| (K/16 accumulation
+    steps of 16 products, each rounding at fp32 precision), plus one fp32 ulp
+    of the result."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    K = A.shape[1]
+    l1 = np.abs(np.asarray(A, np.float64)) @ np.abs(np.asarray(W, np.float64)).T
+    bound = (np.sqrt(K / 16.0) + 2.0) * 2.0 ** -22 * l1 + 2.0 ** -23 * np.abs(ref)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    excess = np.abs(got - ref) - bound
+    assert float(excess.max()) <= 0, f"{what}: error above the fp32 accumulation bound by {float(excess.max()):.3e}"
+
+
 def argmax_agreement(got_logits, ref_logits) -> float:
     g = np.argmax(np.asarray(got_logits), axis=-1)
     r = np.argmax(np.asarray(ref_logits), axis=-1)

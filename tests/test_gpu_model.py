@@ -57,8 +57,9 @@ def test_block_bf16(G, name, B, T):
     assert G.gpt2_sync_status(ctx) == 0
     ref, ref_present = O.block_forward(x, p, w.n_head)
     assert_bf16_close(host(out), ref, what="block out")
-    # The residual branch alone (out - x) is the part the kernels compute.
-    assert_bf16_close(host(out) - x, ref - x, tol=2e-2, what="block branch")
+    # The residual branches alone (out - x): loose, the bf16 rounding of out is
+    # relative to x; a missing or wrong branch would be off by tens of percent.
+    assert_bf16_close(host(out) - x, ref - x, tol=5e-2, what="block branch")
     got_present = host(present.data)[:, :, :, :T]
     assert_bf16_close(got_present[:, 0], ref_present[:, 0], what="present K")
     assert_bf16_close(got_present[:, 1], ref_present[:, 1], what="present V")
@@ -173,7 +174,7 @@ def test_errors_are_reported_before_launch(G):
     with pytest.raises(G.Gpt2Error) as e:
         G.gpt2_block_forward(ctx, x, p, 2, 64, w.d, 16)  # n_head differs from the context
     assert e.value.status == G.GPT2_ERR_INVALID_ARG
-    xm = torch.empty(2 * 64 * w.d + 8, dtype=torch.bfloat16, device="cuda")[8:].view(2, 64, w.d)
+    xm = torch.empty(2 * 64 * w.d + 1, dtype=torch.bfloat16, device="cuda")[1:].view(2, 64, w.d)
     with pytest.raises(G.Gpt2Error) as e:
         G.gpt2_block_forward(ctx, xm, p, 2, 64, w.d, w.n_head)
     assert e.value.status == G.GPT2_ERR_ALIGNMENT
