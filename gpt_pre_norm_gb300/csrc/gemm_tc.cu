@@ -15,14 +15,21 @@
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=BN,
 //               K=16) x4 per slot into one of two TMEM accumulators.
 //   warp 2      allocates / frees 512 TMEM columns.
-//   warps 4-7   epilogue: tcgen05.ld of their 32 TMEM lanes, a transpose
-//               through shared memory so each warp stores whole row segments,
-//               then bias / GELU / residual / scatter and global stores.
+//   warps 4-11  epilogue, two warps per TMEM lane quarter, each taking half
+//               of the tile's columns in chunks of 32 x 32: tcgen05.ld, bias /
+//               GELU / residual in registers, the chunk written to a swizzled
+//               shared-memory box, and one TMA tensor store per chunk (the
+//               fp32 residual arrives the same way, by a TMA load).  Q, K and
+//               V chunks go to their head-major destinations by 3-D TMA
+//               stores.  fp32 logits rows are only 4-byte aligned, so that
+//               epilogue transposes through shared memory and each store
+//               instruction writes one row's 32 consecutive columns.
 // Two accumulators let the epilogue of tile i overlap the mainloop of i+1.
 // Every mbarrier wait is bounded; a wait that runs out raises the context's
 // error word and the CTA drains its copies, frees TMEM and returns.
+#include <string.h>
+
 #include <algorithm>
-#include <cstdio>
 
 #include "device.cuh"
 #include "internal.h"
@@ -36,11 +43,26 @@ constexpr int kBK = 64;                       // one 128-byte swizzle row of bf1
 constexpr int kEpiWarps = 8;                  // two per TMEM lane quarter
 constexpr int kThreads = 128 + 32 * kEpiWarps;
 constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB per A slot
-constexpr int kStageLd = 33;                  // logits transpose row stride (floats)
-constexpr int kEpiStageFloats = kEpiWarps * 32 * kStageLd;
+constexpr int kLogitsLd = 33;                 // logits transpose row stride (floats)
 constexpr int kMaxStages = 8;
 constexpr uint32_t kTmemCols = 512;           // two accumulators of up to 256 columns
 constexpr int kSmemLimit = 232448;            // 227 KB opt-in per CTA
+constexpr int kRBuf = 32 * 32 * 4;            // fp32 32x32 box, rows of 128 B, 128-byte swizzle
+constexpr int kOBuf = 32 * 32 * 2;            // bf16 32x32 box, rows of 64 B, 64-byte swizzle
+
+__host__ __device__ constexpr bool uses_rbuf(int k) {
+  return k == kEpiResidF32 || k == kEpiResidBf16In || k == kEpiResidBf16Out;
+}
+__host__ __device__ constexpr bool uses_obuf(int k) {
+  return k == kEpiBias || k == kEpiGelu || k == kEpiQkv || k == kEpiResidBf16Out;
+}
+__host__ __device__ constexpr int slot_bytes(int k) {
+  return (uses_rbuf(k) ? kRBuf : 0) + (uses_obuf(k) ? kOBuf : 0);
+}
+// Shared memory of one epilogue warp: two staging slots, or the logits transpose.
+__host__ __device__ constexpr int epi_warp_bytes(int k) {
+  return k == kEpiLogits ? 32 * kLogitsLd * 4 : 2 * slot_bytes(k);
+}
 
 struct GemmArgs {
   int M, N, K;
@@ -49,13 +71,18 @@ struct GemmArgs {
   int num_m_blocks;
   int num_tiles;
   int vec_ok;        // row stride allows 16-byte vector access of out / resid
+  int tma_out;       // output written by TMA stores through tmO
+  int tma_resid;     // fp32 residual read by TMA loads through tmR
+  int tma_qkv;       // Q / K / V written by 3-D TMA stores through tmQ / tmKV
+  int kv_z_per_seq;  // tmKV rows (heads) between sequences
   unsigned* err;
   EpiParams ep;
 };
 
-__host__ __device__ inline size_t smem_bytes_for(int BN, int stages) {
+__host__ __device__ inline size_t smem_bytes_for(int kind, int BN, int stages) {
   return 1024 /* alignment slack */ + static_cast<size_t>(stages) * (kABytes + BN * kBK * 2) +
-         kEpiStageFloats * sizeof(float) + (2 * stages + 5) * sizeof(uint64_t) + 16;
+         static_cast<size_t>(kEpiWarps) * epi_warp_bytes(kind) +
+         (2 * stages + 5 + 2 * kEpiWarps) * sizeof(uint64_t) + 16;
 }
 
 __device__ __forceinline__ void unpack8(const uint4 v, float* f) {
@@ -78,16 +105,43 @@ __device__ __forceinline__ void store32_bf16(bf16* dst, const float (&v)[32]) {
   for (int i = 0; i < 4; ++i) p[i] = pack8(v + 8 * i);
 }
 
+// Row r of a 32x32 fp32 box with the 128-byte swizzle: 16-byte chunk c of
+// the row sits at chunk position c ^ (r & 7).
+__device__ __forceinline__ void box_write_f32(uint8_t* box, int r, const float (&v)[32]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<float4*>(box + r * 128 + ((c ^ (r & 7)) << 4)) =
+        make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+}
+__device__ __forceinline__ void box_read_f32(const uint8_t* box, int r, float (&v)[32]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const float4 x = *reinterpret_cast<const float4*>(box + r * 128 + ((c ^ (r & 7)) << 4));
+    v[4 * c] = x.x; v[4 * c + 1] = x.y; v[4 * c + 2] = x.z; v[4 * c + 3] = x.w;
+  }
+}
+// Row r of a 32x32 bf16 box with the 64-byte swizzle: chunk c at c ^ ((r >> 1) & 3).
+__device__ __forceinline__ void box_write_bf16(uint8_t* box, int r, const float (&v)[32]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(box + r * 64 + ((c ^ ((r >> 1) & 3)) << 4)) = pack8(v + 8 * c);
+}
+
 // Epilogue of one warp's share of a tile: rows row0 .. row0+31 (this thread:
 // row0 + lane), columns ncol0 .. ncol0+ncols-1, accumulator at TMEM tbase.
+// `chunk` counts this warp's chunks (it selects the staging slot); rpar holds
+// the parities of the two residual-load barriers.
 template <int KIND>
 __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol0, int ncols,
-                                              int lane, float* st, const GemmArgs& a) {
+                                              int lane, uint8_t* epi, uint64_t* rbar, int& chunk,
+                                              uint32_t (&rpar)[2], const GemmArgs& a,
+                                              const CUtensorMap* tmO, const CUtensorMap* tmR,
+                                              const CUtensorMap* tmQ, const CUtensorMap* tmKV,
+                                              volatile int* abort_flag) {
   const EpiParams& ep = a.ep;
   const int M = a.M, N = a.N;
   const int row = row0 + lane;
   const bool row_ok = row < M;
-  // Per-row destination of the QKV split (fixed for the whole tile).
   int qkv_b = 0, qkv_t = 0;
   if constexpr (KIND == kEpiQkv) {
     qkv_b = row / ep.T;
@@ -97,16 +151,14 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol
     const int col = ncol0 + c;
     if (col >= N) break;  // warp-uniform
     uint32_t r[32];
-    tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), r);
-    const bool full = (col + 32 <= N) && a.vec_ok;
     const size_t off = static_cast<size_t>(row) * ep.ldo + col;
 
     if constexpr (KIND == kEpiLogits) {
+      tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), r);
       tmem_ld_wait();
-      // Rows of the fp32 logits are only 4-byte aligned: transpose through
-      // shared memory so each store instruction writes one row's 32 columns.
+      float* st = reinterpret_cast<float*>(epi);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) st[lane * kStageLd + j] = __uint_as_float(r[j]);
+      for (int j = 0; j < 32; ++j) st[lane * kLogitsLd + j] = __uint_as_float(r[j]);
       __syncwarp();
       float* out = static_cast<float*>(ep.out);
       const int ccol = col + lane;
@@ -114,24 +166,43 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol
 #pragma unroll 8
         for (int rr = 0; rr < 32; ++rr) {
           const int rrow = row0 + rr;
-          if (rrow < M) out[static_cast<size_t>(rrow) * ep.ldo + ccol] = st[rr * kStageLd + lane];
+          if (rrow < M) out[static_cast<size_t>(rrow) * ep.ldo + ccol] = st[rr * kLogitsLd + lane];
         }
       }
       __syncwarp();
     } else {
-      // Residual prefetch, issued before the TMEM load completes.
+      const int slot = chunk & 1;
+      ++chunk;
+      uint8_t* rb = epi + slot * slot_bytes(KIND);
+      uint8_t* ob = rb + (uses_rbuf(KIND) ? kRBuf : 0);
+      const bool tma_store_path = (KIND == kEpiQkv) ? a.tma_qkv != 0 : a.tma_out != 0;
+      constexpr bool kFp32Resid = KIND == kEpiResidF32 || KIND == kEpiResidBf16Out;
+      const bool tma_resid = kFp32Resid && a.tma_resid != 0;
+      if (tma_store_path || tma_resid) {
+        // The TMA store that last used this slot must be done reading it.
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+      }
+      if (tma_resid && lane == 0) {
+        mbar_arrive_expect_tx(&rbar[slot], kRBuf);
+        tma_load_2d(rb, tmR, &rbar[slot], col, row0);
+      }
+      tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), r);
+      const bool full = (col + 32 <= N) && a.vec_ok;
       float rv[32];
-      if constexpr (KIND == kEpiResidF32 || KIND == kEpiResidBf16Out) {
-        const float* rp = static_cast<const float*>(ep.resid) + off;
-        if (full && row_ok) {
+      if constexpr (kFp32Resid) {
+        if (!tma_resid) {
+          const float* rp = static_cast<const float*>(ep.resid) + off;
+          if (full && row_ok) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 v = reinterpret_cast<const float4*>(rp)[i];
-            rv[4 * i] = v.x; rv[4 * i + 1] = v.y; rv[4 * i + 2] = v.z; rv[4 * i + 3] = v.w;
+            for (int i = 0; i < 8; ++i) {
+              const float4 v = reinterpret_cast<const float4*>(rp)[i];
+              rv[4 * i] = v.x; rv[4 * i + 1] = v.y; rv[4 * i + 2] = v.z; rv[4 * i + 3] = v.w;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) rv[j] = (row_ok && col + j < N) ? rp[j] : 0.f;
           }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) rv[j] = (row_ok && col + j < N) ? rp[j] : 0.f;
         }
       } else if constexpr (KIND == kEpiResidBf16In) {
         const bf16* rp = static_cast<const bf16*>(ep.resid) + off;
@@ -156,12 +227,47 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol
         }
       }
       tmem_ld_wait();
+      if (tma_resid) {
+        mbar_wait_bounded(&rbar[slot], rpar[slot], abort_flag, a.err);
+        rpar[slot] ^= 1u;
+        box_read_f32(rb, lane, rv);
+      }
       float v[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) + bv[j];
+      if constexpr (KIND == kEpiGelu) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = gelu_tanh_approx(v[j]);
+      }
+      if constexpr (uses_rbuf(KIND)) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += rv[j];
+      }
 
-      if constexpr (KIND == kEpiQkv) {
-        // 64-column chunks of c_attn's output are one of Q/K/V and one head.
+      if (tma_store_path) {
+        if constexpr (uses_obuf(KIND)) box_write_bf16(ob, lane, v);
+        else box_write_f32(rb, lane, v);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (KIND == kEpiQkv) {
+            // 64-column chunks of c_attn's output are one of Q/K/V and one head;
+            // the 32 rows are 32 consecutive tokens of one sequence.
+            const int which = col / ep.d;
+            const int head = (col - which * ep.d) >> 6;
+            const int dim0 = col & 63;
+            const int b0 = row0 / ep.T, t0 = row0 - b0 * ep.T;
+            if (which == 0)
+              tma_store_3d(tmQ, ob, dim0, t0, b0 * (ep.d >> 6) + head);
+            else
+              tma_store_3d(tmKV, ob, dim0, ep.kv.t_past + t0,
+                           b0 * a.kv_z_per_seq + (which - 1) * (ep.d >> 6) + head);
+          } else {
+            tma_store_2d(tmO, uses_obuf(KIND) ? static_cast<const void*>(ob) : rb, col, row0);
+          }
+          bulk_commit_group();
+        }
+      } else if constexpr (KIND == kEpiQkv) {
         const int which = col / ep.d;
         const int head = (col - which * ep.d) >> 6;
         const int dim0 = col & 63;
@@ -174,15 +280,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol
                 head * ep.kv.s_head + static_cast<long long>(ep.kv.t_past + qkv_t) * 64 + dim0;
         }
         if (row_ok) store32_bf16(dst, v);
-      } else if constexpr (KIND == kEpiBias || KIND == kEpiGelu || KIND == kEpiResidBf16Out) {
-        if constexpr (KIND == kEpiGelu) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = gelu_tanh_approx(v[j]);
-        }
-        if constexpr (KIND == kEpiResidBf16Out) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] += rv[j];
-        }
+      } else if constexpr (uses_obuf(KIND)) {
         bf16* o = static_cast<bf16*>(ep.out) + off;
         if (full && row_ok) {
           store32_bf16(o, v);
@@ -191,10 +289,8 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol
           for (int j = 0; j < 32; ++j)
             if (col + j < N) o[j] = __float2bfloat16_rn(v[j]);
         }
-      } else {  // fp32 out = resid + acc + bias
+      } else {
         float* o = static_cast<float*>(ep.out) + off;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] += rv[j];
         if (full && row_ok) {
 #pragma unroll
           for (int i = 0; i < 8; ++i)
@@ -213,6 +309,8 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmR,
+                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
                    const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -221,14 +319,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t b_bytes = static_cast<uint32_t>(BN) * kBK * 2;
   uint8_t* sA = smem;
   uint8_t* sB = smem + static_cast<size_t>(S) * kABytes;
-  float* ep_stage = reinterpret_cast<float*>(sB + static_cast<size_t>(S) * b_bytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ep_stage + kEpiStageFloats);
-  uint64_t* full = bars;                 // [S]   TMA landed
-  uint64_t* empty = bars + S;            // [S]   slot consumed by the MMAs
-  uint64_t* tfull = bars + 2 * S;        // [2]   accumulator ready
-  uint64_t* tempty = bars + 2 * S + 2;   // [2]   accumulator drained
-  uint64_t* mma_done = bars + 2 * S + 4; // [1]   every issued MMA retired
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  uint8_t* sEpi = sB + static_cast<size_t>(S) * b_bytes;
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(sEpi + static_cast<size_t>(kEpiWarps) * epi_warp_bytes(KIND));
+  uint64_t* full = bars;                  // [S]   TMA landed
+  uint64_t* empty = bars + S;             // [S]   slot consumed by the MMAs
+  uint64_t* tfull = bars + 2 * S;         // [2]   accumulator ready
+  uint64_t* tempty = bars + 2 * S + 2;    // [2]   accumulator drained
+  uint64_t* mma_done = bars + 2 * S + 4;  // [1]   every issued MMA retired
+  uint64_t* rbars = bars + 2 * S + 5;     // [8][2] residual loads of the epilogue warps
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rbars + 2 * kEpiWarps);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -244,6 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tempty[i], kEpiWarps);
     }
     mbar_init(mma_done, 1);
+    for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(&rbars[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -335,7 +436,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int half = e >> 2;
     const int ncols = BN / 2;
-    float* st = ep_stage + e * 32 * kStageLd;
+    uint8_t* epi = sEpi + static_cast<size_t>(e) * epi_warp_bytes(KIND);
+    uint64_t* rbar = rbars + 2 * e;
+    int chunk = 0;
+    uint32_t rpar[2] = {0u, 0u};
+    if (lane == 0) {
+      if (args.tma_out) tma_prefetch_desc(&tmO);
+      if (args.tma_resid) tma_prefetch_desc(&tmR);
+    }
     int it = 0;
     for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x, ++it) {
       const int acc = it & 1;
@@ -346,11 +454,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc * 256 + half * ncols);
       epilogue_tile<KIND>(tbase, m_blk * kBM + quarter * 32, n_blk * BN + half * ncols, ncols,
-                          lane, st, args);
+                          lane, epi, rbar, chunk, rpar, args, &tmO, &tmR, &tmQ, &tmKV,
+                          abort_flag);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
     }
+    // Every TMA store must be complete before the CTA's shared memory goes.
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -390,6 +502,40 @@ bool encode_kmajor_bf16(const LaunchEnv& env, CUtensorMap* map, const void* base
   return r == CUDA_SUCCESS;
 }
 
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// A [rows, cols] row-major matrix with row stride ld elements, boxes of 32 x 32.
+bool encode_box32(const LaunchEnv& env, CUtensorMap* map, const void* base, bool fp32, int rows,
+                  int cols, int ld) {
+  const size_t es = fp32 ? 4 : 2;
+  if (!aligned16(base) || (static_cast<size_t>(ld) * es) % 16 != 0) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * es};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  return env.encode(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                    2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    fp32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+// Head-major bf16 rows of 64: dims {64, tokens, z}, token stride 128 B, z
+// stride z_stride elements; boxes of 32 dims x 32 tokens x 1.
+bool encode_heads(const LaunchEnv& env, CUtensorMap* map, const void* base, long long tokens,
+                  long long z, long long z_stride) {
+  if (!aligned16(base) || (z_stride * 2) % 16 != 0) return false;
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(tokens), static_cast<cuuint64_t>(z)};
+  const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(z_stride) * 2};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return env.encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 // Tile width: the candidate minimising waves x (BN + 32): the busiest SM's
 // share of the work plus a per-tile cost (operand reloads, epilogue start),
 // preferring wider tiles on ties.
@@ -422,10 +568,14 @@ int launch_gemm_tc(const LaunchEnv& env, int kind, const bf16* A, const bf16* W,
 
   const int BN = choose_bn(M, N, env.num_sms);
   int stages = kMaxStages;
-  while (stages > 2 && smem_bytes_for(BN, stages) > static_cast<size_t>(kSmemLimit)) --stages;
-  const size_t smem = smem_bytes_for(BN, stages);
+  while (stages > 2 && smem_bytes_for(kind, BN, stages) > static_cast<size_t>(kSmemLimit)) --stages;
+  const size_t smem = smem_bytes_for(kind, BN, stages);
 
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tmO, tmR, tmQ, tmKV;
+  memset(&tmO, 0, sizeof(tmO));
+  memset(&tmR, 0, sizeof(tmR));
+  memset(&tmQ, 0, sizeof(tmQ));
+  memset(&tmKV, 0, sizeof(tmKV));
   if (!encode_kmajor_bf16(env, &tmA, A, M, K, kBM)) return GPT2_ERR_CUDA;
   if (!encode_kmajor_bf16(env, &tmB, W, N, K, BN)) return GPT2_ERR_CUDA;
 
@@ -439,8 +589,30 @@ int launch_gemm_tc(const LaunchEnv& env, int kind, const bf16* A, const bf16* W,
   args.num_tiles = args.num_m_blocks * ((N + BN - 1) / BN);
   args.vec_ok = (kind == kEpiResidF32 || kind == kEpiResidBf16In) ? (ep.ldo % 4 == 0)
                                                                   : (ep.ldo % 8 == 0);
+  args.tma_out = 0;
+  args.tma_resid = 0;
+  args.tma_qkv = 0;
+  args.kv_z_per_seq = 0;
   args.err = env.err;
   args.ep = ep;
+  if (kind == kEpiBias || kind == kEpiGelu || kind == kEpiResidBf16Out)
+    args.tma_out = encode_box32(env, &tmO, ep.out, false, M, N, ep.ldo);
+  else if (kind == kEpiResidF32 || kind == kEpiResidBf16In)
+    args.tma_out = encode_box32(env, &tmO, ep.out, true, M, N, ep.ldo);
+  if (kind == kEpiResidF32 || kind == kEpiResidBf16Out)
+    args.tma_resid = encode_box32(env, &tmR, ep.resid, true, M, N, ep.ldo);
+  if (kind == kEpiQkv && ep.T % 32 == 0 && M % ep.T == 0) {
+    // Q [B*h, T, 64]; the cache of this layer as rows of heads: z = b *
+    // (heads per sequence in the cache layout) + kv * h + head.
+    const int h = ep.d / 64;
+    const long long B = M / ep.T;
+    const long long z_per_seq = ep.kv.s_batch / ep.kv.s_head;
+    const long long t_cap = ep.kv.s_head / 64;
+    args.kv_z_per_seq = static_cast<int>(z_per_seq);
+    args.tma_qkv = encode_heads(env, &tmQ, ep.q, ep.T, B * h, static_cast<long long>(ep.T) * 64) &&
+                   encode_heads(env, &tmKV, ep.kv.base, t_cap, (B - 1) * z_per_seq + 2 * h,
+                                ep.kv.s_head);
+  }
 
   // Set once per process (the opt-in limit does not depend on the call), so
   // later calls make no non-stream CUDA call (safe under stream capture).
@@ -452,7 +624,7 @@ int launch_gemm_tc(const LaunchEnv& env, int kind, const bf16* A, const bf16* W,
     attr_set[kind] = true;
   }
   const int grid = std::min(args.num_tiles, env.num_sms);
-  void* params[] = {&tmA, &tmB, &args};
+  void* params[] = {&tmA, &tmB, &tmO, &tmR, &tmQ, &tmKV, &args};
   if (cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), params, smem, stream) != cudaSuccess)
     return GPT2_ERR_CUDA;
 
