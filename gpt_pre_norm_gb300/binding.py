@@ -81,6 +81,7 @@ def _load() -> C.CDLL:
         "gpt2_linear": (I, [P, I, P, P, P, P, P, I, I, I, P]),
         "gpt2_attention": (I, [P, P, P, I, I, I, I, I, I, P, P]),
         "gpt2_embed": (I, [P, P, P, P, I, I, I, P, P]),
+        "gpt2_attention_decode_noalloc": (I, [P, P, I, I, I, I, I, I, P, P]),
         "gpt2_profile_enable": (I, [P, I]),
         "gpt2_profile_kinds": (I, []),
         "gpt2_profile_read": (I, [P, I, C.POINTER(C.c_char_p), C.POINTER(LL), C.POINTER(D),
@@ -261,6 +262,19 @@ def gpt2_attention(ctx: Context, q: torch.Tensor, kv: torch.Tensor, T_past: int,
         out = torch.empty((B, T, h * dh), dtype=q.dtype, device=q.device)
     _check(LIB.gpt2_attention(ctx.handle, _ptr(q), _ptr(kv), B, h, T, T_past, T_cap, dh, _ptr(out),
                               _stream(stream)), "gpt2_attention")
+    return out
+
+
+def gpt2_attention_decode_noalloc(q: torch.Tensor, kv: torch.Tensor, T_past: int, splits: int = 0,
+                                  out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Decode attention (T = 1) without a context or workspace: the partial
+    results use the library's own fixed device array."""
+    B, h, T, dh = q.shape
+    if out is None:
+        out = torch.empty((B, T, h * dh), dtype=q.dtype, device=q.device)
+    _check(LIB.gpt2_attention_decode_noalloc(_ptr(q), _ptr(kv), B, h, T_past, kv.shape[-2], dh,
+                                             splits, _ptr(out), _stream(stream)),
+           "gpt2_attention_decode_noalloc")
     return out
 
 

@@ -197,6 +197,32 @@ int gpt2_linear(gpt2_ctx *ctx, int epilogue, const void *A, const void *W, const
 int gpt2_attention(gpt2_ctx *ctx, const void *q, const void *kv, int B, int n_head, int T,
                    int T_past, int T_cap, int d_h, void *out, void *stream);
 
+/* Single-token decode attention that allocates nothing.  The pages have no
+ * counterpart: this exists for callers that cannot allocate device memory
+ * and so cannot hand gpt2_ctx_create a workspace -- a plugin that its host
+ * application gives only pointers and a stream, a process whose device
+ * memory another allocator has already reserved in full, or a
+ * latency-critical path that must not take cudaMalloc's implicit
+ * synchronisation.  It computes what gpt2_attention computes for T = 1 and
+ * T_past > 0 (bf16, d_h = 64), keeping the split-KV partial results in a
+ * 1 MiB array compiled into the library, which every GPU that loads the
+ * library holds until the process exits.
+ *   q: [B, h, 1, 64]; kv: [B, 2, h, T_cap, 64] with T_past + 1 valid
+ *   positions (the new key/value already at position T_past);
+ *   out: [B, 1, h * 64].  The caller still provides all three.
+ *   splits: key chunks per (sequence, head); 0 chooses as gpt2_attention.
+ * The first call on a device looks up the array's device address, once per
+ * device and with that device current; make that first call before any
+ * stream capture.  All calls share the one array, which keeps the previous
+ * call's contents; nothing in it has to start at zero, since each call writes
+ * every partial result before reading it.  Calls that overlap on the GPU
+ * (other streams, other host threads) race on the array.
+ * Errors: INVALID_ARG, UNSUPPORTED (d_h != 64), CTX_OVERFLOW (T_past + 1 >
+ * T_cap), ALIGNMENT, WORKSPACE (B * h * splits partial results of 66 floats
+ * exceed the 1 MiB array), NO_DEVICE, CUDA.                                 */
+int gpt2_attention_decode_noalloc(const void *q, const void *kv, int B, int n_head, int T_past,
+                                  int T_cap, int d_h, int splits, void *out, void *stream);
+
 /* Embedding: H[b, t] = wte[ids[b, t]] + wpe[T_past + t] (fp32 out [B, T, d]).
  * wte [n_vocab, d], wpe [n_ctx, d] in the mode dtype.                      */
 int gpt2_embed(gpt2_ctx *ctx, const int32_t *ids, const void *wte, const void *wpe, int B, int T,
