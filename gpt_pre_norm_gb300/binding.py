@@ -82,6 +82,7 @@ def _load() -> C.CDLL:
         "gpt2_attention": (I, [P, P, P, I, I, I, I, I, I, P, P]),
         "gpt2_embed": (I, [P, P, P, P, I, I, I, P, P]),
         "gpt2_attention_decode_noalloc": (I, [P, P, I, I, I, I, I, I, P, P]),
+        "gpt2_ctx_cache_weights": (I, [P, I]),
         "gpt2_profile_enable": (I, [P, I]),
         "gpt2_profile_kinds": (I, []),
         "gpt2_profile_read": (I, [P, I, C.POINTER(C.c_char_p), C.POINTER(LL), C.POINTER(D),
@@ -173,6 +174,10 @@ class Context:
             self.close()
         except Exception:
             pass
+
+
+def gpt2_ctx_cache_weights(ctx: Context, enable: bool) -> None:
+    _check(LIB.gpt2_ctx_cache_weights(ctx.handle, int(enable)), "gpt2_ctx_cache_weights")
 
 
 def gpt2_sync_status(ctx: Context, stream=None) -> int:

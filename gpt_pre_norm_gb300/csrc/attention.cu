@@ -47,7 +47,7 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
 __global__ void __launch_bounds__(kAttnThreads, 2)
     attn_prefill_bf16(const bf16* __restrict__ q, const bf16* __restrict__ kv, long long s_batch,
                       long long s_kv, long long s_head, int h, int T, int t_past,
-                      bf16* __restrict__ out, int n_qtiles) {
+                      uint16_t* __restrict__ out, int n_qtiles, int out_f16) {
   __shared__ __align__(128) uint8_t sQ[kQTile * 128];
   __shared__ __align__(128) uint8_t sK[2][kKTile * 128];
   __shared__ __align__(128) uint8_t sV[2][kKTile * 128];
@@ -212,15 +212,16 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   const float inv_a = 1.f / l_a, inv_b = 1.f / l_b;
   const int d = h * kDh;
   const int ra = q0 + row_lo + g, rb = ra + 8;
-  bf16* outb = out + static_cast<size_t>(b) * T * d + head * kDh + 2 * tq;
+  uint16_t* outb = out + static_cast<size_t>(b) * T * d + head * kDh + 2 * tq;
+  const bool f16 = out_f16 != 0;
 #pragma unroll
   for (int nd = 0; nd < 8; ++nd) {
     if (ra < T)
       *reinterpret_cast<uint32_t*>(outb + static_cast<size_t>(ra) * d + 8 * nd) =
-          pack_bf16x2(o[nd][0] * inv_a, o[nd][1] * inv_a);
+          pack_16x2(o[nd][0] * inv_a, o[nd][1] * inv_a, f16);
     if (rb < T)
       *reinterpret_cast<uint32_t*>(outb + static_cast<size_t>(rb) * d + 8 * nd) =
-          pack_bf16x2(o[nd][2] * inv_b, o[nd][3] * inv_b);
+          pack_16x2(o[nd][2] * inv_b, o[nd][3] * inv_b, f16);
   }
 }
 
@@ -232,7 +233,7 @@ constexpr int kPartialStride = kDh + 2;  // o[64], m, l
 __global__ void __launch_bounds__(kDecThreads)
     attn_decode_bf16(const bf16* __restrict__ q, const bf16* __restrict__ kv, long long s_batch,
                      long long s_kv, long long s_head, int h, int t_len, int chunk,
-                     bf16* __restrict__ out, float* __restrict__ partials) {
+                     uint16_t* __restrict__ out, float* __restrict__ partials, int out_f16) {
   __shared__ float s_m[kDecWarps], s_l[kDecWarps];
   __shared__ float s_o[kDecWarps][kDh];
 
@@ -345,7 +346,7 @@ __global__ void __launch_bounds__(kDecThreads)
     if (splits == 1) {
       const float inv = 1.f / lsum;
       *reinterpret_cast<uint32_t*>(out + static_cast<size_t>(bh) * kDh + 2 * lane) =
-          pack_bf16x2(o0 * inv, o1 * inv);
+          pack_16x2(o0 * inv, o1 * inv, out_f16 != 0);
     } else {
       float* pp = partials + (static_cast<size_t>(bh) * splits + split) * kPartialStride;
       pp[2 * lane] = o0;
@@ -360,7 +361,7 @@ __global__ void __launch_bounds__(kDecThreads)
 
 // One warp per (sequence, head): merges the splits' partial results.
 __global__ void attn_decode_combine(const float* __restrict__ partials, int n_bh, int splits,
-                                    bf16* __restrict__ out) {
+                                    uint16_t* __restrict__ out, int out_f16) {
   const int bh = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (bh >= n_bh) return;
@@ -377,7 +378,7 @@ __global__ void attn_decode_combine(const float* __restrict__ partials, int n_bh
   }
   const float inv = 1.f / lsum;
   *reinterpret_cast<uint32_t*>(out + static_cast<size_t>(bh) * kDh + 2 * lane) =
-      pack_bf16x2(o0 * inv, o1 * inv);
+      pack_16x2(o0 * inv, o1 * inv, out_f16 != 0);
 }
 
 // -------------------------------------------------------------------- fp32 --
@@ -438,14 +439,15 @@ __global__ void attn_fp32(const float* __restrict__ q, const float* __restrict__
 }  // namespace
 
 int launch_attention_bf16(const bf16* q, const bf16* kv, long long s_batch, long long s_kv,
-                          long long s_head, int B, int h, int T, int t_past, bf16* out,
-                          cudaStream_t stream) {
+                          long long s_head, int B, int h, int T, int t_past, void* out,
+                          cudaStream_t stream, bool out_f16) {
   if (B <= 0 || h <= 0 || T <= 0 || t_past < 0) return GPT2_ERR_INVALID_ARG;
   const int n_qtiles = (T + kQTile - 1) / kQTile;
   if (n_qtiles > 65535) return GPT2_ERR_UNSUPPORTED;
   dim3 grid(B * h, n_qtiles);
   attn_prefill_bf16<<<grid, kAttnThreads, 0, stream>>>(q, kv, s_batch, s_kv, s_head, h, T, t_past,
-                                                       out, n_qtiles);
+                                                       static_cast<uint16_t*>(out), n_qtiles,
+                                                       out_f16 ? 1 : 0);
   return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
@@ -461,19 +463,21 @@ int decode_splits(int B, int h, int t_len, int num_sms) {
 }
 
 int launch_decode_attention_bf16(const bf16* q, const bf16* kv, long long s_batch, long long s_kv,
-                                 long long s_head, int B, int h, int t_len, bf16* out,
+                                 long long s_head, int B, int h, int t_len, void* out,
                                  float* partials, int splits, cudaStream_t stream,
-                                 int* launches) {
+                                 int* launches, bool out_f16) {
   if (B <= 0 || h <= 0 || t_len <= 0 || splits <= 0 || splits > 65535) return GPT2_ERR_INVALID_ARG;
   if (splits > 1 && partials == nullptr) return GPT2_ERR_INVALID_ARG;
   const int chunk = (t_len + splits - 1) / splits;
   dim3 grid(splits, B * h);
   attn_decode_bf16<<<grid, kDecThreads, 0, stream>>>(q, kv, s_batch, s_kv, s_head, h, t_len, chunk,
-                                                     out, partials);
+                                                     static_cast<uint16_t*>(out), partials,
+                                                     out_f16 ? 1 : 0);
   int n = 1;
   if (splits > 1) {
     const int n_bh = B * h;
-    attn_decode_combine<<<(n_bh + 7) / 8, 256, 0, stream>>>(partials, n_bh, splits, out);
+    attn_decode_combine<<<(n_bh + 7) / 8, 256, 0, stream>>>(
+        partials, n_bh, splits, static_cast<uint16_t*>(out), out_f16 ? 1 : 0);
     ++n;
   }
   if (launches) *launches = n;

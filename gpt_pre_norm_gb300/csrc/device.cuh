@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -166,8 +167,9 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, both operands K-major bf16, fp32 accumulate.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+// D[tmem] (+)= A[smem] * B[smem]^T, both operands K-major 16-bit (the kind
+// set by the instruction descriptor), fp32 accumulate.
+__device__ __forceinline__ void umma_f16kind(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -186,14 +188,14 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
       : "memory");
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, fp32 D,
-// both K-major, tile M x N.
-__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
-  return (1u << 4)                              // D format: f32
-         | (1u << 7)                            // A format: bf16
-         | (1u << 10)                           // B format: bf16
-         | (static_cast<uint32_t>(N >> 3) << 17)  // N / 8
-         | (static_cast<uint32_t>(M >> 4) << 24); // M / 16
+// Instruction descriptor of tcgen05.mma kind::f16 with fp32 D, both operands
+// K-major, tile M x N; A and B both bf16 (f16 = false) or both fp16.
+__host__ __device__ constexpr uint32_t umma_idesc_16(int M, int N, bool f16) {
+  return (1u << 4)                                 // D format: f32
+         | ((f16 ? 0u : 1u) << 7)                  // A format: f16 = 0, bf16 = 1
+         | ((f16 ? 0u : 1u) << 10)                 // B format: same as A
+         | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
 }
 
 // Shared-memory matrix descriptor of a K-major operand tile stored with the
@@ -276,6 +278,16 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two floats packed as 16-bit values of the given kind (fp16 or bf16).
+__device__ __forceinline__ uint32_t pack_16x2(float lo, float hi, bool f16) {
+  return f16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }

@@ -75,6 +75,8 @@ struct GemmArgs {
   int tma_resid;     // fp32 residual read by TMA loads through tmR
   int tma_qkv;       // Q / K / V written by 3-D TMA stores through tmQ / tmKV
   int kv_z_per_seq;  // tmKV rows (heads) between sequences
+  int out_f16;       // 16-bit outputs of kEpiBias / kEpiGelu are fp16 (else bf16)
+  uint32_t idesc;    // tcgen05.mma instruction descriptor (operand kind, tile)
   unsigned* err;
   EpiParams ep;
 };
@@ -94,15 +96,15 @@ __device__ __forceinline__ void unpack8(const uint4 v, float* f) {
   }
 }
 
-__device__ __forceinline__ uint4 pack8(const float* f) {
-  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                    pack_bf16x2(f[6], f[7]));
+__device__ __forceinline__ uint4 pack8(const float* f, bool f16) {
+  return make_uint4(pack_16x2(f[0], f[1], f16), pack_16x2(f[2], f[3], f16),
+                    pack_16x2(f[4], f[5], f16), pack_16x2(f[6], f[7], f16));
 }
 
-__device__ __forceinline__ void store32_bf16(bf16* dst, const float (&v)[32]) {
+__device__ __forceinline__ void store32_16(void* dst, const float (&v)[32], bool f16) {
   uint4* p = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) p[i] = pack8(v + 8 * i);
+  for (int i = 0; i < 4; ++i) p[i] = pack8(v + 8 * i, f16);
 }
 
 // Row r of a 32x32 fp32 box with the 128-byte swizzle: 16-byte chunk c of
@@ -120,11 +122,11 @@ __device__ __forceinline__ void box_read_f32(const uint8_t* box, int r, float (&
     v[4 * c] = x.x; v[4 * c + 1] = x.y; v[4 * c + 2] = x.z; v[4 * c + 3] = x.w;
   }
 }
-// Row r of a 32x32 bf16 box with the 64-byte swizzle: chunk c at c ^ ((r >> 1) & 3).
-__device__ __forceinline__ void box_write_bf16(uint8_t* box, int r, const float (&v)[32]) {
+// Row r of a 32x32 16-bit box with the 64-byte swizzle: chunk c at c ^ ((r >> 1) & 3).
+__device__ __forceinline__ void box_write_16(uint8_t* box, int r, const float (&v)[32], bool f16) {
 #pragma unroll
   for (int c = 0; c < 4; ++c)
-    *reinterpret_cast<uint4*>(box + r * 64 + ((c ^ ((r >> 1) & 3)) << 4)) = pack8(v + 8 * c);
+    *reinterpret_cast<uint4*>(box + r * 64 + ((c ^ ((r >> 1) & 3)) << 4)) = pack8(v + 8 * c, f16);
 }
 
 // Epilogue of one warp's share of a tile: rows row0 .. row0+31 (this thread:
@@ -177,6 +179,8 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol
       uint8_t* ob = rb + (uses_rbuf(KIND) ? kRBuf : 0);
       const bool tma_store_path = (KIND == kEpiQkv) ? a.tma_qkv != 0 : a.tma_out != 0;
       constexpr bool kFp32Resid = KIND == kEpiResidF32 || KIND == kEpiResidBf16Out;
+      // bf16 for Q/K/V and the block output; the caller's choice for the others.
+      const bool out16 = (KIND == kEpiBias || KIND == kEpiGelu) && a.out_f16 != 0;
       const bool tma_resid = kFp32Resid && a.tma_resid != 0;
       if (tma_store_path || tma_resid) {
         // The TMA store that last used this slot must be done reading it.
@@ -245,7 +249,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol
       }
 
       if (tma_store_path) {
-        if constexpr (uses_obuf(KIND)) box_write_bf16(ob, lane, v);
+        if constexpr (uses_obuf(KIND)) box_write_16(ob, lane, v, out16);
         else box_write_f32(rb, lane, v);
         fence_proxy_async_smem();
         __syncwarp();
@@ -279,15 +283,15 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol
           dst = static_cast<bf16*>(ep.kv.base) + qkv_b * ep.kv.s_batch + (which - 1) * ep.kv.s_kv +
                 head * ep.kv.s_head + static_cast<long long>(ep.kv.t_past + qkv_t) * 64 + dim0;
         }
-        if (row_ok) store32_bf16(dst, v);
+        if (row_ok) store32_16(dst, v, false);
       } else if constexpr (uses_obuf(KIND)) {
-        bf16* o = static_cast<bf16*>(ep.out) + off;
+        uint16_t* o = static_cast<uint16_t*>(ep.out) + off;
         if (full && row_ok) {
-          store32_bf16(o, v);
+          store32_16(o, v, out16);
         } else if (row_ok) {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (col + j < N) o[j] = __float2bfloat16_rn(v[j]);
+            if (col + j < N) o[j] = static_cast<uint16_t>(pack_16x2(v[j], 0.f, out16) & 0xFFFFu);
         }
       } else {
         float* o = static_cast<float*>(ep.out) + off;
@@ -393,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------- MMA issuer --
-    const uint32_t idesc = umma_idesc_bf16(kBM, BN);
+    const uint32_t idesc = args.idesc;
     int stage = 0;
     uint32_t phase = 0;
     int it = 0;
@@ -415,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < kBK / 16; ++k) {
           // +32 bytes per 16-element K slice: +2 in the descriptor's address field.
-          umma_bf16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          umma_f16kind(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
         }
         umma_commit(&empty[stage]);
         if (++stage == S) {
@@ -489,14 +493,17 @@ void* kernel_for(int kind) {
   }
 }
 
-bool encode_kmajor_bf16(const LaunchEnv& env, CUtensorMap* map, const void* base, int rows,
-                        int K, int box_rows) {
+bool encode_kmajor_16(const LaunchEnv& env, CUtensorMap* map, const void* base, int rows, int K,
+                      int box_rows, bool f16) {
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = env.encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
-                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  const CUresult r = env.encode(map,
+                                f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                2, const_cast<void*>(base), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE,
                                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -504,16 +511,20 @@ bool encode_kmajor_bf16(const LaunchEnv& env, CUtensorMap* map, const void* base
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-// A [rows, cols] row-major matrix with row stride ld elements, boxes of 32 x 32.
+// A [rows, cols] row-major matrix with row stride ld elements, boxes of 32 x 32;
+// fp32, or 16-bit (fp16 when f16, else bf16).
 bool encode_box32(const LaunchEnv& env, CUtensorMap* map, const void* base, bool fp32, int rows,
-                  int cols, int ld) {
+                  int cols, int ld, bool f16 = false) {
   const size_t es = fp32 ? 4 : 2;
   if (!aligned16(base) || (static_cast<size_t>(ld) * es) % 16 != 0) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * es};
   const cuuint32_t box[2] = {32, 32};
   const cuuint32_t estr[2] = {1, 1};
-  return env.encode(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+  return env.encode(map,
+                    fp32  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                    : f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                          : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                     2, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE,
                     fp32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
@@ -557,8 +568,9 @@ int choose_bn(int M, int N, int num_sms) {
 
 }  // namespace
 
-int launch_gemm_tc(const LaunchEnv& env, int kind, const bf16* A, const bf16* W, int M, int N,
-                   int K, const EpiParams& ep, cudaStream_t stream, double* flops, double* bytes) {
+int launch_gemm_tc(const LaunchEnv& env, int kind, const void* A, const void* W, int M, int N,
+                   int K, const EpiParams& ep, cudaStream_t stream, double* flops, double* bytes,
+                   bool operands_f16, bool out_f16) {
   void* fn = kernel_for(kind);
   if (!fn) return GPT2_ERR_INVALID_ARG;
   if (M <= 0 || N <= 0 || K <= 0) return GPT2_ERR_INVALID_ARG;
@@ -576,8 +588,8 @@ int launch_gemm_tc(const LaunchEnv& env, int kind, const bf16* A, const bf16* W,
   memset(&tmR, 0, sizeof(tmR));
   memset(&tmQ, 0, sizeof(tmQ));
   memset(&tmKV, 0, sizeof(tmKV));
-  if (!encode_kmajor_bf16(env, &tmA, A, M, K, kBM)) return GPT2_ERR_CUDA;
-  if (!encode_kmajor_bf16(env, &tmB, W, N, K, BN)) return GPT2_ERR_CUDA;
+  if (!encode_kmajor_16(env, &tmA, A, M, K, kBM, operands_f16)) return GPT2_ERR_CUDA;
+  if (!encode_kmajor_16(env, &tmB, W, N, K, BN, operands_f16)) return GPT2_ERR_CUDA;
 
   GemmArgs args;
   args.M = M;
@@ -593,9 +605,13 @@ int launch_gemm_tc(const LaunchEnv& env, int kind, const bf16* A, const bf16* W,
   args.tma_resid = 0;
   args.tma_qkv = 0;
   args.kv_z_per_seq = 0;
+  args.out_f16 = out_f16 ? 1 : 0;
+  args.idesc = umma_idesc_16(kBM, BN, operands_f16);
   args.err = env.err;
   args.ep = ep;
-  if (kind == kEpiBias || kind == kEpiGelu || kind == kEpiResidBf16Out)
+  if (kind == kEpiBias || kind == kEpiGelu)
+    args.tma_out = encode_box32(env, &tmO, ep.out, false, M, N, ep.ldo, out_f16);
+  else if (kind == kEpiResidBf16Out)
     args.tma_out = encode_box32(env, &tmO, ep.out, false, M, N, ep.ldo);
   else if (kind == kEpiResidF32 || kind == kEpiResidBf16In)
     args.tma_out = encode_box32(env, &tmO, ep.out, true, M, N, ep.ldo);

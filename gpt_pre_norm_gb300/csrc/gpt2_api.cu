@@ -27,7 +27,8 @@ namespace {
 const char* kKindNames[kKindCount] = {
     "embed",          "layer_norm",        "gemm_c_attn",    "attention_prefill",
     "gemm_c_proj",    "gemm_c_fc",         "gemm_mlp_c_proj", "gemm_lm_head",
-    "gemm_other",     "attention_decode",  "attention_decode_combine", "simt_fp32"};
+    "gemm_other",     "attention_decode",  "attention_decode_combine", "simt_fp32",
+    "weight_convert"};
 
 struct ProfRec {
   int kind;
@@ -38,8 +39,15 @@ struct ProfRec {
 
 // Offsets (bytes) of the workspace regions.
 struct WsPlan {
-  size_t err, ln, q, kv, attn, resid, fc, partials, total;
+  size_t err, ln, q, kv, attn, resid, fc, partials, wconv, total;
 };
+
+// fp16 working copies of the weights (bf16 mode): per layer slot, c_attn
+// [3d, d] at 0, c_proj [d, d] at 3d^2, c_fc [4d, d] at 4d^2, mlp c_proj
+// [d, 4d] at 8d^2 (elements); wte after the n_layer slots.
+size_t layer_slot_elems(const gpt2_hparams& hp) {
+  return 12 * static_cast<size_t>(hp.n_embd) * hp.n_embd;
+}
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
@@ -62,6 +70,9 @@ WsPlan plan_workspace(const gpt2_hparams& hp, int max_B, int max_T) {
   p.resid = take(M * d * 4);
   p.fc = take(M * 4 * d * es);
   p.partials = take(decode_partials_floats(max_B, hp.n_head, 64) * 4);
+  p.wconv = take(hp.dtype == GPT2_BF16 ? 2 * (hp.n_layer * layer_slot_elems(hp) +
+                                              static_cast<size_t>(hp.n_vocab) * hp.n_embd)
+                                       : 0);
   p.total = off;
   return p;
 }
@@ -80,6 +91,8 @@ struct gpt2_ctx {
   LaunchEnv env;
   bool prof;
   int extra_kernels;  // set by a launch function that launched more than one kernel
+  bool cache_weights;  // keep fp16 weight copies across calls
+  std::vector<const void*> conv_src;  // source of each converted weight (cache keys)
   std::vector<ProfRec> recs;
   std::vector<cudaEvent_t> free_events;
   long long launches[kKindCount];
@@ -177,11 +190,69 @@ int copy_positions(const KvView& dst, const KvView& src, int B, int h, int t, in
   return GPT2_OK;
 }
 
+// fp16 copies of one block's four weight matrices.
+struct BlockW16 {
+  const __half *attn_w, *proj_w, *fc_w, *mlp_proj_w;
+};
+
+// Converts a block's weights into layer slot `slot` (skipped for matrices the
+// cache already holds).
+int convert_block_weights(gpt2_ctx* c, int slot, const gpt2_block_params* p, cudaStream_t s,
+                          BlockW16* w) {
+  const size_t d = c->hp.n_embd;
+  __half* base = reinterpret_cast<__half*>(c->ws + c->plan.wconv) + slot * layer_slot_elems(c->hp);
+  const void* srcs[4] = {p->attn_w, p->proj_w, p->fc_w, p->mlp_proj_w};
+  const size_t offs[4] = {0, 3 * d * d, 4 * d * d, 8 * d * d};
+  const size_t ns[4] = {3 * d * d, d * d, 4 * d * d, 4 * d * d};
+  ConvSegs segs{};
+  for (int i = 0; i < 4; ++i) {
+    const size_t key = static_cast<size_t>(slot) * 4 + i;
+    if (c->cache_weights && c->conv_src[key] == srcs[i]) continue;
+    segs.src[segs.count] = static_cast<const bf16*>(srcs[i]);
+    segs.dst[segs.count] = base + offs[i];
+    segs.n[segs.count] = static_cast<long long>(ns[i]);
+    ++segs.count;
+    c->conv_src[key] = c->cache_weights ? srcs[i] : nullptr;
+  }
+  w->attn_w = base + offs[0];
+  w->proj_w = base + offs[1];
+  w->fc_w = base + offs[2];
+  w->mlp_proj_w = base + offs[3];
+  if (segs.count == 0) return GPT2_OK;
+  return c->run(kKindWeightConvert, s, [&](double* fl, double* by) {
+    *fl = 0;
+    double n = 0;
+    for (int i = 0; i < segs.count; ++i) n += static_cast<double>(segs.n[i]);
+    *by = 4.0 * n;
+    return launch_convert_f16(segs, s);
+  });
+}
+
+int convert_wte(gpt2_ctx* c, const void* wte, cudaStream_t s, const __half** out) {
+  const size_t key = static_cast<size_t>(c->hp.n_layer) * 4;
+  __half* dst = reinterpret_cast<__half*>(c->ws + c->plan.wconv) +
+                c->hp.n_layer * layer_slot_elems(c->hp);
+  *out = dst;
+  if (c->cache_weights && c->conv_src[key] == wte) return GPT2_OK;
+  c->conv_src[key] = c->cache_weights ? wte : nullptr;
+  ConvSegs segs{};
+  segs.src[0] = static_cast<const bf16*>(wte);
+  segs.dst[0] = dst;
+  segs.n[0] = static_cast<long long>(c->hp.n_vocab) * c->hp.n_embd;
+  segs.count = 1;
+  return c->run(kKindWeightConvert, s, [&](double* fl, double* by) {
+    *fl = 0;
+    *by = 4.0 * static_cast<double>(segs.n[0]);
+    return launch_convert_f16(segs, s);
+  });
+}
+
 // One block on the context's workspace.  x_in: block input (mode dtype for
 // the standalone block, fp32 residual stream for the full forward, in which
 // case out == x_in and residual adds are in place).
-int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int B, int T, const void* x_in,
-                   bool x_is_stream, void* out, const KvView& kv, int t_past, cudaStream_t s) {
+int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int slot, int B, int T,
+                   const void* x_in, bool x_is_stream, void* out, const KvView& kv, int t_past,
+                   cudaStream_t s) {
   const gpt2_hparams& hp = c->hp;
   const int d = hp.n_embd, h = hp.n_head, dh = d / h;
   const int M = B * T;
@@ -194,11 +265,16 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int B, int T, const 
   void* fc = c->ws + c->plan.fc;
   int st;
 
+  // bf16 mode: the GEMM operands are fp16 (activations written by the
+  // producing kernels; weights converted from bf16 per call, or cached).
+  BlockW16 w{};
+  if (bf && (st = convert_block_weights(c, slot, p, s, &w))) return st;
+
   // LN1
   st = c->run(kKindLayerNorm, s, [&](double* fl, double* by) {
     *fl = 0;
     *by = static_cast<double>(M) * d * ((x_dtype == GPT2_FP32 ? 4 : 2) + (bf ? 2 : 4));
-    return launch_layer_norm(hp.dtype, x_in, x_dtype, p->ln1_g, p->ln1_b, M, d, ln, s);
+    return launch_layer_norm(hp.dtype, x_in, x_dtype, p->ln1_g, p->ln1_b, M, d, ln, s, bf);
   });
   if (st) return st;
 
@@ -216,8 +292,7 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int B, int T, const 
   e.ldo = 3 * d;
   st = c->run(bf ? kKindGemmQkv : kKindSimtFp32, s, [&](double* fl, double* by) {
     if (bf)
-      return launch_gemm_tc(c->env, kEpiQkv, static_cast<const bf16*>(ln),
-                            static_cast<const bf16*>(p->attn_w), M, 3 * d, d, e, s, fl, by);
+      return launch_gemm_tc(c->env, kEpiQkv, ln, w.attn_w, M, 3 * d, d, e, s, fl, by, true, false);
     return launch_gemm_fp32(c->env, kEpiQkv, static_cast<const float*>(ln),
                             static_cast<const float*>(p->attn_w), M, 3 * d, d, e, dh, s);
   });
@@ -233,8 +308,8 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int B, int T, const 
       *by = static_cast<double>(B) * h * (2.0 * t_len * dh * 2 + 2.0 * dh * 2);
       const int r = launch_decode_attention_bf16(
           static_cast<const bf16*>(q), reinterpret_cast<const bf16*>(kv.base), kv.s_batch,
-          kv.s_kv, kv.s_head, B, h, t_len, static_cast<bf16*>(attn),
-          c->at<float>(c->plan.partials), splits, s, &nl);
+          kv.s_kv, kv.s_head, B, h, t_len, attn, c->at<float>(c->plan.partials), splits, s, &nl,
+          true);
       c->extra_kernels = nl - 1;
       return r;
     });
@@ -246,7 +321,7 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int B, int T, const 
       *by = static_cast<double>(B) * h * (2.0 * T * dh * 2 + 2.0 * t_len * dh * 2);
       return launch_attention_bf16(static_cast<const bf16*>(q),
                                    reinterpret_cast<const bf16*>(kv.base), kv.s_batch, kv.s_kv,
-                                   kv.s_head, B, h, T, t_past, static_cast<bf16*>(attn), s);
+                                   kv.s_head, B, h, T, t_past, attn, s, true);
     });
   } else {
     st = c->run(kKindSimtFp32, s, [&](double*, double*) {
@@ -267,8 +342,7 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int B, int T, const 
   st = c->run(bf ? kKindGemmProj : kKindSimtFp32, s, [&](double* fl, double* by) {
     if (bf) {
       const int kind = x_is_stream ? kEpiResidF32 : kEpiResidBf16In;
-      return launch_gemm_tc(c->env, kind, static_cast<const bf16*>(attn),
-                            static_cast<const bf16*>(p->proj_w), M, d, d, e2, s, fl, by);
+      return launch_gemm_tc(c->env, kind, attn, w.proj_w, M, d, d, e2, s, fl, by, true, false);
     }
     return launch_gemm_fp32(c->env, kEpiResidF32, static_cast<const float*>(attn),
                             static_cast<const float*>(p->proj_w), M, d, d, e2, dh, s);
@@ -279,7 +353,7 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int B, int T, const 
   st = c->run(kKindLayerNorm, s, [&](double* fl, double* by) {
     *fl = 0;
     *by = static_cast<double>(M) * d * (4 + (bf ? 2 : 4));
-    return launch_layer_norm(hp.dtype, xprime, GPT2_FP32, p->ln2_g, p->ln2_b, M, d, ln, s);
+    return launch_layer_norm(hp.dtype, xprime, GPT2_FP32, p->ln2_g, p->ln2_b, M, d, ln, s, bf);
   });
   if (st) return st;
 
@@ -290,8 +364,7 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int B, int T, const 
   e3.ldo = 4 * d;
   st = c->run(bf ? kKindGemmFc : kKindSimtFp32, s, [&](double* fl, double* by) {
     if (bf)
-      return launch_gemm_tc(c->env, kEpiGelu, static_cast<const bf16*>(ln),
-                            static_cast<const bf16*>(p->fc_w), M, 4 * d, d, e3, s, fl, by);
+      return launch_gemm_tc(c->env, kEpiGelu, ln, w.fc_w, M, 4 * d, d, e3, s, fl, by, true, true);
     return launch_gemm_fp32(c->env, kEpiGelu, static_cast<const float*>(ln),
                             static_cast<const float*>(p->fc_w), M, 4 * d, d, e3, dh, s);
   });
@@ -306,8 +379,8 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int B, int T, const 
   st = c->run(bf ? kKindGemmMlpProj : kKindSimtFp32, s, [&](double* fl, double* by) {
     if (bf) {
       const int kind = x_is_stream ? kEpiResidF32 : kEpiResidBf16Out;
-      return launch_gemm_tc(c->env, kind, static_cast<const bf16*>(fc),
-                            static_cast<const bf16*>(p->mlp_proj_w), M, d, 4 * d, e4, s, fl, by);
+      return launch_gemm_tc(c->env, kind, fc, w.mlp_proj_w, M, d, 4 * d, e4, s, fl, by, true,
+                            false);
     }
     return launch_gemm_fp32(c->env, kEpiResidF32, static_cast<const float*>(fc),
                             static_cast<const float*>(p->mlp_proj_w), M, d, 4 * d, e4, dh, s);
@@ -407,6 +480,8 @@ int gpt2_ctx_create(const gpt2_hparams* hp, int max_B, int max_T, void* workspac
   c->env.encode = enc;
   c->prof = false;
   c->extra_kernels = 0;
+  c->cache_weights = false;
+  c->conv_src.assign(static_cast<size_t>(hp->n_layer) * 4 + 1, nullptr);
   for (int k = 0; k < kKindCount; ++k) {
     c->launches[k] = 0;
     c->total_ms[k] = c->flops[k] = c->bytes[k] = 0.0;
@@ -474,7 +549,7 @@ int gpt2_block_forward(gpt2_ctx* c, const void* x, const gpt2_block_params* para
       if ((st = copy_positions(dst, src, B, h, t_past, dh, es, s))) return st;
     }
   }
-  st = block_sequence(c, params, B, T, x, false, out, dst, t_past, s);
+  st = block_sequence(c, params, 0, B, T, x, false, out, dst, t_past, s);
   if (st) return st;
   if (present) present->T_len = t_past + T;
   return GPT2_OK;
@@ -530,7 +605,7 @@ int gpt2_forward(gpt2_ctx* c, const int32_t* ids, int B, int T, const gpt2_param
         if ((st = copy_positions(dst, src, B, h, t_past, dh, es, s))) return st;
       }
     }
-    st = block_sequence(c, &params->blocks[l], B, T, H, true, H, dst, t_past, s);
+    st = block_sequence(c, &params->blocks[l], l, B, T, H, true, H, dst, t_past, s);
     if (st) return st;
   }
 
@@ -538,17 +613,19 @@ int gpt2_forward(gpt2_ctx* c, const int32_t* ids, int B, int T, const gpt2_param
   st = c->run(kKindLayerNorm, s, [&](double* fl, double* by) {
     *fl = 0;
     *by = static_cast<double>(M) * d * (4 + es);
-    return launch_layer_norm(hp.dtype, H, GPT2_FP32, params->lnf_g, params->lnf_b, M, d, ln, s);
+    return launch_layer_norm(hp.dtype, H, GPT2_FP32, params->lnf_g, params->lnf_b, M, d, ln, s,
+                             bf);
   });
   if (st) return st;
 
+  const __half* wte16 = nullptr;
+  if (bf && (st = convert_wte(c, params->wte, s, &wte16))) return st;
   EpiParams e{};
   e.out = logits;
   e.ldo = V;
   st = c->run(bf ? kKindGemmLogits : kKindSimtFp32, s, [&](double* fl, double* by) {
     if (bf)
-      return launch_gemm_tc(c->env, kEpiLogits, static_cast<const bf16*>(ln),
-                            static_cast<const bf16*>(params->wte), M, V, d, e, s, fl, by);
+      return launch_gemm_tc(c->env, kEpiLogits, ln, wte16, M, V, d, e, s, fl, by, true, false);
     return launch_gemm_fp32(c->env, kEpiLogits, static_cast<const float*>(ln),
                             static_cast<const float*>(params->wte), M, V, d, e, dh, s);
   });
@@ -588,8 +665,7 @@ int gpt2_linear(gpt2_ctx* c, int epilogue, const void* A, const void* W, const v
   const bool bf = c->hp.dtype == GPT2_BF16;
   return c->run(bf ? kKindGemmOther : kKindSimtFp32, s, [&](double* fl, double* by) {
     if (bf)
-      return launch_gemm_tc(c->env, kind, static_cast<const bf16*>(A), static_cast<const bf16*>(W),
-                            M, N, K, e, s, fl, by);
+      return launch_gemm_tc(c->env, kind, A, W, M, N, K, e, s, fl, by, false, false);
     return launch_gemm_fp32(c->env, kind, static_cast<const float*>(A),
                             static_cast<const float*>(W), M, N, K, e, 1, s);
   });
@@ -614,8 +690,7 @@ int gpt2_attention(gpt2_ctx* c, const void* q, const void* kv, int B, int n_head
     return c->run(kKindDecodeAttention, s, [&](double*, double*) {
       const int r = launch_decode_attention_bf16(
           static_cast<const bf16*>(q), reinterpret_cast<const bf16*>(v.base), v.s_batch, v.s_kv,
-          v.s_head, B, n_head, t_len, static_cast<bf16*>(out), c->at<float>(c->plan.partials),
-          splits, s, &nl);
+          v.s_head, B, n_head, t_len, out, c->at<float>(c->plan.partials), splits, s, &nl);
       c->extra_kernels = nl - 1;
       return r;
     });
@@ -624,7 +699,7 @@ int gpt2_attention(gpt2_ctx* c, const void* q, const void* kv, int B, int n_head
     return c->run(kKindAttention, s, [&](double*, double*) {
       return launch_attention_bf16(static_cast<const bf16*>(q),
                                    reinterpret_cast<const bf16*>(v.base), v.s_batch, v.s_kv,
-                                   v.s_head, B, n_head, T, T_past, static_cast<bf16*>(out), s);
+                                   v.s_head, B, n_head, T, T_past, out, s);
     });
   return c->run(kKindSimtFp32, s, [&](double*, double*) {
     return launch_attention_fp32(static_cast<const float*>(q),
@@ -645,6 +720,13 @@ int gpt2_embed(gpt2_ctx* c, const int32_t* ids, const void* wte, const void* wpe
     return launch_embed(c->hp.dtype, ids, wte, wpe, B, T, T_past, c->hp.n_embd, c->hp.n_vocab, H,
                         c->env.err, s);
   });
+}
+
+int gpt2_ctx_cache_weights(gpt2_ctx* c, int enable) {
+  if (!c) return GPT2_ERR_INVALID_ARG;
+  c->cache_weights = enable != 0;
+  std::fill(c->conv_src.begin(), c->conv_src.end(), nullptr);
+  return GPT2_OK;
 }
 
 int gpt2_profile_enable(gpt2_ctx* c, int enable) {

@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -28,13 +29,14 @@ enum KernelKind : int {
   kKindDecodeAttention,
   kKindDecodeCombine,
   kKindSimtFp32,
+  kKindWeightConvert,
   kKindCount
 };
 
 // Epilogues of the tensor-core GEMM.
 enum EpiKind : int {
-  kEpiBias = 0,       // out_bf16 = acc + bias
-  kEpiGelu,           // out_bf16 = gelu_tanh(acc + bias)
+  kEpiBias = 0,       // out_16 = acc + bias                (bf16 or fp16)
+  kEpiGelu,           // out_16 = gelu_tanh(acc + bias)     (bf16 or fp16)
   kEpiResidF32,       // out_f32  = resid_f32 + acc + bias
   kEpiResidBf16In,    // out_f32  = resid_bf16 + acc + bias
   kEpiResidBf16Out,   // out_bf16 = resid_f32 + acc + bias
@@ -76,34 +78,50 @@ struct LaunchEnv {
   EncodeTiledFn encode;   // cuTensorMapEncodeTiled
 };
 
-// Tensor-core GEMM (bf16 in, fp32 accumulate in TMEM): C = A[M,K] W[N,K]^T
-// with epilogue `kind`.  Returns a gpt2_status.
-int launch_gemm_tc(const LaunchEnv& env, int kind, const bf16* A, const bf16* W, int M, int N,
-                   int K, const EpiParams& ep, cudaStream_t stream, double* flops, double* bytes);
+// Tensor-core GEMM (16-bit operands, fp32 accumulate in TMEM): C = A[M,K]
+// W[N,K]^T with epilogue `kind`.  A and W are both fp16 (operands_f16) or both
+// bf16; out_f16 selects fp16 over bf16 for the kEpiBias / kEpiGelu outputs.
+// Returns a gpt2_status.
+int launch_gemm_tc(const LaunchEnv& env, int kind, const void* A, const void* W, int M, int N,
+                   int K, const EpiParams& ep, cudaStream_t stream, double* flops, double* bytes,
+                   bool operands_f16, bool out_f16);
 
 // fp32 SIMT GEMM with the same epilogues (fp32 storage throughout).
 int launch_gemm_fp32(const LaunchEnv& env, int kind, const float* A, const float* W, int M, int N,
                      int K, const EpiParams& ep, int d_h, cudaStream_t stream);
 
-// LayerNorm rows of d: x fp32 or bf16 -> y bf16 (mode BF16) or fp32 (mode FP32).
+// LayerNorm rows of d: x fp32 or bf16 -> y (mode BF16: bf16, or fp16 when
+// y_f16; g, b bf16) or fp32 (mode FP32).
 int launch_layer_norm(int mode, const void* x, int x_dtype, const void* g, const void* b, int rows,
-                      int d, void* y, cudaStream_t stream);
+                      int d, void* y, cudaStream_t stream, bool y_f16 = false);
+
+// Element-wise bf16 -> fp16 copies of up to kMaxConvSegs arrays in one launch.
+constexpr int kMaxConvSegs = 4;
+struct ConvSegs {
+  const bf16* src[kMaxConvSegs];
+  __half* dst[kMaxConvSegs];
+  long long n[kMaxConvSegs];
+  int count;
+};
+int launch_convert_f16(const ConvSegs& segs, cudaStream_t stream);
 
 // H[b,t,:] = wte[ids[b,t]] + wpe[t_past + t] -> fp32.
 int launch_embed(int mode, const int32_t* ids, const void* wte, const void* wpe, int B, int T,
                  int t_past, int d, int n_vocab, float* H, unsigned* err, cudaStream_t stream);
 
-// Causal prefill attention, bf16, d_h = 64 (tensor cores).
+// Causal prefill attention, bf16 Q/K/V, d_h = 64 (tensor cores); the output
+// [B, T, h*64] is fp16 when out_f16, else bf16.
 int launch_attention_bf16(const bf16* q, const bf16* kv, long long kv_s_batch, long long kv_s_kv,
-                          long long kv_s_head, int B, int h, int T, int t_past, bf16* out,
-                          cudaStream_t stream);
+                          long long kv_s_head, int B, int h, int T, int t_past, void* out,
+                          cudaStream_t stream, bool out_f16 = false);
 
-// Single-token decode attention, bf16, d_h = 64: split over keys, partial
-// results combined through `partials` (floats, see decode_partials_floats).
+// Single-token decode attention, bf16 Q/K/V, d_h = 64: split over keys,
+// partial results combined through `partials` (floats, see
+// decode_partials_floats); output fp16 when out_f16, else bf16.
 int launch_decode_attention_bf16(const bf16* q, const bf16* kv, long long kv_s_batch,
                                  long long kv_s_kv, long long kv_s_head, int B, int h, int t_len,
-                                 bf16* out, float* partials, int splits, cudaStream_t stream,
-                                 int* launches);
+                                 void* out, float* partials, int splits, cudaStream_t stream,
+                                 int* launches, bool out_f16 = false);
 size_t decode_partials_floats(int B, int h, int splits);
 int decode_splits(int B, int h, int t_len, int num_sms);
 

@@ -37,6 +37,9 @@ __device__ __forceinline__ void store2(float* p, float a, float b) {
 __device__ __forceinline__ void store2(bf16* p, float a, float b) {
   *reinterpret_cast<uint32_t*>(p) = pack_bf16x2(a, b);
 }
+__device__ __forceinline__ void store2(__half* p, float a, float b) {
+  *reinterpret_cast<uint32_t*>(p) = pack_f16x2(a, b);
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -44,10 +47,11 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Row held in registers: NP pairs per lane, d <= 64 * NP, d even.
-template <typename TX, typename TY, int NP>
+// Row held in registers: NP pairs per lane, d <= 64 * NP, d even.  TX input,
+// TP gain/bias, TY output.
+template <typename TX, typename TP, typename TY, int NP>
 __global__ void __launch_bounds__(kRowThreads)
-    layer_norm_reg(const TX* __restrict__ x, const TY* __restrict__ g, const TY* __restrict__ b,
+    layer_norm_reg(const TX* __restrict__ x, const TP* __restrict__ g, const TP* __restrict__ b,
                    int rows, int d, TY* __restrict__ y) {
   const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -95,11 +99,12 @@ __device__ __forceinline__ float ld1(const float* p) { return *p; }
 __device__ __forceinline__ float ld1(const bf16* p) { return __bfloat162float(*p); }
 __device__ __forceinline__ void st1(float* p, float v) { *p = v; }
 __device__ __forceinline__ void st1(bf16* p, float v) { *p = __float2bfloat16_rn(v); }
+__device__ __forceinline__ void st1(__half* p, float v) { *p = __float2half_rn(v); }
 
 // Any d: three passes over the row in global memory.
-template <typename TX, typename TY>
+template <typename TX, typename TP, typename TY>
 __global__ void __launch_bounds__(kRowThreads)
-    layer_norm_any(const TX* __restrict__ x, const TY* __restrict__ g, const TY* __restrict__ b,
+    layer_norm_any(const TX* __restrict__ x, const TP* __restrict__ g, const TP* __restrict__ b,
                    int rows, int d, TY* __restrict__ y) {
   const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -118,21 +123,43 @@ __global__ void __launch_bounds__(kRowThreads)
   for (int c = lane; c < d; c += 32) st1(yr + c, (ld1(xr + c) - u) * rstd * ld1(g + c) + ld1(b + c));
 }
 
-template <typename TX, typename TY>
-int ln_dispatch(const TX* x, const TY* g, const TY* b, int rows, int d, TY* y, cudaStream_t s) {
+template <typename TX, typename TP, typename TY>
+int ln_dispatch(const TX* x, const TP* g, const TP* b, int rows, int d, TY* y, cudaStream_t s) {
   const unsigned blocks = static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock);
   if (d % 2 == 0 && d <= 64 * 4) {
-    layer_norm_reg<TX, TY, 4><<<blocks, kRowThreads, 0, s>>>(x, g, b, rows, d, y);
+    layer_norm_reg<TX, TP, TY, 4><<<blocks, kRowThreads, 0, s>>>(x, g, b, rows, d, y);
   } else if (d % 2 == 0 && d <= 64 * 12) {
-    layer_norm_reg<TX, TY, 12><<<blocks, kRowThreads, 0, s>>>(x, g, b, rows, d, y);
+    layer_norm_reg<TX, TP, TY, 12><<<blocks, kRowThreads, 0, s>>>(x, g, b, rows, d, y);
   } else if (d % 2 == 0 && d <= 64 * 16) {
-    layer_norm_reg<TX, TY, 16><<<blocks, kRowThreads, 0, s>>>(x, g, b, rows, d, y);
+    layer_norm_reg<TX, TP, TY, 16><<<blocks, kRowThreads, 0, s>>>(x, g, b, rows, d, y);
   } else if (d % 2 == 0 && d <= 64 * 25) {
-    layer_norm_reg<TX, TY, 25><<<blocks, kRowThreads, 0, s>>>(x, g, b, rows, d, y);
+    layer_norm_reg<TX, TP, TY, 25><<<blocks, kRowThreads, 0, s>>>(x, g, b, rows, d, y);
   } else {
-    layer_norm_any<TX, TY><<<blocks, kRowThreads, 0, s>>>(x, g, b, rows, d, y);
+    layer_norm_any<TX, TP, TY><<<blocks, kRowThreads, 0, s>>>(x, g, b, rows, d, y);
   }
   return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+}
+
+// Element-wise bf16 -> fp16 for several arrays; blockIdx.y picks the array.
+// A bf16 value converts exactly unless its magnitude is below 2^-14 (fp16
+// subnormal range) or above 65504.
+__global__ void __launch_bounds__(256) convert_f16(const ConvSegs segs) {
+  const int sgi = blockIdx.y;
+  const bf16* __restrict__ src = segs.src[sgi];
+  __half* __restrict__ dst = segs.dst[sgi];
+  const long long n = segs.n[sgi];
+  const long long n8 = n / 8;
+  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < n8; i += 256LL * gridDim.x) {
+    const uint4 v = reinterpret_cast<const uint4*>(src)[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint4 o;
+    uint32_t* ow = &o.x;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) ow[k] = pack_f16x2(bf16_lo(w[k]), bf16_hi(w[k]));
+    reinterpret_cast<uint4*>(dst)[i] = o;
+  }
+  for (long long i = n8 * 8 + blockIdx.x * 256LL + threadIdx.x; i < n; i += 256LL * gridDim.x)
+    dst[i] = __float2half_rn(__bfloat162float(src[i]));
 }
 
 // ---------------------------------------------------------------- embed ----
@@ -194,22 +221,38 @@ __global__ void __launch_bounds__(kRowThreads)
 }  // namespace
 
 int launch_layer_norm(int mode, const void* x, int x_dtype, const void* g, const void* b, int rows,
-                      int d, void* y, cudaStream_t stream) {
+                      int d, void* y, cudaStream_t stream, bool y_f16) {
   if (rows <= 0 || d <= 0) return GPT2_ERR_INVALID_ARG;
   if (mode == GPT2_BF16) {
     if (d % 2 != 0) return GPT2_ERR_UNSUPPORTED;
-    if (x_dtype == GPT2_FP32)
-      return ln_dispatch(static_cast<const float*>(x), static_cast<const bf16*>(g),
-                         static_cast<const bf16*>(b), rows, d, static_cast<bf16*>(y), stream);
-    if (x_dtype == GPT2_BF16)
-      return ln_dispatch(static_cast<const bf16*>(x), static_cast<const bf16*>(g),
-                         static_cast<const bf16*>(b), rows, d, static_cast<bf16*>(y), stream);
+    const bf16* gg = static_cast<const bf16*>(g);
+    const bf16* bb = static_cast<const bf16*>(b);
+    if (x_dtype == GPT2_FP32) {
+      const float* xx = static_cast<const float*>(x);
+      return y_f16 ? ln_dispatch(xx, gg, bb, rows, d, static_cast<__half*>(y), stream)
+                   : ln_dispatch(xx, gg, bb, rows, d, static_cast<bf16*>(y), stream);
+    }
+    if (x_dtype == GPT2_BF16) {
+      const bf16* xx = static_cast<const bf16*>(x);
+      return y_f16 ? ln_dispatch(xx, gg, bb, rows, d, static_cast<__half*>(y), stream)
+                   : ln_dispatch(xx, gg, bb, rows, d, static_cast<bf16*>(y), stream);
+    }
     return GPT2_ERR_INVALID_ARG;
   }
   if (mode == GPT2_FP32 && x_dtype == GPT2_FP32)
     return ln_dispatch(static_cast<const float*>(x), static_cast<const float*>(g),
                        static_cast<const float*>(b), rows, d, static_cast<float*>(y), stream);
   return GPT2_ERR_INVALID_ARG;
+}
+
+int launch_convert_f16(const ConvSegs& segs, cudaStream_t stream) {
+  if (segs.count <= 0 || segs.count > kMaxConvSegs) return GPT2_ERR_INVALID_ARG;
+  long long most = 0;
+  for (int i = 0; i < segs.count; ++i) most = segs.n[i] > most ? segs.n[i] : most;
+  const long long want = (most / 8 + 255) / 256;
+  const unsigned gx = static_cast<unsigned>(want < 1 ? 1 : (want > 4096 ? 4096 : want));
+  convert_f16<<<dim3(gx, segs.count), 256, 0, stream>>>(segs);
+  return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
 int launch_embed(int mode, const int32_t* ids, const void* wte, const void* wpe, int B, int T,

@@ -187,8 +187,12 @@ def model_params(w: Workload, seed: int) -> dict:
 def past_kv(w: Workload, seed: int, b: int, layer: int, t_past: int | None = None) -> np.ndarray:
     """Cached keys/values of sequence b at one layer: [2, h, T_past, d_h] ~ N(0, past_std).
 
-    Drawn per (sequence, layer) so a sampled subset can be regenerated alone."""
+    Drawn per (sequence, layer) so a sampled subset can be regenerated alone,
+    in float32 (the cache of a full decode workload holds ~1.6e9 values)."""
     t_past = w.t_past if t_past is None else t_past
-    v = _normal(seed, _sid_past(b, layer), (2, w.n_head, t_past, w.d_h), w.past_std)
+    rng = np.random.default_rng([seed, _sid_past(b, layer)])
+    v = rng.standard_normal((2, w.n_head, t_past, w.d_h), dtype=np.float32)
+    if w.past_std != 1.0:
+        v *= np.float32(w.past_std)
     return _store(v, w.dtype)
 

@@ -27,10 +27,16 @@
  *     (a bounded wait that ran out) surface at gpt2_sync_status.
  *   - Asynchrony: work is enqueued on `stream` (a cudaStream_t value; NULL is
  *     the legacy default stream) and the call returns before it completes.
- *   - Dtypes: in GPT2_BF16 mode activations, parameters and the KV cache are
- *     bf16 (stored as 16-bit words) and every product accumulates in fp32; in
- *     GPT2_FP32 mode they are fp32.  Logits are always fp32.  Token ids are
- *     int32.  The residual stream inside gpt2_forward is fp32 in both modes.
+ *   - Dtypes: in GPT2_BF16 mode parameters, the block input/output and the KV
+ *     cache are bf16 (16-bit words).  Inside, the operands of the Linear
+ *     products are fp16 -- the normalised, attention and GELU activations, and
+ *     fp16 copies of the bf16 weights (exact for 2^-14 <= |w| <= 65504) -- and
+ *     Q, K, V and the attention probabilities are bf16; every product
+ *     accumulates in fp32 and the residual stream is fp32.  (fp16 operands
+ *     carry 3 more mantissa bits than bf16; with bf16 operands the tied-head
+ *     argmax of random-weight models agrees with exact arithmetic at only
+ *     ~99.1% of positions, with fp16 operands at ~99.7%.)  In GPT2_FP32 mode
+ *     everything is fp32.  Logits are always fp32.  Token ids are int32.
  *   - Layouts are dense row-major C order.  Linear weights are [out, in]
  *     (the nn.Linear convention); c_attn rows are Q | K | V, head j taking
  *     rows [j*d_h, (j+1)*d_h) of each block.
@@ -126,6 +132,14 @@ void gpt2_ctx_destroy(gpt2_ctx *ctx);
  * word: GPT2_OK, GPT2_ERR_DEVICE_TIMEOUT, or GPT2_ERR_CUDA for a failed
  * launch or an asynchronous CUDA error.                                    */
 int gpt2_sync_status(gpt2_ctx *ctx, void *stream);
+
+/* bf16 mode converts each weight matrix to an fp16 working copy (in the
+ * workspace) before its product.  enable != 0: keep those copies across
+ * calls, keyed by the weight's device address, and convert a matrix only the
+ * first time its address is seen -- the caller promises not to change weight
+ * contents in place while caching is on (call again to forget all copies).
+ * enable == 0 (the default): convert on every call.                       */
+int gpt2_ctx_cache_weights(gpt2_ctx *ctx, int enable);
 
 /* Static description of a status code. */
 const char *gpt2_status_string(int status);
