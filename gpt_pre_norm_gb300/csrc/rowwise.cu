@@ -140,26 +140,36 @@ int ln_dispatch(const TX* x, const TP* g, const TP* b, int rows, int d, TY* y, c
   return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 v) {
+  return make_uint4(pack_f16x2(bf16_lo(v.x), bf16_hi(v.x)), pack_f16x2(bf16_lo(v.y), bf16_hi(v.y)),
+                    pack_f16x2(bf16_lo(v.z), bf16_hi(v.z)), pack_f16x2(bf16_lo(v.w), bf16_hi(v.w)));
+}
+
 // Element-wise bf16 -> fp16 for several arrays; blockIdx.y picks the array.
-// A bf16 value converts exactly unless its magnitude is below 2^-14 (fp16
+// Grid-stride over 16-byte chunks with four loads in flight per thread.  A
+// bf16 value converts exactly unless its magnitude is below 2^-14 (fp16
 // subnormal range) or above 65504.
 __global__ void __launch_bounds__(256) convert_f16(const ConvSegs segs) {
   const int sgi = blockIdx.y;
-  const bf16* __restrict__ src = segs.src[sgi];
-  __half* __restrict__ dst = segs.dst[sgi];
+  const uint4* __restrict__ src = reinterpret_cast<const uint4*>(segs.src[sgi]);
+  uint4* __restrict__ dst = reinterpret_cast<uint4*>(segs.dst[sgi]);
   const long long n = segs.n[sgi];
   const long long n8 = n / 8;
-  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < n8; i += 256LL * gridDim.x) {
-    const uint4 v = reinterpret_cast<const uint4*>(src)[i];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint4 o;
-    uint32_t* ow = &o.x;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) ow[k] = pack_f16x2(bf16_lo(w[k]), bf16_hi(w[k]));
-    reinterpret_cast<uint4*>(dst)[i] = o;
+  const long long stride = 256LL * gridDim.x;
+  long long i = blockIdx.x * 256LL + threadIdx.x;
+  for (; i + 3 * stride < n8; i += 4 * stride) {
+    const uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride], d = src[i + 3 * stride];
+    dst[i] = bf16x8_to_f16x8(a);
+    dst[i + stride] = bf16x8_to_f16x8(b);
+    dst[i + 2 * stride] = bf16x8_to_f16x8(c);
+    dst[i + 3 * stride] = bf16x8_to_f16x8(d);
   }
-  for (long long i = n8 * 8 + blockIdx.x * 256LL + threadIdx.x; i < n; i += 256LL * gridDim.x)
-    dst[i] = __float2half_rn(__bfloat162float(src[i]));
+  for (; i < n8; i += stride) dst[i] = bf16x8_to_f16x8(src[i]);
+  if (blockIdx.x == 0) {
+    const bf16* s1 = segs.src[sgi];
+    __half* d1 = segs.dst[sgi];
+    for (long long j = n8 * 8 + threadIdx.x; j < n; j += 256) d1[j] = __float2half_rn(__bfloat162float(s1[j]));
+  }
 }
 
 // ---------------------------------------------------------------- embed ----
@@ -249,8 +259,9 @@ int launch_convert_f16(const ConvSegs& segs, cudaStream_t stream) {
   if (segs.count <= 0 || segs.count > kMaxConvSegs) return GPT2_ERR_INVALID_ARG;
   long long most = 0;
   for (int i = 0; i < segs.count; ++i) most = segs.n[i] > most ? segs.n[i] : most;
-  const long long want = (most / 8 + 255) / 256;
-  const unsigned gx = static_cast<unsigned>(want < 1 ? 1 : (want > 4096 ? 4096 : want));
+  // About four 16-byte chunks per thread for the largest array.
+  const long long want = (most / 8 + 1023) / 1024;
+  const unsigned gx = static_cast<unsigned>(want < 1 ? 1 : (want > 2048 ? 2048 : want));
   convert_f16<<<dim3(gx, segs.count), 256, 0, stream>>>(segs);
   return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }

@@ -100,7 +100,8 @@ def test_linear_gelu_bf16(G, M, N, K):
     assert_bf16_close(host(out), O.gelu(O.linear(A, W, bias)), what="linear+gelu")
 
 
-@pytest.mark.parametrize("M,V", [(130, 50257), (1, 50257), (256, 1000)])
+@pytest.mark.parametrize("M,V", [(130, 50257), (1, 50257), (3, 50257), (256, 1000), (77, 1001),
+                                 (200, 1002), (33, 1003), (5, 40)])
 def test_tied_head_logits(G, M, V):
     rng = np.random.default_rng(M + V)
     ctx = _ctx(G, G.GPT2_BF16, V=V)
