@@ -285,6 +285,23 @@ class Runner:
         return self.ids.numel() * 4, self.logits.numel() * 4
 
 
+def reduce_over_ranks(times_ms, device):
+    """Maximum of each per-step time over all ranks (the slowest rank sets the
+    whole job's step time); a no-op without a process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(t) for t in times_ms]
+    t = torch.tensor(times_ms, device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_throughput(tokens_per_rank, world_size, ms_per_step):
+    """Whole-job tokens/s: every rank processes its own replica's tokens."""
+    return tokens_per_rank * world_size / (ms_per_step / 1e3)
+
+
 def timed_steps(fn, K, flush, barrier, torch):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -444,17 +461,13 @@ def main():
     if st != G.GPT2_OK:
         raise SystemExit(f"device error in the timed region: {G.status_string(st)}")
 
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms, ms_e2e], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_e2e = float(t[0]), float(t[1])
+    ms, ms_e2e = reduce_over_ranks([ms, ms_e2e], device)
     if rank != 0:
         return 0
 
     peaks = load_peaks()
     tokens = r.tokens * ws
-    value = tokens / (ms / 1e3)
+    value = job_throughput(r.tokens, ws, ms)
     flops = workload_flops(w)
     kernels = {}
     for kind, rec in prof.items():
@@ -496,7 +509,8 @@ def main():
         "tflops": flops * ws / (ms / 1e3) / 1e12,
         "tflops_frac_of_bf16_peak": flops * ws / (ms / 1e3) / 1e12 / peaks["bf16_tflops"],
         "roofline": roof,
-        "e2e": {"value": tokens / (ms_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_throughput(r.tokens, ws, ms_e2e), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": int(round(launches)),
         "clocks": clk.summary(),
