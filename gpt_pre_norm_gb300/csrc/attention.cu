@@ -51,6 +51,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   __shared__ __align__(128) uint8_t sQ[kQTile * 128];
   __shared__ __align__(128) uint8_t sK[2][kKTile * 128];
   __shared__ __align__(128) uint8_t sV[2][kKTile * 128];
+  pdl_trigger();
+  pdl_wait();
 
   const int bh = blockIdx.x;
   const int qt = n_qtiles - 1 - static_cast<int>(blockIdx.y);  // most keys first
@@ -236,6 +238,8 @@ __global__ void __launch_bounds__(kDecThreads)
                      uint16_t* __restrict__ out, float* __restrict__ partials, int out_f16) {
   __shared__ float s_m[kDecWarps], s_l[kDecWarps];
   __shared__ float s_o[kDecWarps][kDh];
+  pdl_trigger();
+  pdl_wait();
 
   const int split = blockIdx.x, splits = gridDim.x;
   const int bh = blockIdx.y;
@@ -362,6 +366,8 @@ __global__ void __launch_bounds__(kDecThreads)
 // One warp per (sequence, head): merges the splits' partial results.
 __global__ void attn_decode_combine(const float* __restrict__ partials, int n_bh, int splits,
                                     uint16_t* __restrict__ out, int out_f16) {
+  pdl_trigger();
+  pdl_wait();
   const int bh = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (bh >= n_bh) return;
@@ -387,6 +393,8 @@ constexpr int kF32MaxPerLane = 8;  // d_h <= 256
 __global__ void attn_fp32(const float* __restrict__ q, const float* __restrict__ kv,
                           long long s_batch, long long s_kv, long long s_head, int B, int h,
                           int T, int t_past, int dh, float* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);  // (b, head, i)
   const int lane = threadIdx.x & 31;
   if (row >= B * h * T) return;
@@ -445,10 +453,10 @@ int launch_attention_bf16(const bf16* q, const bf16* kv, long long s_batch, long
   const int n_qtiles = (T + kQTile - 1) / kQTile;
   if (n_qtiles > 65535) return GPT2_ERR_UNSUPPORTED;
   dim3 grid(B * h, n_qtiles);
-  attn_prefill_bf16<<<grid, kAttnThreads, 0, stream>>>(q, kv, s_batch, s_kv, s_head, h, T, t_past,
-                                                       static_cast<uint16_t*>(out), n_qtiles,
-                                                       out_f16 ? 1 : 0);
-  return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+  const cudaError_t e = launch_pdl(attn_prefill_bf16, grid, dim3(kAttnThreads), 0, stream, q, kv,
+                                   s_batch, s_kv, s_head, h, T, t_past,
+                                   static_cast<uint16_t*>(out), n_qtiles, out_f16 ? 1 : 0);
+  return e == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
 size_t decode_partials_floats(int B, int h, int splits) {
@@ -470,14 +478,17 @@ int launch_decode_attention_bf16(const bf16* q, const bf16* kv, long long s_batc
   if (splits > 1 && partials == nullptr) return GPT2_ERR_INVALID_ARG;
   const int chunk = (t_len + splits - 1) / splits;
   dim3 grid(splits, B * h);
-  attn_decode_bf16<<<grid, kDecThreads, 0, stream>>>(q, kv, s_batch, s_kv, s_head, h, t_len, chunk,
-                                                     static_cast<uint16_t*>(out), partials,
-                                                     out_f16 ? 1 : 0);
+  cudaError_t e = launch_pdl(attn_decode_bf16, grid, dim3(kDecThreads), 0, stream, q, kv, s_batch,
+                             s_kv, s_head, h, t_len, chunk, static_cast<uint16_t*>(out), partials,
+                             out_f16 ? 1 : 0);
+  if (e != cudaSuccess) return GPT2_ERR_CUDA;
   int n = 1;
   if (splits > 1) {
     const int n_bh = B * h;
-    attn_decode_combine<<<(n_bh + 7) / 8, 256, 0, stream>>>(
-        partials, n_bh, splits, static_cast<uint16_t*>(out), out_f16 ? 1 : 0);
+    e = launch_pdl(attn_decode_combine, dim3((n_bh + 7) / 8), dim3(256), 0, stream,
+                   static_cast<const float*>(partials), n_bh, splits,
+                   static_cast<uint16_t*>(out), out_f16 ? 1 : 0);
+    if (e != cudaSuccess) return GPT2_ERR_CUDA;
     ++n;
   }
   if (launches) *launches = n;
@@ -493,9 +504,10 @@ int launch_attention_fp32(const float* q, const float* kv, long long s_batch, lo
   const int warps_per_block = 8;
   const long long blocks = (rows + warps_per_block - 1) / warps_per_block;
   if (blocks > 0x7fffffffLL) return GPT2_ERR_UNSUPPORTED;
-  attn_fp32<<<static_cast<unsigned>(blocks), 32 * warps_per_block, 0, stream>>>(
-      q, kv, s_batch, s_kv, s_head, B, h, T, t_past, d_h, out);
-  return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+  const cudaError_t e = launch_pdl(attn_fp32, dim3(static_cast<unsigned>(blocks)),
+                                   dim3(32 * warps_per_block), 0, stream, q, kv, s_batch, s_kv,
+                                   s_head, B, h, T, t_past, d_h, out);
+  return e == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
 }  // namespace gpt2

@@ -34,6 +34,18 @@ __device__ __forceinline__ void raise_error(unsigned* err, unsigned bits) {
   if (err) atomicOr(err, bits);
 }
 
+// --------------------------------------------- programmatic dependent launch ----
+// A kernel launched with programmatic stream serialisation may start while
+// the previous kernel in the stream is still running.  pdl_wait() blocks
+// until that kernel has completed and its memory is visible; it must come
+// before this kernel's first global-memory access.  pdl_trigger() lets the
+// next kernel launch early (its CTAs start as ours retire).  Both are no-ops
+// for a kernel launched normally.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------- mbarrier ----
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

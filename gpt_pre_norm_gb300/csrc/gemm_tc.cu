@@ -360,6 +360,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Set-up above touched only shared memory and TMEM: let the next kernel
+  // launch, then wait for the previous one before any global access.
+  pdl_trigger();
+  pdl_wait();
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------- producer --
@@ -641,8 +645,17 @@ int launch_gemm_tc(const LaunchEnv& env, int kind, const void* A, const void* W,
   }
   const int grid = std::min(args.num_tiles, env.num_sms);
   void* params[] = {&tmA, &tmB, &tmO, &tmR, &tmQ, &tmKV, &args};
-  if (cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), params, smem, stream) != cudaSuccess)
-    return GPT2_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelExC(&cfg, fn, params) != cudaSuccess) return GPT2_ERR_CUDA;
 
   if (flops) *flops = 2.0 * M * N * static_cast<double>(K);
   if (bytes) {

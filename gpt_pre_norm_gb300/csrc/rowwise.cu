@@ -53,6 +53,8 @@ template <typename TX, typename TP, typename TY, int NP>
 __global__ void __launch_bounds__(kRowThreads)
     layer_norm_reg(const TX* __restrict__ x, const TP* __restrict__ g, const TP* __restrict__ b,
                    int rows, int d, TY* __restrict__ y) {
+  pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -106,6 +108,8 @@ template <typename TX, typename TP, typename TY>
 __global__ void __launch_bounds__(kRowThreads)
     layer_norm_any(const TX* __restrict__ x, const TP* __restrict__ g, const TP* __restrict__ b,
                    int rows, int d, TY* __restrict__ y) {
+  pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -126,18 +130,20 @@ __global__ void __launch_bounds__(kRowThreads)
 template <typename TX, typename TP, typename TY>
 int ln_dispatch(const TX* x, const TP* g, const TP* b, int rows, int d, TY* y, cudaStream_t s) {
   const unsigned blocks = static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock);
+  const dim3 grid(blocks), block(kRowThreads);
+  cudaError_t e;
   if (d % 2 == 0 && d <= 64 * 4) {
-    layer_norm_reg<TX, TP, TY, 4><<<blocks, kRowThreads, 0, s>>>(x, g, b, rows, d, y);
+    e = launch_pdl(layer_norm_reg<TX, TP, TY, 4>, grid, block, 0, s, x, g, b, rows, d, y);
   } else if (d % 2 == 0 && d <= 64 * 12) {
-    layer_norm_reg<TX, TP, TY, 12><<<blocks, kRowThreads, 0, s>>>(x, g, b, rows, d, y);
+    e = launch_pdl(layer_norm_reg<TX, TP, TY, 12>, grid, block, 0, s, x, g, b, rows, d, y);
   } else if (d % 2 == 0 && d <= 64 * 16) {
-    layer_norm_reg<TX, TP, TY, 16><<<blocks, kRowThreads, 0, s>>>(x, g, b, rows, d, y);
+    e = launch_pdl(layer_norm_reg<TX, TP, TY, 16>, grid, block, 0, s, x, g, b, rows, d, y);
   } else if (d % 2 == 0 && d <= 64 * 25) {
-    layer_norm_reg<TX, TP, TY, 25><<<blocks, kRowThreads, 0, s>>>(x, g, b, rows, d, y);
+    e = launch_pdl(layer_norm_reg<TX, TP, TY, 25>, grid, block, 0, s, x, g, b, rows, d, y);
   } else {
-    layer_norm_any<TX, TP, TY><<<blocks, kRowThreads, 0, s>>>(x, g, b, rows, d, y);
+    e = launch_pdl(layer_norm_any<TX, TP, TY>, grid, block, 0, s, x, g, b, rows, d, y);
   }
-  return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+  return e == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 v) {
@@ -150,6 +156,8 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 v) {
 // bf16 value converts exactly unless its magnitude is below 2^-14 (fp16
 // subnormal range) or above 65504.
 __global__ void __launch_bounds__(256) convert_f16(const ConvSegs segs) {
+  pdl_trigger();
+  pdl_wait();
   const int sgi = blockIdx.y;
   const uint4* __restrict__ src = reinterpret_cast<const uint4*>(segs.src[sgi]);
   uint4* __restrict__ dst = reinterpret_cast<uint4*>(segs.dst[sgi]);
@@ -186,6 +194,8 @@ __global__ void __launch_bounds__(kRowThreads)
     embed_bf16(const int32_t* __restrict__ ids, const bf16* __restrict__ wte,
                const bf16* __restrict__ wpe, int rows, int T, int t_past, int d, int n_vocab,
                float* __restrict__ H, unsigned* err) {
+  pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -217,6 +227,8 @@ __global__ void __launch_bounds__(kRowThreads)
     embed_fp32(const int32_t* __restrict__ ids, const float* __restrict__ wte,
                const float* __restrict__ wpe, int rows, int T, int t_past, int d, int n_vocab,
                float* __restrict__ H, unsigned* err) {
+  pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -262,8 +274,9 @@ int launch_convert_f16(const ConvSegs& segs, cudaStream_t stream) {
   // About four 16-byte chunks per thread for the largest array.
   const long long want = (most / 8 + 1023) / 1024;
   const unsigned gx = static_cast<unsigned>(want < 1 ? 1 : (want > 2048 ? 2048 : want));
-  convert_f16<<<dim3(gx, segs.count), 256, 0, stream>>>(segs);
-  return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+  const cudaError_t e =
+      launch_pdl(convert_f16, dim3(gx, segs.count), dim3(256), 0, stream, segs);
+  return e == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
 int launch_embed(int mode, const int32_t* ids, const void* wte, const void* wpe, int B, int T,
@@ -273,13 +286,15 @@ int launch_embed(int mode, const int32_t* ids, const void* wte, const void* wpe,
   const unsigned blocks = static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock);
   if (mode == GPT2_BF16) {
     if (d % 8 != 0) return GPT2_ERR_UNSUPPORTED;
-    embed_bf16<<<blocks, kRowThreads, 0, stream>>>(ids, static_cast<const bf16*>(wte),
-                                                   static_cast<const bf16*>(wpe), rows, T, t_past,
-                                                   d, n_vocab, H, err);
+    if (launch_pdl(embed_bf16, dim3(blocks), dim3(kRowThreads), 0, stream, ids,
+                   static_cast<const bf16*>(wte), static_cast<const bf16*>(wpe), rows, T, t_past,
+                   d, n_vocab, H, err) != cudaSuccess)
+      return GPT2_ERR_CUDA;
   } else {
-    embed_fp32<<<blocks, kRowThreads, 0, stream>>>(ids, static_cast<const float*>(wte),
-                                                   static_cast<const float*>(wpe), rows, T, t_past,
-                                                   d, n_vocab, H, err);
+    if (launch_pdl(embed_fp32, dim3(blocks), dim3(kRowThreads), 0, stream, ids,
+                   static_cast<const float*>(wte), static_cast<const float*>(wpe), rows, T,
+                   t_past, d, n_vocab, H, err) != cudaSuccess)
+      return GPT2_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }

@@ -60,6 +60,8 @@ __global__ void __launch_bounds__(256)
     gemm_fp32_kernel(const float* __restrict__ A, const float* __restrict__ W, const Fp32Args a) {
   __shared__ float sA[kKt][kT + 1];
   __shared__ float sW[kKt][kT + 1];
+  pdl_trigger();
+  pdl_wait();
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int m0 = blockIdx.y * kT, n0 = blockIdx.x * kT;
   float acc[4][4] = {};
@@ -108,15 +110,19 @@ int launch_gemm_fp32(const LaunchEnv& env, int kind, const float* A, const float
   Fp32Args a{M, N, K, d_h, ep};
   dim3 grid((N + kT - 1) / kT, (M + kT - 1) / kT);
   if (grid.y > 65535) return GPT2_ERR_UNSUPPORTED;
+  cudaError_t e;
+  const dim3 block(256);
   switch (kind) {
-    case kEpiBias: gemm_fp32_kernel<kEpiBias><<<grid, 256, 0, stream>>>(A, W, a); break;
-    case kEpiGelu: gemm_fp32_kernel<kEpiGelu><<<grid, 256, 0, stream>>>(A, W, a); break;
-    case kEpiResidF32: gemm_fp32_kernel<kEpiResidF32><<<grid, 256, 0, stream>>>(A, W, a); break;
-    case kEpiLogits: gemm_fp32_kernel<kEpiLogits><<<grid, 256, 0, stream>>>(A, W, a); break;
-    case kEpiQkv: gemm_fp32_kernel<kEpiQkv><<<grid, 256, 0, stream>>>(A, W, a); break;
+    case kEpiBias: e = launch_pdl(gemm_fp32_kernel<kEpiBias>, grid, block, 0, stream, A, W, a); break;
+    case kEpiGelu: e = launch_pdl(gemm_fp32_kernel<kEpiGelu>, grid, block, 0, stream, A, W, a); break;
+    case kEpiResidF32:
+      e = launch_pdl(gemm_fp32_kernel<kEpiResidF32>, grid, block, 0, stream, A, W, a);
+      break;
+    case kEpiLogits: e = launch_pdl(gemm_fp32_kernel<kEpiLogits>, grid, block, 0, stream, A, W, a); break;
+    case kEpiQkv: e = launch_pdl(gemm_fp32_kernel<kEpiQkv>, grid, block, 0, stream, A, W, a); break;
     default: return GPT2_ERR_INVALID_ARG;
   }
-  return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+  return e == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
 }  // namespace gpt2
