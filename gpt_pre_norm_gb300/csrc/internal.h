@@ -86,6 +86,14 @@ int launch_gemm_tc(const LaunchEnv& env, int kind, const void* A, const void* W,
                    int K, const EpiParams& ep, cudaStream_t stream, double* flops, double* bytes,
                    bool operands_f16, bool out_f16);
 
+// Weight-streaming GEMM for M <= 32 rows (cached decode): fp16 X [M, K] and
+// W [N, K], fp32 accumulate, epilogues kEpiQkv / kEpiGelu / kEpiBias (fp16
+// out) / kEpiResidF32 (K > 1024 only in place, out == resid).
+bool smallm_supported(int kind, int M, int K);
+int launch_gemm_smallm(const LaunchEnv& env, int kind, const __half* X, const __half* W, int M,
+                       int N, int K, const EpiParams& ep, cudaStream_t stream, double* flops,
+                       double* bytes);
+
 // fp32 SIMT GEMM with the same epilogues (fp32 storage throughout).
 int launch_gemm_fp32(const LaunchEnv& env, int kind, const float* A, const float* W, int M, int N,
                      int K, const EpiParams& ep, int d_h, cudaStream_t stream);
