@@ -45,7 +45,9 @@ def test_block_fp32_debug_shape(G):
 
 
 @pytest.mark.parametrize("name,B,T", [("block_bf16_d768", 2, 300), ("block_bf16_d1600", 1, 130),
-                                      ("block_bf16_d768", 3, 1)])
+                                      ("block_bf16_d768", 3, 1), ("block_bf16_d768", 2, 160),
+                                      ("block_bf16_d768", 1, 256), ("block_bf16_d1600", 2, 96),
+                                      ("block_bf16_d768", 2, 32)])
 def test_block_bf16(G, name, B, T):
     w = S.WORKLOADS[name]
     p = S.block_params(w, seed=1)
@@ -113,6 +115,22 @@ def test_forward_bf16_small(G):
     assert_bf16_close(got, ref, what="logits")
     assert argmax_agreement(got, ref) >= ARGMAX_AGREE
     assert_bf16_close(host(present.data)[..., :w.T, :], ref_present, what="present")
+
+
+def test_forward_bf16_tensor_core_attention(G):
+    """T a multiple of 32 with no cached prefix: attention on tcgen05."""
+    w = S.Workload("small_tc", "forward", "bf16", d=768, n_head=12, B=2, T=192, n_layer=2,
+                   resid_scale_layers=2)
+    p = S.model_params(w, seed=6)
+    ids = S.token_ids(w, seed=6)
+    ctx = G.Context(w.n_vocab, w.n_ctx, w.d, w.n_head, w.n_layer, G.GPT2_BF16, w.B, w.T)
+    mp = G.ModelParams(model_to_device(p))
+    logits = G.gpt2_forward(ctx, dev(ids, torch.int32), mp, w.B, w.T)
+    assert G.gpt2_sync_status(ctx) == 0
+    ref, _ = O.forward(ids, p, w.n_head)
+    got = host(logits)
+    assert_bf16_close(got, ref, what="logits")
+    assert argmax_agreement(got, ref) >= ARGMAX_AGREE
 
 
 def test_forward_fp32_tiny(G):
