@@ -43,12 +43,16 @@ constexpr int kBK = 64;                       // one 128-byte swizzle row of bf1
 constexpr int kEpiWarps = 8;                  // two per TMEM lane quarter
 constexpr int kThreads = 128 + 32 * kEpiWarps;
 constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB per A slot
-constexpr int kLogitsLd = 33;                 // logits transpose row stride (floats)
 constexpr int kMaxStages = 8;
 constexpr uint32_t kTmemCols = 512;           // two accumulators of up to 256 columns
 constexpr int kSmemLimit = 232448;            // 227 KB opt-in per CTA
 constexpr int kRBuf = 32 * 32 * 4;            // fp32 32x32 box, rows of 128 B, 128-byte swizzle
 constexpr int kOBuf = 32 * 32 * 2;            // bf16 32x32 box, rows of 64 B, 64-byte swizzle
+constexpr int kBiasBufs = 3;                  // bias buffers per column half, by tile index mod 3
+constexpr int kBiasBytes = 2 * kBiasBufs * 128 * 2;  // bf16 bias of each half's columns (<= 128)
+constexpr int kLogitsLd = 33;                 // logits transpose row stride (floats)
+
+static_assert(kRBuf % 1024 == 0 && kOBuf % 1024 == 0, "staging boxes must stay 1 KB aligned");
 
 __host__ __device__ constexpr bool uses_rbuf(int k) {
   return k == kEpiResidF32 || k == kEpiResidBf16In || k == kEpiResidBf16Out;
@@ -59,10 +63,17 @@ __host__ __device__ constexpr bool uses_obuf(int k) {
 __host__ __device__ constexpr int slot_bytes(int k) {
   return (uses_rbuf(k) ? kRBuf : 0) + (uses_obuf(k) ? kOBuf : 0);
 }
-// Shared memory of one epilogue warp: two staging slots, or the logits transpose.
+// Shared memory of one epilogue warp: two staging slots (multiples of 1 KB,
+// so every swizzled box stays 1024-byte aligned), or (logits) one transposed
+// 32 x 32 chunk.  The bias buffers follow all warps' slots:
+// the four warps of a column half share one (each writes the same values),
+// and three of them rotate by tile, so a warp that runs two tiles ahead of
+// another (the most the two accumulators allow) never overwrites a buffer
+// still being read.
 __host__ __device__ constexpr int epi_warp_bytes(int k) {
   return k == kEpiLogits ? 32 * kLogitsLd * 4 : 2 * slot_bytes(k);
 }
+__host__ __device__ constexpr int epi_bias_bytes(int k) { return k == kEpiLogits ? 0 : kBiasBytes; }
 
 struct GemmArgs {
   int M, N, K;
@@ -81,9 +92,11 @@ struct GemmArgs {
   EpiParams ep;
 };
 
-__host__ __device__ inline size_t smem_bytes_for(int kind, int BN, int stages) {
-  return 1024 /* alignment slack */ + static_cast<size_t>(stages) * (kABytes + BN * kBK * 2) +
-         static_cast<size_t>(kEpiWarps) * epi_warp_bytes(kind) +
+// Dynamic shared memory of one CTA; cg = 2 holds half of the tile's B rows.
+__host__ __device__ inline size_t smem_bytes_for(int kind, int BN, int stages, int cg) {
+  return 1024 /* alignment slack */ +
+         static_cast<size_t>(stages) * (kABytes + (BN / cg) * kBK * 2) +
+         static_cast<size_t>(kEpiWarps) * epi_warp_bytes(kind) + epi_bias_bytes(kind) +
          (2 * stages + 5 + 2 * kEpiWarps) * sizeof(uint64_t) + 16;
 }
 
@@ -129,14 +142,94 @@ __device__ __forceinline__ void box_write_16(uint8_t* box, int r, const float (&
     *reinterpret_cast<uint4*>(box + r * 64 + ((c ^ ((r >> 1) & 3)) << 4)) = pack8(v + 8 * c, f16);
 }
 
+// Per-warp epilogue state carried across chunks and tiles.
+struct EpiState {
+  int chunk;          // chunks processed so far (selects the staging slot)
+  uint32_t rpar;      // bit s: parity of the next wait on residual barrier s
+  uint32_t inflight;  // bit s: a residual load into slot s is in flight
+  uint4 rnext[4];     // kEpiResidBf16In: next chunk's bf16 residual, one row of 32
+};
+
+// Issues the TMA load of the fp32 residual box of chunk column `col` into slot s.
+__device__ __forceinline__ void resid_load(uint8_t* rb, uint64_t* bar, const CUtensorMap* tmR,
+                                           int col, int row0) {
+  fence_proxy_async_smem();  // earlier generic reads of the box come first
+  mbar_arrive_expect_tx(bar, kRBuf);
+  tma_load_2d(rb, tmR, bar, col, row0);
+}
+
+// Loads one row's 32 bf16 residual values (columns col .. col+31) into registers.
+__device__ __forceinline__ void resid16_fetch(const GemmArgs& a, int row, int col, uint4 (&v)[4]) {
+  const EpiParams& ep = a.ep;
+  const bf16* rp = static_cast<const bf16*>(ep.resid) + static_cast<size_t>(row) * ep.ldo + col;
+  if (row >= a.M) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = make_uint4(0u, 0u, 0u, 0u);
+  } else if (col + 32 <= a.N && a.vec_ok) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = reinterpret_cast<const uint4*>(rp)[i];
+  } else {
+    uint32_t w[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t lo = col + 2 * j < a.N ? reinterpret_cast<const uint16_t*>(rp)[2 * j] : 0u;
+      const uint32_t hi = col + 2 * j + 1 < a.N ? reinterpret_cast<const uint16_t*>(rp)[2 * j + 1] : 0u;
+      w[j] = lo | (hi << 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  }
+}
+
+// Work a warp can do for its share of a tile before the accumulator is ready:
+// the bias of its columns into shared memory, the fp32 residual boxes of its
+// first two chunks by TMA, the bf16 residual of its first chunk into registers.
+template <int KIND>
+__device__ __forceinline__ void epilogue_prefetch(int row0, int ncol0, int ncols, int lane,
+                                                  uint8_t* epi, uint16_t* bias_s, uint64_t* rbar,
+                                                  EpiState& s, const GemmArgs& a,
+                                                  const CUtensorMap* tmR) {
+  if constexpr (KIND != kEpiLogits) {
+    const int N = a.N;
+    const int j = 4 * lane;
+    if (j < ncols) {
+      const int col = ncol0 + j;
+      const uint16_t* bp = static_cast<const uint16_t*>(a.ep.bias) + col;
+      uint2 w;
+      if (col + 4 <= N) {
+        w = *reinterpret_cast<const uint2*>(bp);
+      } else {
+        const uint32_t b0 = col < N ? bp[0] : 0u, b1 = col + 1 < N ? bp[1] : 0u;
+        const uint32_t b2 = col + 2 < N ? bp[2] : 0u;
+        w = make_uint2(b0 | (b1 << 16), b2);
+      }
+      *reinterpret_cast<uint2*>(bias_s + j) = w;
+    }
+    if constexpr (KIND == kEpiResidF32 || KIND == kEpiResidBf16Out) {
+      if (a.tma_resid && lane == 0) {
+        // kEpiResidF32 stages its output in the residual box: the stores that
+        // last read the slots must be done.
+        if constexpr (KIND == kEpiResidF32) bulk_wait_group_read<0>();
+        for (int c = 0; c < 2; ++c) {
+          const int col = ncol0 + 32 * c;
+          if (32 * c >= ncols || col >= N) break;
+          const int slot = (s.chunk + c) & 1;
+          resid_load(epi + slot * slot_bytes(KIND), &rbar[slot], tmR, col, row0);
+          s.inflight |= 1u << slot;
+        }
+      }
+    }
+    if constexpr (KIND == kEpiResidBf16In) resid16_fetch(a, row0 + lane, ncol0, s.rnext);
+    __syncwarp();
+  }
+}
+
 // Epilogue of one warp's share of a tile: rows row0 .. row0+31 (this thread:
 // row0 + lane), columns ncol0 .. ncol0+ncols-1, accumulator at TMEM tbase.
-// `chunk` counts this warp's chunks (it selects the staging slot); rpar holds
-// the parities of the two residual-load barriers.
 template <int KIND>
 __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol0, int ncols,
-                                              int lane, uint8_t* epi, uint64_t* rbar, int& chunk,
-                                              uint32_t (&rpar)[2], const GemmArgs& a,
+                                              int lane, uint8_t* epi, const uint16_t* bias_s,
+                                              uint64_t* rbar, EpiState& s, const GemmArgs& a,
                                               const CUtensorMap* tmO, const CUtensorMap* tmR,
                                               const CUtensorMap* tmQ, const CUtensorMap* tmKV,
                                               volatile int* abort_flag) {
@@ -144,18 +237,21 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol
   const int M = a.M, N = a.N;
   const int row = row0 + lane;
   const bool row_ok = row < M;
+  const int seg_end = min(ncols, N - ncol0);  // valid columns of this warp's segment
   int qkv_b = 0, qkv_t = 0;
   if constexpr (KIND == kEpiQkv) {
     qkv_b = row / ep.T;
     qkv_t = row - qkv_b * ep.T;
   }
-  for (int c = 0; c < ncols; c += 32) {
+  for (int c = 0; c < seg_end; c += 32) {
     const int col = ncol0 + c;
-    if (col >= N) break;  // warp-uniform
     uint32_t r[32];
     const size_t off = static_cast<size_t>(row) * ep.ldo + col;
 
     if constexpr (KIND == kEpiLogits) {
+      // fp32 logits rows are only 4-byte aligned: transpose the chunk through
+      // shared memory so each store instruction writes 32 consecutive columns
+      // of one row.
       tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), r);
       tmem_ld_wait();
       float* st = reinterpret_cast<float*>(epi);
@@ -173,8 +269,8 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol
       }
       __syncwarp();
     } else {
-      const int slot = chunk & 1;
-      ++chunk;
+      const int slot = s.chunk & 1;
+      ++s.chunk;
       uint8_t* rb = epi + slot * slot_bytes(KIND);
       uint8_t* ob = rb + (uses_rbuf(KIND) ? kRBuf : 0);
       const bool tma_store_path = (KIND == kEpiQkv) ? a.tma_qkv != 0 : a.tma_out != 0;
@@ -182,14 +278,14 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol
       // bf16 for Q/K/V and the block output; the caller's choice for the others.
       const bool out16 = (KIND == kEpiBias || KIND == kEpiGelu) && a.out_f16 != 0;
       const bool tma_resid = kFp32Resid && a.tma_resid != 0;
-      if (tma_store_path || tma_resid) {
+      if (tma_store_path) {
         // The TMA store that last used this slot must be done reading it.
         if (lane == 0) bulk_wait_group_read<1>();
         __syncwarp();
       }
-      if (tma_resid && lane == 0) {
-        mbar_arrive_expect_tx(&rbar[slot], kRBuf);
-        tma_load_2d(rb, tmR, &rbar[slot], col, row0);
+      if (KIND == kEpiResidF32 && tma_resid && c >= 64 && lane == 0) {
+        resid_load(rb, &rbar[slot], tmR, col, row0);
+        s.inflight |= 1u << slot;
       }
       tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), r);
       const bool full = (col + 32 <= N) && a.vec_ok;
@@ -209,32 +305,28 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol
           }
         }
       } else if constexpr (KIND == kEpiResidBf16In) {
-        const bf16* rp = static_cast<const bf16*>(ep.resid) + off;
-        if (full && row_ok) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) unpack8(reinterpret_cast<const uint4*>(rp)[i], rv + 8 * i);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            rv[j] = (row_ok && col + j < N) ? __bfloat162float(rp[j]) : 0.f;
-        }
+        for (int i = 0; i < 4; ++i) unpack8(s.rnext[i], rv + 8 * i);
+        if (c + 32 < seg_end) resid16_fetch(a, row, col + 32, s.rnext);
       }
       float bv[32];
-      {
-        const bf16* bp = static_cast<const bf16*>(ep.bias) + col;
-        if (col + 32 <= N) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) unpack8(reinterpret_cast<const uint4*>(bp)[i], bv + 8 * i);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) bv[j] = col + j < N ? __bfloat162float(bp[j]) : 0.f;
-        }
-      }
+      for (int i = 0; i < 4; ++i) unpack8(*reinterpret_cast<const uint4*>(bias_s + c + 8 * i), bv + 8 * i);
       tmem_ld_wait();
       if (tma_resid) {
-        mbar_wait_bounded(&rbar[slot], rpar[slot], abort_flag, a.err);
-        rpar[slot] ^= 1u;
+        if (mbar_wait_bounded(&rbar[slot], (s.rpar >> slot) & 1u, abort_flag, a.err)) {
+          s.rpar ^= 1u << slot;
+          s.inflight &= ~(1u << slot);
+        }
         box_read_f32(rb, lane, rv);
+        if constexpr (KIND == kEpiResidBf16Out) {
+          // The box is free again: fetch the residual of chunk c+2 into it.
+          __syncwarp();
+          if (c + 64 < seg_end && lane == 0) {
+            resid_load(rb, &rbar[slot], tmR, col + 64, row0);
+            s.inflight |= 1u << slot;
+          }
+        }
       }
       float v[32];
 #pragma unroll
@@ -310,7 +402,12 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol
   }
 }
 
-template <int KIND>
+// CG = 1: one CTA per tile of 128 x BN.  CG = 2: a cluster of two CTAs per
+// tile of 256 x BN; each CTA loads its 128 rows of A and half of the tile's B
+// rows into its own shared memory, both CTAs' copies complete on the first
+// CTA's stage barrier, the first CTA issues the pair MMA, and each CTA's
+// epilogue drains its own 128 accumulator rows.
+template <int KIND, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmR,
@@ -320,16 +417,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int BN = args.BN, S = args.stages;
-  const uint32_t b_bytes = static_cast<uint32_t>(BN) * kBK * 2;
+  const uint32_t b_bytes = static_cast<uint32_t>(BN / CG) * kBK * 2;  // this CTA's B rows
   uint8_t* sA = smem;
   uint8_t* sB = smem + static_cast<size_t>(S) * kABytes;
   uint8_t* sEpi = sB + static_cast<size_t>(S) * b_bytes;
   uint64_t* bars =
-      reinterpret_cast<uint64_t*>(sEpi + static_cast<size_t>(kEpiWarps) * epi_warp_bytes(KIND));
-  uint64_t* full = bars;                  // [S]   TMA landed
+      reinterpret_cast<uint64_t*>(sEpi + static_cast<size_t>(kEpiWarps) * epi_warp_bytes(KIND) +
+                                  epi_bias_bytes(KIND));
+  uint64_t* full = bars;                  // [S]   TMA landed (pair: both CTAs', first CTA's barrier)
   uint64_t* empty = bars + S;             // [S]   slot consumed by the MMAs
   uint64_t* tfull = bars + 2 * S;         // [2]   accumulator ready
-  uint64_t* tempty = bars + 2 * S + 2;    // [2]   accumulator drained
+  uint64_t* tempty = bars + 2 * S + 2;    // [2]   accumulator drained (pair: both CTAs)
   uint64_t* mma_done = bars + 2 * S + 4;  // [1]   every issued MMA retired
   uint64_t* rbars = bars + 2 * S + 5;     // [8][2] residual loads of the epilogue warps
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rbars + 2 * kEpiWarps);
@@ -337,6 +435,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KB = (args.K + kBK - 1) / kBK;
+  const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
+  const int first_tile = CG == 2 ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int tile_step = CG == 2 ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int tile_rows = kBM * CG;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -345,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], kEpiWarps);
+      mbar_init(&tempty[i], kEpiWarps * CG);
     }
     mbar_init(mma_done, 1);
     for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(&rbars[i], 1);
@@ -353,11 +455,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 2) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
+    if constexpr (CG == 2) {
+      tmem_alloc_pair(tmem_slot, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // both CTAs' barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // Set-up above touched only shared memory and TMEM: let the next kernel
@@ -369,44 +477,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- producer --
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    int last_parity[kMaxStages];
-    for (int s = 0; s < kMaxStages; ++s) last_parity[s] = -1;
+    uint32_t issued = 0u, issued_par = 0u;  // bit s: slot s has a load issued / its parity
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
+    const uint32_t full0 = CG == 2 ? mapa_shared(smem_u32(full), 0u) : 0u;  // first CTA's barriers
+    for (int tile = first_tile; ok && tile < args.num_tiles; tile += tile_step) {
       const int m_blk = tile % args.num_m_blocks, n_blk = tile / args.num_m_blocks;
+      const int a_row = m_blk * tile_rows + static_cast<int>(rank) * kBM;
+      const int b_row = n_blk * BN + static_cast<int>(rank) * (BN / CG);
       for (int kb = 0; kb < KB; ++kb) {
         if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.err)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&full[stage], kABytes + b_bytes);
-        tma_load_2d(sA + static_cast<size_t>(stage) * kABytes, &tmA, &full[stage], kb * kBK,
-                    m_blk * kBM);
-        tma_load_2d(sB + static_cast<size_t>(stage) * b_bytes, &tmB, &full[stage], kb * kBK,
-                    n_blk * BN);
-        last_parity[stage] = static_cast<int>(phase);
+        if constexpr (CG == 2) {
+          // The first CTA's barrier counts both CTAs' bytes; only it arrives.
+          const uint32_t bar = full0 + stage * static_cast<uint32_t>(sizeof(uint64_t));
+          if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2u * (kABytes + b_bytes));
+          tma_load_2d_pair(sA + static_cast<size_t>(stage) * kABytes, &tmA, bar, kb * kBK, a_row);
+          tma_load_2d_pair(sB + static_cast<size_t>(stage) * b_bytes, &tmB, bar, kb * kBK, b_row);
+        } else {
+          mbar_arrive_expect_tx(&full[stage], kABytes + b_bytes);
+          tma_load_2d(sA + static_cast<size_t>(stage) * kABytes, &tmA, &full[stage], kb * kBK, a_row);
+          tma_load_2d(sB + static_cast<size_t>(stage) * b_bytes, &tmB, &full[stage], kb * kBK, b_row);
+        }
+        issued |= 1u << stage;
+        issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
         }
       }
     }
-    if (!ok) {
-      // Drain: every copy already issued must land before the CTA exits.
+    if (!ok && rank == 0) {
+      // Drain: every copy already issued must land before the CTA exits.  (A
+      // pair's second CTA cannot wait on the first CTA's barriers; after an
+      // abort its copies land long before the closing cluster barrier, which
+      // waits for the first CTA's bounded waits to run out.)
       for (int s = 0; s < S; ++s)
-        if (last_parity[s] >= 0)
-          mbar_wait_bounded(&full[s], static_cast<uint32_t>(last_parity[s]), nullptr, args.err);
+        if ((issued >> s) & 1u) mbar_wait_bounded(&full[s], (issued_par >> s) & 1u, nullptr, args.err);
     }
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1 && lane == 0 && rank == 0) {
     // ------------------------------------------------------- MMA issuer --
     const uint32_t idesc = args.idesc;
     int stage = 0;
     uint32_t phase = 0;
     int it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x, ++it) {
+    for (int tile = first_tile; ok && tile < args.num_tiles; tile += tile_step, ++it) {
       const int acc = it & 1;
       const uint32_t acc_par = static_cast<uint32_t>((it >> 1) & 1);
       if (!mbar_wait_bounded(&tempty[acc], acc_par ^ 1u, abort_flag, args.err)) break;
@@ -423,76 +542,112 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < kBK / 16; ++k) {
           // +32 bytes per 16-element K slice: +2 in the descriptor's address field.
-          umma_f16kind(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          if constexpr (CG == 2)
+            umma_f16kind_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          else
+            umma_f16kind(d_tmem, a_desc + 2 * k, b_desc + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
         }
-        umma_commit(&empty[stage]);
+        if constexpr (CG == 2) umma_commit_pair(&empty[stage], 3);
+        else umma_commit(&empty[stage]);
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
         }
       }
-      if (ok) umma_commit(&tfull[acc]);
+      if (ok) {
+        if constexpr (CG == 2) umma_commit_pair(&tfull[acc], 3);
+        else umma_commit(&tfull[acc]);
+      }
     }
     // Every MMA issued above must retire before TMEM is freed.
-    umma_commit(mma_done);
+    if constexpr (CG == 2) umma_commit_pair(mma_done, 1);
+    else umma_commit(mma_done);
     mbar_wait_bounded(mma_done, 0, nullptr, args.err);
   } else if (warp >= 4) {
     // --------------------------------------------------------- epilogue --
     // Warp w may read TMEM lanes 32*(w%4) .. +31; the two warps of a lane
-    // quarter split the tile's columns in halves.
+    // quarter split the tile's columns in halves.  What does not depend on the
+    // accumulator is fetched before waiting for it.
     const int e = warp - 4;
     const int quarter = warp & 3;
     const int half = e >> 2;
     const int ncols = BN / 2;
     uint8_t* epi = sEpi + static_cast<size_t>(e) * epi_warp_bytes(KIND);
+    uint16_t* bias_half = reinterpret_cast<uint16_t*>(sEpi + kEpiWarps * epi_warp_bytes(KIND)) +
+                          half * kBiasBufs * 128;
     uint64_t* rbar = rbars + 2 * e;
-    int chunk = 0;
-    uint32_t rpar[2] = {0u, 0u};
+    EpiState st;
+    st.chunk = 0;
+    st.rpar = 0u;
+    st.inflight = 0u;
     if (lane == 0) {
       if (args.tma_out) tma_prefetch_desc(&tmO);
       if (args.tma_resid) tma_prefetch_desc(&tmR);
     }
+    // The accumulator-drained barrier lives in the pair's first CTA.
+    const uint32_t tempty_addr = CG == 2 ? mapa_shared(smem_u32(tempty), 0u) : 0u;
     int it = 0;
-    for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x, ++it) {
+    for (int tile = first_tile; tile < args.num_tiles; tile += tile_step, ++it) {
       const int acc = it & 1;
       const uint32_t acc_par = static_cast<uint32_t>((it >> 1) & 1);
+      const int m_blk = tile % args.num_m_blocks, n_blk = tile / args.num_m_blocks;
+      const int row0 = m_blk * tile_rows + static_cast<int>(rank) * kBM + quarter * 32;
+      const int ncol0 = n_blk * BN + half * ncols;
+      uint16_t* bias_s = bias_half + (it % kBiasBufs) * 128;
+      epilogue_prefetch<KIND>(row0, ncol0, ncols, lane, epi, bias_s, rbar, st, args, &tmR);
       if (!mbar_wait_bounded(&tfull[acc], acc_par, abort_flag, args.err)) break;
       tc_fence_after();
-      const int m_blk = tile % args.num_m_blocks, n_blk = tile / args.num_m_blocks;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc * 256 + half * ncols);
-      epilogue_tile<KIND>(tbase, m_blk * kBM + quarter * 32, n_blk * BN + half * ncols, ncols,
-                          lane, epi, rbar, chunk, rpar, args, &tmO, &tmR, &tmQ, &tmKV,
-                          abort_flag);
+      epilogue_tile<KIND>(tbase, row0, ncol0, ncols, lane, epi, bias_s, rbar, st, args, &tmO,
+                          &tmR, &tmQ, &tmKV, abort_flag);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (lane == 0) {
+        if constexpr (CG == 2)
+          mbar_arrive_cluster(tempty_addr + acc * static_cast<uint32_t>(sizeof(uint64_t)));
+        else
+          mbar_arrive(&tempty[acc]);
+      }
     }
-    // Every TMA store must be complete before the CTA's shared memory goes.
-    if (lane == 0) bulk_wait_group<0>();
+    // Residual loads still in flight (after an abort) must land, and every TMA
+    // store must be complete, before the CTA's shared memory goes.
+    if (lane == 0) {
+      for (int sl = 0; sl < 2; ++sl)
+        if ((st.inflight >> sl) & 1u)
+          mbar_wait_bounded(&rbar[sl], (st.rpar >> sl) & 1u, nullptr, args.err);
+      bulk_wait_group<0>();
+    }
     __syncwarp();
   }
 
   tc_fence_before();
   __syncthreads();
+  // Pair: the partner's shared memory and TMEM stay in use (remote arrivals,
+  // MMAs of the first CTA) until both CTAs get here.
+  if constexpr (CG == 2) cluster_sync();
   tc_fence_after();
-  if (warp == 2) tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == 2) {
+    if constexpr (CG == 2) tmem_dealloc_pair(tmem_base, kTmemCols);
+    else tmem_dealloc(tmem_base, kTmemCols);
+  }
 }
 
 template <int KIND>
-void* kernel_ptr() {
-  return reinterpret_cast<void*>(&gemm_tc_kernel<KIND>);
+void* kernel_ptr(int cg) {
+  return cg == 2 ? reinterpret_cast<void*>(&gemm_tc_kernel<KIND, 2>)
+                 : reinterpret_cast<void*>(&gemm_tc_kernel<KIND, 1>);
 }
 
-void* kernel_for(int kind) {
+void* kernel_for(int kind, int cg) {
   switch (kind) {
-    case kEpiBias: return kernel_ptr<kEpiBias>();
-    case kEpiGelu: return kernel_ptr<kEpiGelu>();
-    case kEpiResidF32: return kernel_ptr<kEpiResidF32>();
-    case kEpiResidBf16In: return kernel_ptr<kEpiResidBf16In>();
-    case kEpiResidBf16Out: return kernel_ptr<kEpiResidBf16Out>();
-    case kEpiLogits: return kernel_ptr<kEpiLogits>();
-    case kEpiQkv: return kernel_ptr<kEpiQkv>();
+    case kEpiBias: return kernel_ptr<kEpiBias>(cg);
+    case kEpiGelu: return kernel_ptr<kEpiGelu>(cg);
+    case kEpiResidF32: return kernel_ptr<kEpiResidF32>(cg);
+    case kEpiResidBf16In: return kernel_ptr<kEpiResidBf16In>(cg);
+    case kEpiResidBf16Out: return kernel_ptr<kEpiResidBf16Out>(cg);
+    case kEpiLogits: return kernel_ptr<kEpiLogits>(cg);
+    case kEpiQkv: return kernel_ptr<kEpiQkv>(cg);
     default: return nullptr;
   }
 }
@@ -552,10 +707,12 @@ bool encode_heads(const LaunchEnv& env, CUtensorMap* map, const void* base, long
 }
 
 // Tile width: the candidate minimising waves x (BN + 32): the busiest SM's
-// share of the work plus a per-tile cost (operand reloads, epilogue start),
-// preferring wider tiles on ties.
-int choose_bn(int M, int N, int num_sms) {
-  const int m_blocks = (M + kBM - 1) / kBM;
+// (or CTA pair's) share of the work plus a per-tile cost (operand reloads,
+// epilogue start), preferring wider tiles on ties.  Tiles have tile_rows rows
+// and `units` of them run at once.
+int choose_bn(int M, int N, int tile_rows, int units) {
+  const int num_sms = units;
+  const int m_blocks = (M + tile_rows - 1) / tile_rows;
   int best = 256;
   long long best_cost = -1;
   for (int bn : {256, 192, 128, 64}) {
@@ -575,17 +732,23 @@ int choose_bn(int M, int N, int num_sms) {
 int launch_gemm_tc(const LaunchEnv& env, int kind, const void* A, const void* W, int M, int N,
                    int K, const EpiParams& ep, cudaStream_t stream, double* flops, double* bytes,
                    bool operands_f16, bool out_f16) {
-  void* fn = kernel_for(kind);
+  // CTA pairs (256-row tiles on two SMs, each holding half of B) where the
+  // mainloop is long enough to gain from halving each SM's operand traffic;
+  // measured on GB300: faster from K = 1600 up, no gain at K = 768.
+  const int cg = (M > kBM && K >= 1024 && env.num_sms >= 2) ? 2 : 1;
+  void* fn = kernel_for(kind, cg);
   if (!fn) return GPT2_ERR_INVALID_ARG;
   if (M <= 0 || N <= 0 || K <= 0) return GPT2_ERR_INVALID_ARG;
   if (K % 8 != 0) return GPT2_ERR_UNSUPPORTED;
   if (kind != kEpiLogits && (N % 2 != 0)) return GPT2_ERR_UNSUPPORTED;
   if (kind == kEpiQkv && (ep.d % 64 != 0 || N != 3 * ep.d)) return GPT2_ERR_UNSUPPORTED;
 
-  const int BN = choose_bn(M, N, env.num_sms);
+  const int units = cg == 2 ? env.num_sms / 2 : env.num_sms;
+  const int BN = choose_bn(M, N, kBM * cg, units);
   int stages = kMaxStages;
-  while (stages > 2 && smem_bytes_for(kind, BN, stages) > static_cast<size_t>(kSmemLimit)) --stages;
-  const size_t smem = smem_bytes_for(kind, BN, stages);
+  while (stages > 2 && smem_bytes_for(kind, BN, stages, cg) > static_cast<size_t>(kSmemLimit))
+    --stages;
+  const size_t smem = smem_bytes_for(kind, BN, stages, cg);
 
   CUtensorMap tmA, tmB, tmO, tmR, tmQ, tmKV;
   memset(&tmO, 0, sizeof(tmO));
@@ -593,7 +756,7 @@ int launch_gemm_tc(const LaunchEnv& env, int kind, const void* A, const void* W,
   memset(&tmQ, 0, sizeof(tmQ));
   memset(&tmKV, 0, sizeof(tmKV));
   if (!encode_kmajor_16(env, &tmA, A, M, K, kBM, operands_f16)) return GPT2_ERR_CUDA;
-  if (!encode_kmajor_16(env, &tmB, W, N, K, BN, operands_f16)) return GPT2_ERR_CUDA;
+  if (!encode_kmajor_16(env, &tmB, W, N, K, BN / cg, operands_f16)) return GPT2_ERR_CUDA;
 
   GemmArgs args;
   args.M = M;
@@ -601,7 +764,7 @@ int launch_gemm_tc(const LaunchEnv& env, int kind, const void* A, const void* W,
   args.K = K;
   args.BN = BN;
   args.stages = stages;
-  args.num_m_blocks = (M + kBM - 1) / kBM;
+  args.num_m_blocks = (M + kBM * cg - 1) / (kBM * cg);
   args.num_tiles = args.num_m_blocks * ((N + BN - 1) / BN);
   args.vec_ok = (kind == kEpiResidF32 || kind == kEpiResidBf16In) ? (ep.ldo % 4 == 0)
                                                                   : (ep.ldo % 8 == 0);
@@ -610,7 +773,7 @@ int launch_gemm_tc(const LaunchEnv& env, int kind, const void* A, const void* W,
   args.tma_qkv = 0;
   args.kv_z_per_seq = 0;
   args.out_f16 = out_f16 ? 1 : 0;
-  args.idesc = umma_idesc_16(kBM, BN, operands_f16);
+  args.idesc = umma_idesc_16(kBM * cg, BN, operands_f16);
   args.err = env.err;
   args.ep = ep;
   if (kind == kEpiBias || kind == kEpiGelu)
@@ -636,25 +799,29 @@ int launch_gemm_tc(const LaunchEnv& env, int kind, const void* A, const void* W,
 
   // Set once per process (the opt-in limit does not depend on the call), so
   // later calls make no non-stream CUDA call (safe under stream capture).
-  static bool attr_set[kEpiCount] = {};
-  if (!attr_set[kind]) {
+  static bool attr_set[2][kEpiCount] = {};
+  if (!attr_set[cg - 1][kind]) {
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) !=
         cudaSuccess)
       return GPT2_ERR_CUDA;
-    attr_set[kind] = true;
+    attr_set[cg - 1][kind] = true;
   }
-  const int grid = std::min(args.num_tiles, env.num_sms);
+  const int grid = std::min(args.num_tiles, units) * cg;
   void* params[] = {&tmA, &tmB, &tmO, &tmR, &tmQ, &tmKV, &args};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(cg);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (cudaLaunchKernelExC(&cfg, fn, params) != cudaSuccess) return GPT2_ERR_CUDA;
 
   if (flops) *flops = 2.0 * M * N * static_cast<double>(K);

@@ -65,8 +65,11 @@ def test_layer_norm_fp32(G, d):
 
 
 # ----------------------------------------------------------------- GEMMs ----
+# K >= 1024 with M > 128 runs on CTA pairs (256-row tiles); (200, 640, 1024) leaves the
+# second CTA's rows partly outside M.
 GEMM_SHAPES = [(128, 256, 64), (300, 200, 768), (1000, 768, 768), (129, 2304, 768),
-               (77, 3072, 200), (1, 64, 64), (32, 1024, 1024), (640, 768, 3072)]
+               (77, 3072, 200), (1, 64, 64), (32, 1024, 1024), (640, 768, 3072),
+               (200, 640, 1024), (1000, 200, 1600)]
 
 
 @pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
@@ -88,7 +91,7 @@ def test_linear_bias_resid_bf16(G, M, N, K):
     assert np.max(np.abs(host(out_b) - ref)) <= 2 ** -7 * np.max(np.abs(ref)) + 1e-3
 
 
-@pytest.mark.parametrize("M,N,K", [(300, 3072, 768), (128, 256, 1600)])
+@pytest.mark.parametrize("M,N,K", [(300, 3072, 768), (128, 256, 1600), (384, 3072, 1024)])
 def test_linear_gelu_bf16(G, M, N, K):
     rng = np.random.default_rng(11)
     ctx = _ctx(G, G.GPT2_BF16)
@@ -100,13 +103,15 @@ def test_linear_gelu_bf16(G, M, N, K):
     assert_bf16_close(host(out), O.gelu(O.linear(A, W, bias)), what="linear+gelu")
 
 
-@pytest.mark.parametrize("M,V", [(130, 50257), (1, 50257), (3, 50257), (256, 1000), (77, 1001),
-                                 (200, 1002), (33, 1003), (5, 40)])
-def test_tied_head_logits(G, M, V):
+@pytest.mark.parametrize("M,V,K", [(130, 50257, 768), (1, 50257, 768), (3, 50257, 768),
+                                   (256, 1000, 768), (77, 1001, 768), (200, 1002, 768),
+                                   (33, 1003, 768), (5, 40, 768), (300, 50257, 1024),
+                                   (260, 1001, 1600)])
+def test_tied_head_logits(G, M, V, K):
     rng = np.random.default_rng(M + V)
     ctx = _ctx(G, G.GPT2_BF16, V=V)
-    A = _rand(rng, (M, 768))
-    W = _rand(rng, (V, 768), 0.02)
+    A = _rand(rng, (M, K))
+    W = _rand(rng, (V, K), 0.02)
     out = G.gpt2_linear(ctx, G.GPT2_EPI_LOGITS, dev(A), dev(W))
     assert G.gpt2_sync_status(ctx) == 0
     assert out.shape == (M, V)
