@@ -27,8 +27,7 @@ namespace {
 const char* kKindNames[kKindCount] = {
     "embed",          "layer_norm",        "gemm_c_attn",    "attention_prefill",
     "gemm_c_proj",    "gemm_c_fc",         "gemm_mlp_c_proj", "gemm_lm_head",
-    "gemm_other",     "attention_decode",  "attention_decode_combine", "simt_fp32",
-    "weight_convert"};
+    "gemm_other",     "attention_decode",  "attention_decode_combine", "simt_fp32"};
 
 struct ProfRec {
   int kind;
@@ -195,56 +194,52 @@ struct BlockW16 {
   const __half *attn_w, *proj_w, *fc_w, *mlp_proj_w;
 };
 
-// Converts a block's weights into layer slot `slot` (skipped for matrices the
-// cache already holds).
-int convert_block_weights(gpt2_ctx* c, int slot, const gpt2_block_params* p, cudaStream_t s,
-                          BlockW16* w) {
+// The fp16 copies of a block's weights in layer slot `slot`: fills `segs`
+// with the conversions still to do (matrices the cache already holds are
+// skipped); the LayerNorm launch in front of the block's first product runs
+// them.
+void block_weight_conversions(gpt2_ctx* c, int slot, const gpt2_block_params* p, BlockW16* w,
+                              ConvSegs* segs) {
   const size_t d = c->hp.n_embd;
   __half* base = reinterpret_cast<__half*>(c->ws + c->plan.wconv) + slot * layer_slot_elems(c->hp);
   const void* srcs[4] = {p->attn_w, p->proj_w, p->fc_w, p->mlp_proj_w};
   const size_t offs[4] = {0, 3 * d * d, 4 * d * d, 8 * d * d};
   const size_t ns[4] = {3 * d * d, d * d, 4 * d * d, 4 * d * d};
-  ConvSegs segs{};
+  *segs = ConvSegs{};
   for (int i = 0; i < 4; ++i) {
     const size_t key = static_cast<size_t>(slot) * 4 + i;
     if (c->cache_weights && c->conv_src[key] == srcs[i]) continue;
-    segs.src[segs.count] = static_cast<const bf16*>(srcs[i]);
-    segs.dst[segs.count] = base + offs[i];
-    segs.n[segs.count] = static_cast<long long>(ns[i]);
-    ++segs.count;
+    segs->src[segs->count] = static_cast<const bf16*>(srcs[i]);
+    segs->dst[segs->count] = base + offs[i];
+    segs->n[segs->count] = static_cast<long long>(ns[i]);
+    ++segs->count;
     c->conv_src[key] = c->cache_weights ? srcs[i] : nullptr;
   }
   w->attn_w = base + offs[0];
   w->proj_w = base + offs[1];
   w->fc_w = base + offs[2];
   w->mlp_proj_w = base + offs[3];
-  if (segs.count == 0) return GPT2_OK;
-  return c->run(kKindWeightConvert, s, [&](double* fl, double* by) {
-    *fl = 0;
-    double n = 0;
-    for (int i = 0; i < segs.count; ++i) n += static_cast<double>(segs.n[i]);
-    *by = 4.0 * n;
-    return launch_convert_f16(segs, s);
-  });
 }
 
-int convert_wte(gpt2_ctx* c, const void* wte, cudaStream_t s, const __half** out) {
+// The tied embedding's fp16 copy (for the head); conversion as above.
+void wte_conversion(gpt2_ctx* c, const void* wte, const __half** out, ConvSegs* segs) {
   const size_t key = static_cast<size_t>(c->hp.n_layer) * 4;
   __half* dst = reinterpret_cast<__half*>(c->ws + c->plan.wconv) +
                 c->hp.n_layer * layer_slot_elems(c->hp);
   *out = dst;
-  if (c->cache_weights && c->conv_src[key] == wte) return GPT2_OK;
+  *segs = ConvSegs{};
+  if (c->cache_weights && c->conv_src[key] == wte) return;
   c->conv_src[key] = c->cache_weights ? wte : nullptr;
-  ConvSegs segs{};
-  segs.src[0] = static_cast<const bf16*>(wte);
-  segs.dst[0] = dst;
-  segs.n[0] = static_cast<long long>(c->hp.n_vocab) * c->hp.n_embd;
-  segs.count = 1;
-  return c->run(kKindWeightConvert, s, [&](double* fl, double* by) {
-    *fl = 0;
-    *by = 4.0 * static_cast<double>(segs.n[0]);
-    return launch_convert_f16(segs, s);
-  });
+  segs->src[0] = static_cast<const bf16*>(wte);
+  segs->dst[0] = dst;
+  segs->n[0] = static_cast<long long>(c->hp.n_vocab) * c->hp.n_embd;
+  segs->count = 1;
+}
+
+double conversion_bytes(const ConvSegs& segs) {
+  double n = 0;
+  for (int i = 0; i < segs.count; ++i) n += static_cast<double>(segs.n[i]);
+  return 4.0 * n;
 }
 
 // A bf16-mode product with fp16 operands: the weight-streaming kernel for a
@@ -279,13 +274,16 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int slot, int B, int
   // bf16 mode: the GEMM operands are fp16 (activations written by the
   // producing kernels; weights converted from bf16 per call, or cached).
   BlockW16 w{};
-  if (bf && (st = convert_block_weights(c, slot, p, s, &w))) return st;
+  ConvSegs conv{};
+  if (bf) block_weight_conversions(c, slot, p, &w, &conv);
 
-  // LN1
+  // LN1, with the block's weight conversion in the same launch
   st = c->run(kKindLayerNorm, s, [&](double* fl, double* by) {
     *fl = 0;
-    *by = static_cast<double>(M) * d * ((x_dtype == GPT2_FP32 ? 4 : 2) + (bf ? 2 : 4));
-    return launch_layer_norm(hp.dtype, x_in, x_dtype, p->ln1_g, p->ln1_b, M, d, ln, s, bf);
+    *by = static_cast<double>(M) * d * ((x_dtype == GPT2_FP32 ? 4 : 2) + (bf ? 2 : 4)) +
+          conversion_bytes(conv);
+    return launch_layer_norm(hp.dtype, x_in, x_dtype, p->ln1_g, p->ln1_b, M, d, ln, s, bf,
+                             conv.count ? &conv : nullptr);
   });
   if (st) return st;
 
@@ -619,17 +617,19 @@ int gpt2_forward(gpt2_ctx* c, const int32_t* ids, int B, int T, const gpt2_param
     if (st) return st;
   }
 
+  // LN_f, with the tied embedding's fp16 conversion in the same launch
+  const __half* wte16 = nullptr;
+  ConvSegs conv{};
+  if (bf) wte_conversion(c, params->wte, &wte16, &conv);
   void* ln = c->ws + c->plan.ln;
   st = c->run(kKindLayerNorm, s, [&](double* fl, double* by) {
     *fl = 0;
-    *by = static_cast<double>(M) * d * (4 + es);
+    *by = static_cast<double>(M) * d * (4 + es) + conversion_bytes(conv);
     return launch_layer_norm(hp.dtype, H, GPT2_FP32, params->lnf_g, params->lnf_b, M, d, ln, s,
-                             bf);
+                             bf, conv.count ? &conv : nullptr);
   });
   if (st) return st;
 
-  const __half* wte16 = nullptr;
-  if (bf && (st = convert_wte(c, params->wte, s, &wte16))) return st;
   EpiParams e{};
   e.out = logits;
   e.ldo = V;

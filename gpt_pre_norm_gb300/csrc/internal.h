@@ -29,7 +29,6 @@ enum KernelKind : int {
   kKindDecodeAttention,
   kKindDecodeCombine,
   kKindSimtFp32,
-  kKindWeightConvert,
   kKindCount
 };
 
@@ -98,12 +97,8 @@ int launch_gemm_smallm(const LaunchEnv& env, int kind, const __half* X, const __
 int launch_gemm_fp32(const LaunchEnv& env, int kind, const float* A, const float* W, int M, int N,
                      int K, const EpiParams& ep, int d_h, cudaStream_t stream);
 
-// LayerNorm rows of d: x fp32 or bf16 -> y (mode BF16: bf16, or fp16 when
-// y_f16; g, b bf16) or fp32 (mode FP32).
-int launch_layer_norm(int mode, const void* x, int x_dtype, const void* g, const void* b, int rows,
-                      int d, void* y, cudaStream_t stream, bool y_f16 = false);
-
-// Element-wise bf16 -> fp16 copies of up to kMaxConvSegs arrays in one launch.
+// Element-wise bf16 -> fp16 copies of up to kMaxConvSegs arrays (run by the
+// extra blocks of a LayerNorm launch).
 constexpr int kMaxConvSegs = 4;
 struct ConvSegs {
   const bf16* src[kMaxConvSegs];
@@ -111,7 +106,15 @@ struct ConvSegs {
   long long n[kMaxConvSegs];
   int count;
 };
-int launch_convert_f16(const ConvSegs& segs, cudaStream_t stream);
+
+// LayerNorm rows of d: x fp32 or bf16 -> y (mode BF16: bf16, or fp16 when
+// y_f16; g, b bf16) or fp32 (mode FP32).  `side`, if given, is a weight
+// conversion done by extra blocks of the same launch (both are memory-bound
+// and too small to fill the GPU's memory pipeline alone).
+int launch_layer_norm(int mode, const void* x, int x_dtype, const void* g, const void* b, int rows,
+                      int d, void* y, cudaStream_t stream, bool y_f16 = false,
+                      const ConvSegs* side = nullptr);
+
 
 // H[b,t,:] = wte[ids[b,t]] + wpe[t_past + t] -> fp32.
 int launch_embed(int mode, const int32_t* ids, const void* wte, const void* wpe, int B, int T,

@@ -1,5 +1,7 @@
 // rowwise.cu -- the memory-bound row kernels: LayerNorm (fused with the cast
-// of its output) and the embedding gather + position add.
+// of its output, and carrying the bf16 -> fp16 weight conversion of the
+// products that follow it as extra blocks of the same launch) and the
+// embedding gather + position add.
 //
 // LayerNorm follows the openai/gpt-2 ``norm`` excerpt on the "GPT-2
 // Transformer block" page: over the feature axis u = mean(x), s = mean((x -
@@ -47,15 +49,81 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 v) {
+  return make_uint4(pack_f16x2(bf16_lo(v.x), bf16_hi(v.x)), pack_f16x2(bf16_lo(v.y), bf16_hi(v.y)),
+                    pack_f16x2(bf16_lo(v.z), bf16_hi(v.z)), pack_f16x2(bf16_lo(v.w), bf16_hi(v.w)));
+}
+
+// bf16 -> fp16 conversion of up to kMaxConvSegs arrays, cut into blocks of
+// kRowThreads x kConvChunks 16-byte chunks; first[i] is array i's first block.
+// A bf16 value converts exactly unless its magnitude is below 2^-14 (fp16
+// subnormal range) or above 65504.
+constexpr int kConvChunks = 8;
+constexpr long long kConvBlockChunks = static_cast<long long>(kRowThreads) * kConvChunks;
+
+struct ConvJob {
+  const bf16* src[kMaxConvSegs];
+  __half* dst[kMaxConvSegs];
+  long long n[kMaxConvSegs];
+  int first[kMaxConvSegs + 1];  // first[count] = blocks in all
+  int count;
+};
+
+ConvJob make_conv_job(const ConvSegs* segs) {
+  ConvJob j{};
+  j.count = segs ? segs->count : 0;
+  for (int i = 0; i < j.count; ++i) {
+    j.src[i] = segs->src[i];
+    j.dst[i] = segs->dst[i];
+    j.n[i] = segs->n[i];
+    const long long chunks = (segs->n[i] + 7) / 8;
+    const long long blocks = (chunks + kConvBlockChunks - 1) / kConvBlockChunks;
+    j.first[i + 1] = j.first[i] + static_cast<int>(blocks < 1 ? 1 : blocks);
+  }
+  return j;
+}
+
+// Block b of a conversion job: all of its loads are issued before any store.
+__device__ __forceinline__ void convert_part(const ConvJob& job, int b) {
+  int i = 0;
+  while (i + 1 < job.count && b >= job.first[i + 1]) ++i;
+  const uint4* __restrict__ src = reinterpret_cast<const uint4*>(job.src[i]);
+  uint4* __restrict__ dst = reinterpret_cast<uint4*>(job.dst[i]);
+  const long long n = job.n[i], n8 = n / 8;
+  const long long c0 = static_cast<long long>(b - job.first[i]) * kConvBlockChunks + threadIdx.x;
+  uint4 v[kConvChunks];
+#pragma unroll
+  for (int k = 0; k < kConvChunks; ++k) {
+    const long long c = c0 + static_cast<long long>(k) * kRowThreads;
+    if (c < n8) v[k] = src[c];
+  }
+#pragma unroll
+  for (int k = 0; k < kConvChunks; ++k) {
+    const long long c = c0 + static_cast<long long>(k) * kRowThreads;
+    if (c < n8) dst[c] = bf16x8_to_f16x8(v[k]);
+  }
+  if (b == job.first[i + 1] - 1) {  // the array's last block: its ragged tail
+    const bf16* s1 = job.src[i];
+    __half* d1 = job.dst[i];
+    for (long long e = n8 * 8 + threadIdx.x; e < n; e += kRowThreads)
+      d1[e] = __float2half_rn(__bfloat162float(s1[e]));
+  }
+}
+
 // Row held in registers: NP pairs per lane, d <= 64 * NP, d even.  TX input,
 // TP gain/bias, TY output.
 template <typename TX, typename TP, typename TY, int NP>
 __global__ void __launch_bounds__(kRowThreads)
     layer_norm_reg(const TX* __restrict__ x, const TP* __restrict__ g, const TP* __restrict__ b,
-                   int rows, int d, TY* __restrict__ y) {
+                   int rows, int d, TY* __restrict__ y, const __grid_constant__ ConvJob side) {
   pdl_trigger();
   pdl_wait();
-  const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+  const int conv_blocks = side.first[side.count];
+  if (static_cast<int>(blockIdx.x) < conv_blocks) {
+    convert_part(side, blockIdx.x);
+    return;
+  }
+  const int row = (blockIdx.x - conv_blocks) * kRowsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
   const TX* xr = x + static_cast<size_t>(row) * d;
@@ -107,10 +175,15 @@ __device__ __forceinline__ void st1(__half* p, float v) { *p = __float2half_rn(v
 template <typename TX, typename TP, typename TY>
 __global__ void __launch_bounds__(kRowThreads)
     layer_norm_any(const TX* __restrict__ x, const TP* __restrict__ g, const TP* __restrict__ b,
-                   int rows, int d, TY* __restrict__ y) {
+                   int rows, int d, TY* __restrict__ y, const __grid_constant__ ConvJob side) {
   pdl_trigger();
   pdl_wait();
-  const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+  const int conv_blocks = side.first[side.count];
+  if (static_cast<int>(blockIdx.x) < conv_blocks) {
+    convert_part(side, blockIdx.x);
+    return;
+  }
+  const int row = (blockIdx.x - conv_blocks) * kRowsPerBlock + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
   const TX* xr = x + static_cast<size_t>(row) * d;
@@ -127,57 +200,27 @@ __global__ void __launch_bounds__(kRowThreads)
   for (int c = lane; c < d; c += 32) st1(yr + c, (ld1(xr + c) - u) * rstd * ld1(g + c) + ld1(b + c));
 }
 
+// The conversion blocks come first in the grid, so they start in the first
+// wave; the LayerNorm rows follow.
 template <typename TX, typename TP, typename TY>
-int ln_dispatch(const TX* x, const TP* g, const TP* b, int rows, int d, TY* y, cudaStream_t s) {
-  const unsigned blocks = static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock);
+int ln_dispatch(const TX* x, const TP* g, const TP* b, int rows, int d, TY* y, cudaStream_t s,
+                const ConvJob& side) {
+  const unsigned blocks = static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock) +
+                          static_cast<unsigned>(side.first[side.count]);
   const dim3 grid(blocks), block(kRowThreads);
   cudaError_t e;
   if (d % 2 == 0 && d <= 64 * 4) {
-    e = launch_pdl(layer_norm_reg<TX, TP, TY, 4>, grid, block, 0, s, x, g, b, rows, d, y);
+    e = launch_pdl(layer_norm_reg<TX, TP, TY, 4>, grid, block, 0, s, x, g, b, rows, d, y, side);
   } else if (d % 2 == 0 && d <= 64 * 12) {
-    e = launch_pdl(layer_norm_reg<TX, TP, TY, 12>, grid, block, 0, s, x, g, b, rows, d, y);
+    e = launch_pdl(layer_norm_reg<TX, TP, TY, 12>, grid, block, 0, s, x, g, b, rows, d, y, side);
   } else if (d % 2 == 0 && d <= 64 * 16) {
-    e = launch_pdl(layer_norm_reg<TX, TP, TY, 16>, grid, block, 0, s, x, g, b, rows, d, y);
+    e = launch_pdl(layer_norm_reg<TX, TP, TY, 16>, grid, block, 0, s, x, g, b, rows, d, y, side);
   } else if (d % 2 == 0 && d <= 64 * 25) {
-    e = launch_pdl(layer_norm_reg<TX, TP, TY, 25>, grid, block, 0, s, x, g, b, rows, d, y);
+    e = launch_pdl(layer_norm_reg<TX, TP, TY, 25>, grid, block, 0, s, x, g, b, rows, d, y, side);
   } else {
-    e = launch_pdl(layer_norm_any<TX, TP, TY>, grid, block, 0, s, x, g, b, rows, d, y);
+    e = launch_pdl(layer_norm_any<TX, TP, TY>, grid, block, 0, s, x, g, b, rows, d, y, side);
   }
   return e == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
-}
-
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 v) {
-  return make_uint4(pack_f16x2(bf16_lo(v.x), bf16_hi(v.x)), pack_f16x2(bf16_lo(v.y), bf16_hi(v.y)),
-                    pack_f16x2(bf16_lo(v.z), bf16_hi(v.z)), pack_f16x2(bf16_lo(v.w), bf16_hi(v.w)));
-}
-
-// Element-wise bf16 -> fp16 for several arrays; blockIdx.y picks the array.
-// Grid-stride over 16-byte chunks with four loads in flight per thread.  A
-// bf16 value converts exactly unless its magnitude is below 2^-14 (fp16
-// subnormal range) or above 65504.
-__global__ void __launch_bounds__(256) convert_f16(const ConvSegs segs) {
-  pdl_trigger();
-  pdl_wait();
-  const int sgi = blockIdx.y;
-  const uint4* __restrict__ src = reinterpret_cast<const uint4*>(segs.src[sgi]);
-  uint4* __restrict__ dst = reinterpret_cast<uint4*>(segs.dst[sgi]);
-  const long long n = segs.n[sgi];
-  const long long n8 = n / 8;
-  const long long stride = 256LL * gridDim.x;
-  long long i = blockIdx.x * 256LL + threadIdx.x;
-  for (; i + 3 * stride < n8; i += 4 * stride) {
-    const uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride], d = src[i + 3 * stride];
-    dst[i] = bf16x8_to_f16x8(a);
-    dst[i + stride] = bf16x8_to_f16x8(b);
-    dst[i + 2 * stride] = bf16x8_to_f16x8(c);
-    dst[i + 3 * stride] = bf16x8_to_f16x8(d);
-  }
-  for (; i < n8; i += stride) dst[i] = bf16x8_to_f16x8(src[i]);
-  if (blockIdx.x == 0) {
-    const bf16* s1 = segs.src[sgi];
-    __half* d1 = segs.dst[sgi];
-    for (long long j = n8 * 8 + threadIdx.x; j < n; j += 256) d1[j] = __float2half_rn(__bfloat162float(s1[j]));
-  }
 }
 
 // ---------------------------------------------------------------- embed ----
@@ -243,40 +286,30 @@ __global__ void __launch_bounds__(kRowThreads)
 }  // namespace
 
 int launch_layer_norm(int mode, const void* x, int x_dtype, const void* g, const void* b, int rows,
-                      int d, void* y, cudaStream_t stream, bool y_f16) {
+                      int d, void* y, cudaStream_t stream, bool y_f16, const ConvSegs* side) {
   if (rows <= 0 || d <= 0) return GPT2_ERR_INVALID_ARG;
+  if (side && (side->count < 0 || side->count > kMaxConvSegs)) return GPT2_ERR_INVALID_ARG;
+  const ConvJob job = make_conv_job(side);
   if (mode == GPT2_BF16) {
     if (d % 2 != 0) return GPT2_ERR_UNSUPPORTED;
     const bf16* gg = static_cast<const bf16*>(g);
     const bf16* bb = static_cast<const bf16*>(b);
     if (x_dtype == GPT2_FP32) {
       const float* xx = static_cast<const float*>(x);
-      return y_f16 ? ln_dispatch(xx, gg, bb, rows, d, static_cast<__half*>(y), stream)
-                   : ln_dispatch(xx, gg, bb, rows, d, static_cast<bf16*>(y), stream);
+      return y_f16 ? ln_dispatch(xx, gg, bb, rows, d, static_cast<__half*>(y), stream, job)
+                   : ln_dispatch(xx, gg, bb, rows, d, static_cast<bf16*>(y), stream, job);
     }
     if (x_dtype == GPT2_BF16) {
       const bf16* xx = static_cast<const bf16*>(x);
-      return y_f16 ? ln_dispatch(xx, gg, bb, rows, d, static_cast<__half*>(y), stream)
-                   : ln_dispatch(xx, gg, bb, rows, d, static_cast<bf16*>(y), stream);
+      return y_f16 ? ln_dispatch(xx, gg, bb, rows, d, static_cast<__half*>(y), stream, job)
+                   : ln_dispatch(xx, gg, bb, rows, d, static_cast<bf16*>(y), stream, job);
     }
     return GPT2_ERR_INVALID_ARG;
   }
   if (mode == GPT2_FP32 && x_dtype == GPT2_FP32)
     return ln_dispatch(static_cast<const float*>(x), static_cast<const float*>(g),
-                       static_cast<const float*>(b), rows, d, static_cast<float*>(y), stream);
+                       static_cast<const float*>(b), rows, d, static_cast<float*>(y), stream, job);
   return GPT2_ERR_INVALID_ARG;
-}
-
-int launch_convert_f16(const ConvSegs& segs, cudaStream_t stream) {
-  if (segs.count <= 0 || segs.count > kMaxConvSegs) return GPT2_ERR_INVALID_ARG;
-  long long most = 0;
-  for (int i = 0; i < segs.count; ++i) most = segs.n[i] > most ? segs.n[i] : most;
-  // About four 16-byte chunks per thread for the largest array.
-  const long long want = (most / 8 + 1023) / 1024;
-  const unsigned gx = static_cast<unsigned>(want < 1 ? 1 : (want > 2048 ? 2048 : want));
-  const cudaError_t e =
-      launch_pdl(convert_f16, dim3(gx, segs.count), dim3(256), 0, stream, segs);
-  return e == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
 int launch_embed(int mode, const int32_t* ids, const void* wte, const void* wpe, int B, int T,
