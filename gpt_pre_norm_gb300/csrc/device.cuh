@@ -113,6 +113,24 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// 3-D / 4-D tiled loads, as above.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
+                                            int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
+                                            int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
 // 2-D / 3-D tiled stores of a shared-memory box to global memory (bulk
 // async-group completion).  Coordinates outside the tensor are not written.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
@@ -279,12 +297,14 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
       : "memory");
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16 with fp32 D, both operands
-// K-major, tile M x N; A and B both bf16 (f16 = false) or both fp16.
-__host__ __device__ constexpr uint32_t umma_idesc_16(int M, int N, bool f16) {
+// Instruction descriptor of tcgen05.mma kind::f16 with fp32 D, tile M x N;
+// A and B both bf16 (f16 = false) or both fp16; A K-major, B K-major or (b_mn)
+// MN-major.
+__host__ __device__ constexpr uint32_t umma_idesc_16(int M, int N, bool f16, bool b_mn = false) {
   return (1u << 4)                                 // D format: f32
          | ((f16 ? 0u : 1u) << 7)                  // A format: f16 = 0, bf16 = 1
          | ((f16 ? 0u : 1u) << 10)                 // B format: same as A
+         | ((b_mn ? 1u : 0u) << 16)                // B major: K = 0, MN = 1
          | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
 }
@@ -298,6 +318,22 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
   d |= static_cast<uint64_t>(1) << 16;                   // leading byte offset (unused here)
   d |= static_cast<uint64_t>(1024 >> 4) << 32;           // stride byte offset: 8 rows
+  d |= static_cast<uint64_t>(1) << 46;                   // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                   // 128-byte swizzle
+  return d;
+}
+
+// Shared-memory matrix descriptor of an MN-major operand tile stored with
+// the 128-byte swizzle: each 128-byte row holds 64 consecutive MN elements of
+// one k, and groups of 8 k-rows lie 1024 B apart (the stride byte offset).
+// For an operand 64 elements wide in MN this is one swizzle atom across, so
+// the leading byte offset is not used.  Advancing k by 16 moves the start
+// 2048 bytes.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= static_cast<uint64_t>(1) << 16;                   // leading byte offset (unused here)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;           // stride byte offset: 8 k-rows
   d |= static_cast<uint64_t>(1) << 46;                   // descriptor version
   d |= static_cast<uint64_t>(2) << 61;                   // 128-byte swizzle
   return d;

@@ -328,9 +328,9 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int slot, int B, int
       const double pairs = static_cast<double>(T) * t_past + 0.5 * T * (T + 1.0);
       *fl = 4.0 * B * h * pairs * dh;
       *by = static_cast<double>(B) * h * (2.0 * T * dh * 2 + 2.0 * t_len * dh * 2);
-      return launch_attention_bf16(static_cast<const bf16*>(q),
-                                   reinterpret_cast<const bf16*>(kv.base), kv.s_batch, kv.s_kv,
-                                   kv.s_head, B, h, T, t_past, attn, s, true);
+      return launch_attention_tc(c->env, static_cast<const bf16*>(q),
+                                 reinterpret_cast<const bf16*>(kv.base), kv.s_batch, kv.s_kv,
+                                 kv.s_head, B, h, T, t_past, attn, s, true);
     });
   } else {
     st = c->run(kKindSimtFp32, s, [&](double*, double*) {
@@ -707,9 +707,9 @@ int gpt2_attention(gpt2_ctx* c, const void* q, const void* kv, int B, int n_head
   }
   if (bf)
     return c->run(kKindAttention, s, [&](double*, double*) {
-      return launch_attention_bf16(static_cast<const bf16*>(q),
-                                   reinterpret_cast<const bf16*>(v.base), v.s_batch, v.s_kv,
-                                   v.s_head, B, n_head, T, T_past, out, s);
+      return launch_attention_tc(c->env, static_cast<const bf16*>(q),
+                                 reinterpret_cast<const bf16*>(v.base), v.s_batch, v.s_kv,
+                                 v.s_head, B, n_head, T, T_past, out, s, false);
     });
   return c->run(kKindSimtFp32, s, [&](double*, double*) {
     return launch_attention_fp32(static_cast<const float*>(q),

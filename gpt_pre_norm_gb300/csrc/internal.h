@@ -120,8 +120,13 @@ int launch_layer_norm(int mode, const void* x, int x_dtype, const void* g, const
 int launch_embed(int mode, const int32_t* ids, const void* wte, const void* wpe, int B, int T,
                  int t_past, int d, int n_vocab, float* H, unsigned* err, cudaStream_t stream);
 
-// Causal prefill attention, bf16 Q/K/V, d_h = 64 (tensor cores); the output
-// [B, T, h*64] is fp16 when out_f16, else bf16.
+// Causal prefill attention, bf16 Q/K/V, d_h = 64, on tcgen05 (TMEM
+// accumulators, TMA); the output [B, T, h*64] is fp16 when out_f16, else bf16.
+int launch_attention_tc(const LaunchEnv& env, const bf16* q, const bf16* kv, long long s_batch,
+                        long long s_kv, long long s_head, int B, int h, int T, int t_past,
+                        void* out, cudaStream_t stream, bool out_f16);
+
+// The same on the legacy tensor-core path (mma.sync).
 int launch_attention_bf16(const bf16* q, const bf16* kv, long long kv_s_batch, long long kv_s_kv,
                           long long kv_s_head, int B, int h, int T, int t_past, void* out,
                           cudaStream_t stream, bool out_f16 = false);
