@@ -8,14 +8,7 @@
 // values are read from the KV cache the c_attn epilogue wrote; the output is
 // written with heads merged, [B, T, h * d_h].
 //
-//   attn_prefill_bf16   d_h = 64.  One CTA per (128-query tile, sequence x
-//                       head), 8 warps of 16 query rows.  Key/value tiles of 64
-//                       stream through a cp.async double buffer; S = Q K^T and
-//                       O += P V run on the tensor cores (mma.sync m16n8k16,
-//                       bf16 in, fp32 accumulate); softmax is online in
-//                       registers with exp2; tiles entirely above the diagonal
-//                       are never loaded, and the tiles with the most keys are
-//                       scheduled first.
+//   (causal prefill on the tcgen05 tensor cores is in attn_tc.cu)
 //   attn_decode_bf16    one new token: split over keys, 8 warps per CTA, each
 //                       8-lane group streams one key per step with 16-byte
 //                       loads; partial (max, sum, o) merged in shared memory,
@@ -33,201 +26,8 @@ namespace gpt2 {
 namespace {
 
 constexpr int kDh = 64;
-constexpr int kQTile = 128;
-constexpr int kKTile = 64;
-constexpr int kAttnThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Byte offset of 16-byte chunk c of row r in a [rows x 64] bf16 tile whose
-// chunks are XOR-swizzled by the row's low three bits (conflict-free ldmatrix).
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-  return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
-}
-
-__global__ void __launch_bounds__(kAttnThreads, 2)
-    attn_prefill_bf16(const bf16* __restrict__ q, const bf16* __restrict__ kv, long long s_batch,
-                      long long s_kv, long long s_head, int h, int T, int t_past,
-                      uint16_t* __restrict__ out, int n_qtiles, int out_f16) {
-  __shared__ __align__(128) uint8_t sQ[kQTile * 128];
-  __shared__ __align__(128) uint8_t sK[2][kKTile * 128];
-  __shared__ __align__(128) uint8_t sV[2][kKTile * 128];
-  pdl_trigger();
-  pdl_wait();
-
-  const int bh = blockIdx.x;
-  const int qt = n_qtiles - 1 - static_cast<int>(blockIdx.y);  // most keys first
-  const int b = bh / h, head = bh - b * h;
-  const int q0 = qt * kQTile;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int t_all = t_past + T;
-
-  const bf16* Qg = q + static_cast<size_t>(bh) * T * kDh;
-  const bf16* Kg = kv + b * s_batch + head * s_head;
-  const bf16* Vg = Kg + s_kv;
-
-  // Keys this tile needs: up to the last query row's position.
-  const int q_last = min(q0 + kQTile, T) - 1;
-  const int kv_len = t_past + q_last + 1;
-  const int n_kt = (kv_len + kKTile - 1) / kKTile;
-
-  const uint32_t sQa = smem_u32(sQ);
-  const uint32_t sKa[2] = {smem_u32(sK[0]), smem_u32(sK[1])};
-  const uint32_t sVa[2] = {smem_u32(sV[0]), smem_u32(sV[1])};
-
-  // Q tile: 128 rows x 8 chunks.
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int idx = tid + i * kAttnThreads;
-    const int r = idx >> 3, c = idx & 7;
-    const bool valid = q0 + r < T;
-    const bf16* src = Qg + static_cast<size_t>(valid ? q0 + r : 0) * kDh + c * 8;
-    cp_async_16(sQa + swz(r, c), src, valid);
-  }
-  auto load_kv = [&](int j, int buf) {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int idx = tid + i * kAttnThreads;
-      const int r = idx >> 3, c = idx & 7;
-      const int key = j * kKTile + r;
-      const bool valid = key < t_all;
-      const size_t off = static_cast<size_t>(valid ? key : 0) * kDh + c * 8;
-      cp_async_16(sKa[buf] + swz(r, c), Kg + off, valid);
-      cp_async_16(sVa[buf] + swz(r, c), Vg + off, valid);
-    }
-  };
-  load_kv(0, 0);
-  cp_async_commit();
-
-  const int g = lane >> 2, tq = lane & 3;
-  const int row_lo = 16 * warp;                   // warp's first row in the tile
-  const int pos_lo = t_past + q0 + row_lo;        // its absolute position
-  const int pos_a = pos_lo + g, pos_b = pos_a + 8;
-  const float sl2 = 0.125f * kLog2e;              // 1/sqrt(64) in log2 units
-
-  uint32_t qf[4][4];
-  float o[8][4];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) o[i][j] = 0.f;
-  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-
-  for (int j = 0; j < n_kt; ++j) {
-    if (j + 1 < n_kt) load_kv(j + 1, (j + 1) & 1);
-    cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();
-    if (j == 0) {
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        ldmatrix_x4(qf[kk], sQa + swz(row_lo + (lane & 15), 2 * kk + (lane >> 4)));
-    }
-    const int kbase = j * kKTile;
-    const int buf = j & 1;
-    if (kbase <= pos_lo + 15) {  // some key of this tile is visible to the warp
-      float s[8][4];
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) s[i][e] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-        for (int np = 0; np < 4; ++np) {
-          uint32_t r[4];
-          ldmatrix_x4(r, sKa[buf] + swz(16 * np + ((lane >> 4) << 3) + (lane & 7),
-                                        2 * kk + ((lane >> 3) & 1)));
-          mma_bf16_16816(s[2 * np], qf[kk], r[0], r[1]);
-          mma_bf16_16816(s[2 * np + 1], qf[kk], r[2], r[3]);
-        }
-      }
-      if (kbase + kKTile - 1 > pos_lo) {  // the tile crosses this warp's diagonal
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-          const int key = kbase + 8 * nt + 2 * tq;
-          if (key > pos_a) s[nt][0] = -INFINITY;
-          if (key + 1 > pos_a) s[nt][1] = -INFINITY;
-          if (key > pos_b) s[nt][2] = -INFINITY;
-          if (key + 1 > pos_b) s[nt][3] = -INFINITY;
-        }
-      }
-      float mx_a = -INFINITY, mx_b = -INFINITY;
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        mx_a = fmaxf(mx_a, fmaxf(s[nt][0], s[nt][1]));
-        mx_b = fmaxf(mx_b, fmaxf(s[nt][2], s[nt][3]));
-      }
-      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-      const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-      const float base_a = (mn_a == -INFINITY) ? 0.f : mn_a * sl2;
-      const float base_b = (mn_b == -INFINITY) ? 0.f : mn_b * sl2;
-      const float alpha_a = ex2(m_a * sl2 - base_a), alpha_b = ex2(m_b * sl2 - base_b);
-      m_a = mn_a;
-      m_b = mn_b;
-      float sum_a = 0.f, sum_b = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        s[nt][0] = ex2(fmaf(s[nt][0], sl2, -base_a));
-        s[nt][1] = ex2(fmaf(s[nt][1], sl2, -base_a));
-        s[nt][2] = ex2(fmaf(s[nt][2], sl2, -base_b));
-        s[nt][3] = ex2(fmaf(s[nt][3], sl2, -base_b));
-        sum_a += s[nt][0] + s[nt][1];
-        sum_b += s[nt][2] + s[nt][3];
-      }
-      l_a = l_a * alpha_a + sum_a;
-      l_b = l_b * alpha_b + sum_b;
-#pragma unroll
-      for (int nd = 0; nd < 8; ++nd) {
-        o[nd][0] *= alpha_a;
-        o[nd][1] *= alpha_a;
-        o[nd][2] *= alpha_b;
-        o[nd][3] *= alpha_b;
-      }
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        uint32_t pa[4];
-        pa[0] = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
-        pa[1] = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
-        pa[2] = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-        pa[3] = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-#pragma unroll
-        for (int dp = 0; dp < 4; ++dp) {
-          uint32_t r[4];
-          ldmatrix_x4_trans(r, sVa[buf] + swz(16 * kk + (((lane >> 3) & 1) << 3) + (lane & 7),
-                                              2 * dp + (lane >> 4)));
-          mma_bf16_16816(o[2 * dp], pa, r[0], r[1]);
-          mma_bf16_16816(o[2 * dp + 1], pa, r[2], r[3]);
-        }
-      }
-    }
-    __syncthreads();  // buffer `buf` is refilled two iterations later
-  }
-  cp_async_wait<0>();
-
-  l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-  l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-  l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-  l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-  const float inv_a = 1.f / l_a, inv_b = 1.f / l_b;
-  const int d = h * kDh;
-  const int ra = q0 + row_lo + g, rb = ra + 8;
-  uint16_t* outb = out + static_cast<size_t>(b) * T * d + head * kDh + 2 * tq;
-  const bool f16 = out_f16 != 0;
-#pragma unroll
-  for (int nd = 0; nd < 8; ++nd) {
-    if (ra < T)
-      *reinterpret_cast<uint32_t*>(outb + static_cast<size_t>(ra) * d + 8 * nd) =
-          pack_16x2(o[nd][0] * inv_a, o[nd][1] * inv_a, f16);
-    if (rb < T)
-      *reinterpret_cast<uint32_t*>(outb + static_cast<size_t>(rb) * d + 8 * nd) =
-          pack_16x2(o[nd][2] * inv_b, o[nd][3] * inv_b, f16);
-  }
-}
-
-// ------------------------------------------------------------------ decode --
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kPartialStride = kDh + 2;  // o[64], m, l
@@ -445,19 +245,6 @@ __global__ void attn_fp32(const float* __restrict__ q, const float* __restrict__
 }
 
 }  // namespace
-
-int launch_attention_bf16(const bf16* q, const bf16* kv, long long s_batch, long long s_kv,
-                          long long s_head, int B, int h, int T, int t_past, void* out,
-                          cudaStream_t stream, bool out_f16) {
-  if (B <= 0 || h <= 0 || T <= 0 || t_past < 0) return GPT2_ERR_INVALID_ARG;
-  const int n_qtiles = (T + kQTile - 1) / kQTile;
-  if (n_qtiles > 65535) return GPT2_ERR_UNSUPPORTED;
-  dim3 grid(B * h, n_qtiles);
-  const cudaError_t e = launch_pdl(attn_prefill_bf16, grid, dim3(kAttnThreads), 0, stream, q, kv,
-                                   s_batch, s_kv, s_head, h, T, t_past,
-                                   static_cast<uint16_t*>(out), n_qtiles, out_f16 ? 1 : 0);
-  return e == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
-}
 
 size_t decode_partials_floats(int B, int h, int splits) {
   return static_cast<size_t>(B) * h * splits * kPartialStride;

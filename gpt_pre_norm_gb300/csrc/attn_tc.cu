@@ -10,7 +10,10 @@
 //
 // One CTA per (sequence x head, 128-query tile), 6 warps, two CTAs per SM:
 //   warp 0      TMA: the Q tile once, then the 64-key K and V tiles of each
-//               step into a 3-stage ring (128-byte swizzle).
+//               step into separate rings (128-byte swizzle): a K stage is
+//               free again once its scores are computed, a V stage only
+//               after its P V product, so K runs further ahead.  One thread
+//               polls both rings and issues whichever copy is possible.
 //   warp 1      allocates 256 TMEM columns; one thread issues
 //                 S_j = Q K_j^T  (M=128, N=64, K=64; K-major operands)
 //               into one of two TMEM score buffers, one step ahead, and
@@ -43,7 +46,8 @@ namespace {
 constexpr int kD = 64;
 constexpr int kQT = 128;                        // queries per CTA
 constexpr int kKT = 64;                         // keys per step
-constexpr int kStages = 3;                      // K/V ring
+constexpr int kSK = 4;                          // K ring
+constexpr int kSV = 3;                          // V ring
 constexpr int kThreads = 192;
 constexpr uint32_t kQBytes = kQT * kD * 2;      // 16 KB
 constexpr uint32_t kKVBytes = kKT * kD * 2;     // 8 KB: one K or V tile
@@ -52,21 +56,15 @@ constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0;                   // two score buffers of 64 columns
 constexpr uint32_t kColO = 128;                 // two partial-output buffers of 64
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kBars = 1 + 2 * kStages + 5 * 2 + 1;
+constexpr int kBars = 1 + 2 * kSK + 2 * kSV + 5 * 2 + 1;
 constexpr size_t kSmemBytes =
-    1024 + kQBytes + 2 * kStages * kKVBytes + 2 * kPBytes + kBars * 8 + 16;
+    1024 + kQBytes + (kSK + kSV) * kKVBytes + 2 * kPBytes + kBars * 8 + 16;
 
 struct AttnArgs {
   int T, t_past, h, n_qtiles;
   int out_f16;  // output fp16 (else bf16)
   unsigned* err;
 };
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 __global__ void __launch_bounds__(kThreads, 2)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -76,13 +74,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = sm;
-  uint8_t* sK = sQ + kQBytes;                  // [kStages][8 KB]
-  uint8_t* sV = sK + kStages * kKVBytes;       // [kStages][8 KB]
-  uint8_t* sP = sV + kStages * kKVBytes;       // [2][16 KB]
+  uint8_t* sK = sQ + kQBytes;                  // [kSK][8 KB]
+  uint8_t* sV = sK + kSK * kKVBytes;           // [kSV][8 KB]
+  uint8_t* sP = sV + kSV * kKVBytes;           // [2][16 KB]
   uint64_t* q_full = reinterpret_cast<uint64_t*>(sP + 2 * kPBytes);
-  uint64_t* kv_full = q_full + 1;              // [kStages] K and V landed
-  uint64_t* kv_empty = kv_full + kStages;      // [kStages] both products done with them
-  uint64_t* s_full = kv_empty + kStages;       // [2] scores ready
+  uint64_t* k_full = q_full + 1;               // [kSK] K landed
+  uint64_t* k_empty = k_full + kSK;            // [kSK] its scores computed
+  uint64_t* v_full = k_empty + kSK;            // [kSV] V landed
+  uint64_t* v_empty = v_full + kSV;            // [kSV] its P V product done
+  uint64_t* s_full = v_empty + kSV;            // [2] scores ready
   uint64_t* s_free = s_full + 2;               // [2] scores read (4 warps)
   uint64_t* p_full = s_free + 2;               // [2] P written (4 warps)
   uint64_t* pv_done = p_full + 2;              // [2] P V product done (P read, O ready)
@@ -101,9 +101,13 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+    for (int s = 0; s < kSK; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < kSV; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -134,26 +138,52 @@ __global__ void __launch_bounds__(kThreads, 2)
     tma_prefetch_desc(&tmV);
     mbar_arrive_expect_tx(q_full, kQBytes);
     tma_load_3d(sQ, &tmQ, q_full, 0, q0, bh);
-    int issued = 0;
+    // Next K and V steps to load; a stage is free once the product that read
+    // its previous tile has completed (no wait for the first pass).
+    int kj = 0, vj = 0;
     bool ok = true;
-    for (int j = 0; j < n_kt; ++j) {
-      const int s = j % kStages;
-      const uint32_t use = static_cast<uint32_t>(j / kStages);
-      if (j >= kStages && !mbar_wait_bounded(&kv_empty[s], (use - 1) & 1u, abort_flag, a.err)) {
-        ok = false;
-        break;
+    unsigned long long t_idle = 0;
+    while (kj < n_kt || vj < n_kt) {
+      bool progress = false;
+      if (kj < n_kt && (kj < kSK || mbar_test_wait(&k_empty[kj % kSK],
+                                                   static_cast<uint32_t>(kj / kSK - 1) & 1u))) {
+        const int s = kj % kSK;
+        mbar_arrive_expect_tx(&k_full[s], kKVBytes);
+        tma_load_4d(sK + s * kKVBytes, &tmK, &k_full[s], 0, kj * kKT, head, b);
+        ++kj;
+        progress = true;
       }
-      mbar_arrive_expect_tx(&kv_full[s], 2 * kKVBytes);
-      tma_load_4d(sK + s * kKVBytes, &tmK, &kv_full[s], 0, j * kKT, head, b);
-      tma_load_4d(sV + s * kKVBytes, &tmV, &kv_full[s], 0, j * kKT, head, b);
-      issued = j + 1;
+      if (vj < n_kt && (vj < kSV || mbar_test_wait(&v_empty[vj % kSV],
+                                                   static_cast<uint32_t>(vj / kSV - 1) & 1u))) {
+        const int s = vj % kSV;
+        mbar_arrive_expect_tx(&v_full[s], kKVBytes);
+        tma_load_4d(sV + s * kKVBytes, &tmV, &v_full[s], 0, vj * kKT, head, b);
+        ++vj;
+        progress = true;
+      }
+      if (progress) {
+        t_idle = 0;
+      } else {
+        // Neither ring has a free stage: the same bounded wait as elsewhere.
+        __nanosleep(32);
+        const unsigned long long now = global_timer_ns();
+        if (t_idle == 0) {
+          t_idle = now;
+        } else if (*abort_flag || now - t_idle > kWaitLimitNs) {
+          if (!*abort_flag) raise_error(a.err, kErrTimeout);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+      }
     }
     if (!ok) {
       // Drain: every copy already issued must land before the CTA exits.
       mbar_wait_bounded(q_full, 0, nullptr, a.err);
-      for (int j = max(0, issued - kStages); j < issued; ++j)
-        mbar_wait_bounded(&kv_full[j % kStages], static_cast<uint32_t>(j / kStages) & 1u, nullptr,
-                          a.err);
+      for (int j = max(0, kj - kSK); j < kj; ++j)
+        mbar_wait_bounded(&k_full[j % kSK], static_cast<uint32_t>(j / kSK) & 1u, nullptr, a.err);
+      for (int j = max(0, vj - kSV); j < vj; ++j)
+        mbar_wait_bounded(&v_full[j % kSV], static_cast<uint32_t>(j / kSV) & 1u, nullptr, a.err);
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------- MMA issuer --
@@ -162,8 +192,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint64_t q_desc = sdesc_k_sw128(smem_u32(sQ));
     bool ok = mbar_wait_bounded(q_full, 0, abort_flag, a.err);
     auto issue_s = [&](int j) -> bool {
-      const int s = j % kStages, sb = j & 1;
-      if (!mbar_wait_bounded(&kv_full[s], static_cast<uint32_t>(j / kStages) & 1u, abort_flag, a.err))
+      const int s = j % kSK, sb = j & 1;
+      if (!mbar_wait_bounded(&k_full[s], static_cast<uint32_t>(j / kSK) & 1u, abort_flag, a.err))
         return false;
       if (j >= 2 &&
           !mbar_wait_bounded(&s_free[sb], static_cast<uint32_t>((j >> 1) - 1) & 1u, abort_flag, a.err))
@@ -175,13 +205,15 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int k = 0; k < kD / 16; ++k)
         umma_f16kind(d, q_desc + 2 * k, k_desc + 2 * k, id_s, k != 0 ? 1u : 0u);
       umma_commit(&s_full[sb]);
+      umma_commit(&k_empty[s]);
       return true;
     };
     if (ok) ok = issue_s(0);
     for (int j = 0; ok && j < n_kt; ++j) {
       if (j + 1 < n_kt && !(ok = issue_s(j + 1))) break;
-      const int pb = j & 1, s = j % kStages;
-      if (!mbar_wait_bounded(&p_full[pb], static_cast<uint32_t>(j >> 1) & 1u, abort_flag, a.err) ||
+      const int pb = j & 1, s = j % kSV;
+      if (!mbar_wait_bounded(&v_full[s], static_cast<uint32_t>(j / kSV) & 1u, abort_flag, a.err) ||
+          !mbar_wait_bounded(&p_full[pb], static_cast<uint32_t>(j >> 1) & 1u, abort_flag, a.err) ||
           (j >= 2 && !mbar_wait_bounded(&o_free[pb], static_cast<uint32_t>((j >> 1) - 1) & 1u,
                                         abort_flag, a.err))) {
         ok = false;
@@ -195,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int k = 0; k < kKT / 16; ++k)  // 16 keys: +32 B in P's rows, +2048 B in V's
         umma_f16kind(d, p_desc + 2 * k, v_desc + 128 * k, id_pv, k != 0 ? 1u : 0u);
       umma_commit(&pv_done[pb]);
-      umma_commit(&kv_empty[s]);
+      umma_commit(&v_empty[s]);
     }
     // Every MMA issued above must retire before TMEM is freed.
     umma_commit(mma_done);

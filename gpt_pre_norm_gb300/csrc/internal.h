@@ -126,10 +126,6 @@ int launch_attention_tc(const LaunchEnv& env, const bf16* q, const bf16* kv, lon
                         long long s_kv, long long s_head, int B, int h, int T, int t_past,
                         void* out, cudaStream_t stream, bool out_f16);
 
-// The same on the legacy tensor-core path (mma.sync).
-int launch_attention_bf16(const bf16* q, const bf16* kv, long long kv_s_batch, long long kv_s_kv,
-                          long long kv_s_head, int B, int h, int T, int t_past, void* out,
-                          cudaStream_t stream, bool out_f16 = false);
 
 // Single-token decode attention, bf16 Q/K/V, d_h = 64: split over keys,
 // partial results combined through `partials` (floats, see
