@@ -419,4 +419,18 @@ __device__ __forceinline__ float gelu_tanh_approx(float x) {
   return 0.5f * x * (1.0f + tanh_approx(u));
 }
 
+// The same GELU on two values in fp16 arithmetic (tanh on the MUFU in
+// f16x2 form), returned as packed fp16: used where the result is stored as
+// fp16; its error is a few fp16 ulps of the output.
+__device__ __forceinline__ uint32_t gelu_tanh_f16x2(float a, float b) {
+  const __half2 x = __floats2half2_rn(a, b);
+  const __half2 inner = __hfma2(__hmul2(x, x), __float2half2_rn(0.044715f), __float2half2_rn(1.0f));
+  const __half2 u = __hmul2(__hmul2(x, __float2half2_rn(0.7978845608028654f)), inner);
+  uint32_t t;
+  asm("tanh.approx.f16x2 %0, %1;" : "=r"(t) : "r"(*reinterpret_cast<const uint32_t*>(&u)));
+  const __half2 hx = __hmul2(x, __float2half2_rn(0.5f));
+  const __half2 y = __hfma2(hx, *reinterpret_cast<const __half2*>(&t), hx);
+  return *reinterpret_cast<const uint32_t*>(&y);
+}
+
 }  // namespace gpt2

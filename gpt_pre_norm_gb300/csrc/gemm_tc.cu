@@ -142,6 +142,14 @@ __device__ __forceinline__ void box_write_16(uint8_t* box, int r, const float (&
     *reinterpret_cast<uint4*>(box + r * 64 + ((c ^ ((r >> 1) & 3)) << 4)) = pack8(v + 8 * c, f16);
 }
 
+// The same box row from 16 packed pairs.
+__device__ __forceinline__ void box_write_packed(uint8_t* box, int r, const uint32_t (&w)[16]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(box + r * 64 + ((c ^ ((r >> 1) & 3)) << 4)) =
+        make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+}
+
 // Per-warp epilogue state carried across chunks and tiles.
 struct EpiState {
   int chunk;          // chunks processed so far (selects the staging slot)
@@ -332,6 +340,35 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) + bv[j];
       if constexpr (KIND == kEpiGelu) {
+        if (out16) {
+          // fp16 output: GELU on packed pairs (half the instructions), the
+          // result already in its stored form.
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w[i] = gelu_tanh_f16x2(v[2 * i], v[2 * i + 1]);
+          if (tma_store_path) {
+            box_write_packed(ob, lane, w);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(tmO, ob, col, row0);
+              bulk_commit_group();
+            }
+          } else if (row_ok) {
+            uint16_t* o = static_cast<uint16_t*>(ep.out) + off;
+            if (full) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                reinterpret_cast<uint4*>(o)[i] =
+                    make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (col + j < N) o[j] = static_cast<uint16_t>(w[j >> 1] >> (16 * (j & 1)));
+            }
+          }
+          continue;
+        }
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = gelu_tanh_approx(v[j]);
       }
