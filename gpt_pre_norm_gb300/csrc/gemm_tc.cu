@@ -71,15 +71,19 @@ __host__ __device__ constexpr int slot_bytes(int k) {
 // another (the most the two accumulators allow) never overwrites a buffer
 // still being read.
 __host__ __device__ constexpr int epi_warp_bytes(int k) {
-  return k == kEpiLogits ? 32 * kLogitsLd * 4 : 2 * slot_bytes(k);
+  return k == kEpiLogits ? 32 * kLogitsLd * 4 : k == kEpiLogitsT ? 0 : 2 * slot_bytes(k);
 }
-__host__ __device__ constexpr int epi_bias_bytes(int k) { return k == kEpiLogits ? 0 : kBiasBytes; }
+__host__ __device__ constexpr int epi_bias_bytes(int k) {
+  return k == kEpiLogits || k == kEpiLogitsT ? 0 : kBiasBytes;
+}
 
 struct GemmArgs {
   int M, N, K;
   int BN;
   int stages;
   int num_m_blocks;
+  int num_n_blocks;
+  int n_inner;       // tile index runs over N blocks first (else over M blocks)
   int num_tiles;
   int vec_ok;        // row stride allows 16-byte vector access of out / resid
   int tma_out;       // output written by TMA stores through tmO
@@ -93,6 +97,16 @@ struct GemmArgs {
 };
 
 // Dynamic shared memory of one CTA; cg = 2 holds half of the tile's B rows.
+__device__ __forceinline__ void tile_coords(const GemmArgs& a, int tile, int& m_blk, int& n_blk) {
+  if (a.n_inner) {
+    m_blk = tile / a.num_n_blocks;
+    n_blk = tile - m_blk * a.num_n_blocks;
+  } else {
+    n_blk = tile / a.num_m_blocks;
+    m_blk = tile - n_blk * a.num_m_blocks;
+  }
+}
+
 __host__ __device__ inline size_t smem_bytes_for(int kind, int BN, int stages, int cg) {
   return 1024 /* alignment slack */ +
          static_cast<size_t>(stages) * (kABytes + (BN / cg) * kBK * 2) +
@@ -197,7 +211,7 @@ __device__ __forceinline__ void epilogue_prefetch(int row0, int ncol0, int ncols
                                                   uint8_t* epi, uint16_t* bias_s, uint64_t* rbar,
                                                   EpiState& s, const GemmArgs& a,
                                                   const CUtensorMap* tmR) {
-  if constexpr (KIND != kEpiLogits) {
+  if constexpr (KIND != kEpiLogits && KIND != kEpiLogitsT) {
     const int N = a.N;
     const int j = 4 * lane;
     if (j < ncols) {
@@ -256,7 +270,21 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol
     uint32_t r[32];
     const size_t off = static_cast<size_t>(row) * ep.ldo + col;
 
-    if constexpr (KIND == kEpiLogits) {
+    if constexpr (KIND == kEpiLogitsT) {
+      // Transposed accumulator (the head computed as W_e H^T): this thread's
+      // TMEM lane is vocabulary entry `row`, the chunk's 32 columns are 32
+      // consecutive tokens, so for each token the warp writes 32 consecutive
+      // logits of one row with one store, straight from registers.
+      tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), r);
+      tmem_ld_wait();
+      const int nt = min(32, N - col);  // tokens in this chunk
+      if (row_ok) {
+        float* o = static_cast<float*>(ep.out) + static_cast<size_t>(col) * ep.ldo + row;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < nt) o[static_cast<size_t>(j) * ep.ldo] = __uint_as_float(r[j]);
+      }
+    } else if constexpr (KIND == kEpiLogits) {
       // fp32 logits rows are only 4-byte aligned: transpose the chunk through
       // shared memory so each store instruction writes 32 consecutive columns
       // of one row.
@@ -520,7 +548,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     const uint32_t full0 = CG == 2 ? mapa_shared(smem_u32(full), 0u) : 0u;  // first CTA's barriers
     for (int tile = first_tile; ok && tile < args.num_tiles; tile += tile_step) {
-      const int m_blk = tile % args.num_m_blocks, n_blk = tile / args.num_m_blocks;
+      int m_blk, n_blk;
+      tile_coords(args, tile, m_blk, n_blk);
       const int a_row = m_blk * tile_rows + static_cast<int>(rank) * kBM;
       const int b_row = n_blk * BN + static_cast<int>(rank) * (BN / CG);
       for (int kb = 0; kb < KB; ++kb) {
@@ -627,7 +656,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = first_tile; tile < args.num_tiles; tile += tile_step, ++it) {
       const int acc = it & 1;
       const uint32_t acc_par = static_cast<uint32_t>((it >> 1) & 1);
-      const int m_blk = tile % args.num_m_blocks, n_blk = tile / args.num_m_blocks;
+      int m_blk, n_blk;
+      tile_coords(args, tile, m_blk, n_blk);
       const int row0 = m_blk * tile_rows + static_cast<int>(rank) * kBM + quarter * 32;
       const int ncol0 = n_blk * BN + half * ncols;
       uint16_t* bias_s = bias_half + (it % kBiasBufs) * 128;
@@ -684,6 +714,7 @@ void* kernel_for(int kind, int cg) {
     case kEpiResidBf16In: return kernel_ptr<kEpiResidBf16In>(cg);
     case kEpiResidBf16Out: return kernel_ptr<kEpiResidBf16Out>(cg);
     case kEpiLogits: return kernel_ptr<kEpiLogits>(cg);
+    case kEpiLogitsT: return kernel_ptr<kEpiLogitsT>(cg);
     case kEpiQkv: return kernel_ptr<kEpiQkv>(cg);
     default: return nullptr;
   }
@@ -766,19 +797,33 @@ int choose_bn(int M, int N, int tile_rows, int units) {
 
 }  // namespace
 
-int launch_gemm_tc(const LaunchEnv& env, int kind, const void* A, const void* W, int M, int N,
-                   int K, const EpiParams& ep, cudaStream_t stream, double* flops, double* bytes,
-                   bool operands_f16, bool out_f16) {
+int launch_gemm_tc(const LaunchEnv& env, int kind_in, const void* A_in, const void* W_in,
+                   int M_in, int N_in, int K, const EpiParams& ep, cudaStream_t stream,
+                   double* flops, double* bytes, bool operands_f16, bool out_f16) {
+  if (M_in <= 0 || N_in <= 0 || K <= 0 || kind_in < 0 || kind_in >= kEpiLogitsT)
+    return GPT2_ERR_INVALID_ARG;
+  if (K % 8 != 0) return GPT2_ERR_UNSUPPORTED;
+  if (kind_in != kEpiLogits && (N_in % 2 != 0)) return GPT2_ERR_UNSUPPORTED;
+  if (kind_in == kEpiQkv && (ep.d % 64 != 0 || N_in != 3 * ep.d)) return GPT2_ERR_UNSUPPORTED;
+  // The tied head runs transposed, logits^T = W_e H^T: vocabulary entries on
+  // the TMEM lanes and tokens on the columns, so the epilogue stores each
+  // token's logits row segment straight from registers; the tile index runs
+  // over token blocks first, so each block of W_e is streamed from HBM once.
+  int kind = kind_in, M = M_in, N = N_in;
+  const void* A = A_in;
+  const void* W = W_in;
+  const bool transposed = kind_in == kEpiLogits;
+  if (transposed) {
+    kind = kEpiLogitsT;
+    std::swap(A, W);
+    std::swap(M, N);
+  }
   // CTA pairs (256-row tiles on two SMs, each holding half of B) where the
   // mainloop is long enough to gain from halving each SM's operand traffic;
   // measured on GB300: faster from K = 1600 up, no gain at K = 768.
   const int cg = (M > kBM && K >= 1024 && env.num_sms >= 2) ? 2 : 1;
   void* fn = kernel_for(kind, cg);
   if (!fn) return GPT2_ERR_INVALID_ARG;
-  if (M <= 0 || N <= 0 || K <= 0) return GPT2_ERR_INVALID_ARG;
-  if (K % 8 != 0) return GPT2_ERR_UNSUPPORTED;
-  if (kind != kEpiLogits && (N % 2 != 0)) return GPT2_ERR_UNSUPPORTED;
-  if (kind == kEpiQkv && (ep.d % 64 != 0 || N != 3 * ep.d)) return GPT2_ERR_UNSUPPORTED;
 
   const int units = cg == 2 ? env.num_sms / 2 : env.num_sms;
   const int BN = choose_bn(M, N, kBM * cg, units);
@@ -802,7 +847,9 @@ int launch_gemm_tc(const LaunchEnv& env, int kind, const void* A, const void* W,
   args.BN = BN;
   args.stages = stages;
   args.num_m_blocks = (M + kBM * cg - 1) / (kBM * cg);
-  args.num_tiles = args.num_m_blocks * ((N + BN - 1) / BN);
+  args.num_n_blocks = (N + BN - 1) / BN;
+  args.n_inner = transposed ? 1 : 0;
+  args.num_tiles = args.num_m_blocks * args.num_n_blocks;
   args.vec_ok = (kind == kEpiResidF32 || kind == kEpiResidBf16In) ? (ep.ldo % 4 == 0)
                                                                   : (ep.ldo % 8 == 0);
   args.tma_out = 0;
@@ -861,11 +908,11 @@ int launch_gemm_tc(const LaunchEnv& env, int kind, const void* A, const void* W,
   cfg.numAttrs = 2;
   if (cudaLaunchKernelExC(&cfg, fn, params) != cudaSuccess) return GPT2_ERR_CUDA;
 
-  if (flops) *flops = 2.0 * M * N * static_cast<double>(K);
+  if (flops) *flops = 2.0 * M_in * N_in * static_cast<double>(K);
   if (bytes) {
-    double b = 2.0 * (static_cast<double>(M) * K + static_cast<double>(N) * K);
-    const double mn = static_cast<double>(M) * N;
-    switch (kind) {
+    double b = 2.0 * (static_cast<double>(M_in) * K + static_cast<double>(N_in) * K);
+    const double mn = static_cast<double>(M_in) * N_in;
+    switch (kind_in) {
       case kEpiBias: case kEpiGelu: case kEpiQkv: b += 2.0 * mn + 2.0 * N; break;
       case kEpiResidF32: b += 8.0 * mn + 2.0 * N; break;
       case kEpiResidBf16In: b += 6.0 * mn + 2.0 * N; break;

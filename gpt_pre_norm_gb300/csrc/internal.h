@@ -41,6 +41,7 @@ enum EpiKind : int {
   kEpiResidBf16Out,   // out_bf16 = resid_f32 + acc + bias
   kEpiLogits,         // out_f32  = acc (no bias, N tail masked)
   kEpiQkv,            // acc + bias scattered to Q [B,h,T,64] and the K/V cache
+  kEpiLogitsT,        // (internal) kEpiLogits computed as W A^T: TMEM lanes = vocabulary
   kEpiCount
 };
 
