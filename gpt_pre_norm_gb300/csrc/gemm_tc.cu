@@ -819,9 +819,11 @@ int launch_gemm_tc(const LaunchEnv& env, int kind_in, const void* A_in, const vo
     std::swap(M, N);
   }
   // CTA pairs (256-row tiles on two SMs, each holding half of B) where the
-  // mainloop is long enough to gain from halving each SM's operand traffic;
-  // measured on GB300: faster from K = 1600 up, no gain at K = 768.
-  const int cg = (M > kBM && K >= 1024 && env.num_sms >= 2) ? 2 : 1;
+  // mainloop is long enough to gain from halving each SM's operand traffic
+  // (measured on GB300: faster from K = 1600 up, no gain at K = 768), and for
+  // the transposed head, whose 256-entry vocabulary tiles give each token row
+  // 1 KB of contiguous logits per tile (GPT-2-small head 564 -> 542 us).
+  const int cg = (M > kBM && (K >= 1024 || kind == kEpiLogitsT) && env.num_sms >= 2) ? 2 : 1;
   void* fn = kernel_for(kind, cg);
   if (!fn) return GPT2_ERR_INVALID_ARG;
 
