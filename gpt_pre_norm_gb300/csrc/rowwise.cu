@@ -110,8 +110,8 @@ __device__ __forceinline__ void convert_part(const ConvJob& job, int b) {
   }
 }
 
-// Row held in registers: NP pairs per lane, d <= 64 * NP, d even.  TX input,
-// TP gain/bias, TY output.
+// Row held in registers: NP pairs per lane, d <= 64 * NP, d even (the form
+// used where the 16-byte one does not apply).  TX input, TP gain/bias, TY output.
 template <typename TX, typename TP, typename TY, int NP>
 __global__ void __launch_bounds__(kRowThreads)
     layer_norm_reg(const TX* __restrict__ x, const TP* __restrict__ g, const TP* __restrict__ b,
@@ -165,6 +165,96 @@ __global__ void __launch_bounds__(kRowThreads)
   }
 }
 
+// Eight consecutive row values <-> registers with 16-byte accesses.
+__device__ __forceinline__ void load8(const float* p, float* v) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], c = reinterpret_cast<const float4*>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+}
+__device__ __forceinline__ void load8(const bf16* p, float* v) {
+  const uint4 w = *reinterpret_cast<const uint4*>(p);
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = bf16_lo(u[i]);
+    v[2 * i + 1] = bf16_hi(u[i]);
+  }
+}
+__device__ __forceinline__ void store8(float* p, const float* v) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+__device__ __forceinline__ void store8(bf16* p, const float* v) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                            pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+}
+__device__ __forceinline__ void store8(__half* p, const float* v) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]),
+                                            pack_f16x2(v[4], v[5]), pack_f16x2(v[6], v[7]));
+}
+
+// Row held in registers as NC groups of eight values per lane (group
+// lane + 32 i covers elements 8 (lane + 32 i) .. +7): 16-byte loads and
+// stores, d % 8 == 0, d <= 256 NC; mean and variance in two passes over the
+// registers.
+template <typename TX, typename TP, typename TY, int NC>
+__global__ void __launch_bounds__(kRowThreads, NC <= 3 ? 6 : (NC <= 4 ? 5 : 3))
+    layer_norm_vec(const TX* __restrict__ x, const TP* __restrict__ g, const TP* __restrict__ b,
+                   int rows, int d, TY* __restrict__ y, const __grid_constant__ ConvJob side) {
+  pdl_trigger();
+  pdl_wait();
+  const int conv_blocks = side.first[side.count];
+  if (static_cast<int>(blockIdx.x) < conv_blocks) {
+    convert_part(side, blockIdx.x);
+    return;
+  }
+  const int row = (blockIdx.x - conv_blocks) * kRowsPerBlock + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const int ng = d >> 3;
+  const TX* xr = x + static_cast<size_t>(row) * d;
+  float v[8 * NC];
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < NC; ++i) {
+    const int gi = lane + 32 * i;
+    if (gi < ng) {
+      load8(xr + 8 * gi, v + 8 * i);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[8 * i + e] = 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sum += v[8 * i + e];
+  }
+  const float inv_d = 1.0f / static_cast<float>(d);
+  const float u = warp_sum(sum) * inv_d;
+  float sq = 0.f;
+#pragma unroll
+  for (int i = 0; i < NC; ++i) {
+    if (lane + 32 * i < ng) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float a = v[8 * i + e] - u;
+        sq = fmaf(a, a, sq);
+      }
+    }
+  }
+  const float rstd = rsqrtf(warp_sum(sq) * inv_d + kLnEps);
+  TY* yr = y + static_cast<size_t>(row) * d;
+#pragma unroll
+  for (int i = 0; i < NC; ++i) {
+    const int gi = lane + 32 * i;
+    if (gi < ng) {
+      float gg[8], bb[8], o[8];
+      load8(g + 8 * gi, gg);
+      load8(b + 8 * gi, bb);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = (v[8 * i + e] - u) * rstd * gg[e] + bb[e];
+      store8(yr + 8 * gi, o);
+    }
+  }
+}
+
 __device__ __forceinline__ float ld1(const float* p) { return *p; }
 __device__ __forceinline__ float ld1(const bf16* p) { return __bfloat162float(*p); }
 __device__ __forceinline__ void st1(float* p, float v) { *p = v; }
@@ -200,6 +290,10 @@ __global__ void __launch_bounds__(kRowThreads)
   for (int c = lane; c < d; c += 32) st1(yr + c, (ld1(xr + c) - u) * rstd * ld1(g + c) + ld1(b + c));
 }
 
+__host__ __device__ inline bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15) == 0;
+}
+
 // The conversion blocks come first in the grid, so they start in the first
 // wave; the LayerNorm rows follow.
 template <typename TX, typename TP, typename TY>
@@ -209,7 +303,16 @@ int ln_dispatch(const TX* x, const TP* g, const TP* b, int rows, int d, TY* y, c
                           static_cast<unsigned>(side.first[side.count]);
   const dim3 grid(blocks), block(kRowThreads);
   cudaError_t e;
-  if (d % 2 == 0 && d <= 64 * 4) {
+  const bool vec = d % 8 == 0 && aligned16(x) && aligned16(g) && aligned16(b) && aligned16(y);
+  if (vec && d <= 256 * 1) {
+    e = launch_pdl(layer_norm_vec<TX, TP, TY, 1>, grid, block, 0, s, x, g, b, rows, d, y, side);
+  } else if (vec && d <= 256 * 3) {
+    e = launch_pdl(layer_norm_vec<TX, TP, TY, 3>, grid, block, 0, s, x, g, b, rows, d, y, side);
+  } else if (vec && d <= 256 * 4) {
+    e = launch_pdl(layer_norm_vec<TX, TP, TY, 4>, grid, block, 0, s, x, g, b, rows, d, y, side);
+  } else if (vec && d <= 256 * 7) {
+    e = launch_pdl(layer_norm_vec<TX, TP, TY, 7>, grid, block, 0, s, x, g, b, rows, d, y, side);
+  } else if (d % 2 == 0 && d <= 64 * 4) {
     e = launch_pdl(layer_norm_reg<TX, TP, TY, 4>, grid, block, 0, s, x, g, b, rows, d, y, side);
   } else if (d % 2 == 0 && d <= 64 * 12) {
     e = launch_pdl(layer_norm_reg<TX, TP, TY, 12>, grid, block, 0, s, x, g, b, rows, d, y, side);
