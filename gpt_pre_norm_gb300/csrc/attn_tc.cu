@@ -56,7 +56,7 @@ constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0;                   // two score buffers of 64 columns
 constexpr uint32_t kColO = 128;                 // two partial-output buffers of 64
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kBars = 1 + 2 * kSK + 2 * kSV + 5 * 2 + 1;
+constexpr int kBars = 1 + 2 * kSK + 2 * kSV + 3 * 2 + 1;
 constexpr size_t kSmemBytes =
     1024 + kQBytes + (kSK + kSV) * kKVBytes + 2 * kPBytes + kBars * 8 + 16;
 
@@ -82,12 +82,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint64_t* k_empty = k_full + kSK;            // [kSK] its scores computed
   uint64_t* v_full = k_empty + kSK;            // [kSV] V landed
   uint64_t* v_empty = v_full + kSV;            // [kSV] its P V product done
+  // A softmax warp reads S_j, publishes P_j, then folds O_{j-1}: so P_j
+  // published by all four warps also means that S_j's buffer (next used by
+  // S_{j+2}) and O_{j-2}'s (next used by P_j V_j) have been read, and no
+  // separate "free" barriers are needed.
   uint64_t* s_full = v_empty + kSV;            // [2] scores ready
-  uint64_t* s_free = s_full + 2;               // [2] scores read (4 warps)
-  uint64_t* p_full = s_free + 2;               // [2] P written (4 warps)
+  uint64_t* p_full = s_full + 2;               // [2] P written (4 warps)
   uint64_t* pv_done = p_full + 2;              // [2] P V product done (P read, O ready)
-  uint64_t* o_free = pv_done + 2;              // [2] partial output read (4 warps)
-  uint64_t* mma_done = o_free + 2;             // [1]
+  uint64_t* mma_done = pv_done + 2;            // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -111,10 +113,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 4);
       mbar_init(&p_full[i], 4);
       mbar_init(&pv_done[i], 1);
-      mbar_init(&o_free[i], 4);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -193,10 +193,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     bool ok = mbar_wait_bounded(q_full, 0, abort_flag, a.err);
     auto issue_s = [&](int j) -> bool {
       const int s = j % kSK, sb = j & 1;
+      // S_{j-2}, the buffer's previous tile, was read before P_{j-2} was
+      // published, which this thread has already waited for.
       if (!mbar_wait_bounded(&k_full[s], static_cast<uint32_t>(j / kSK) & 1u, abort_flag, a.err))
-        return false;
-      if (j >= 2 &&
-          !mbar_wait_bounded(&s_free[sb], static_cast<uint32_t>((j >> 1) - 1) & 1u, abort_flag, a.err))
         return false;
       tc_fence_after();
       const uint64_t k_desc = sdesc_k_sw128(smem_u32(sK + s * kKVBytes));
@@ -212,10 +211,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int j = 0; ok && j < n_kt; ++j) {
       if (j + 1 < n_kt && !(ok = issue_s(j + 1))) break;
       const int pb = j & 1, s = j % kSV;
+      // P_j published: O_{j-2}, this product's buffer, has been read too.
       if (!mbar_wait_bounded(&v_full[s], static_cast<uint32_t>(j / kSV) & 1u, abort_flag, a.err) ||
-          !mbar_wait_bounded(&p_full[pb], static_cast<uint32_t>(j >> 1) & 1u, abort_flag, a.err) ||
-          (j >= 2 && !mbar_wait_bounded(&o_free[pb], static_cast<uint32_t>((j >> 1) - 1) & 1u,
-                                        abort_flag, a.err))) {
+          !mbar_wait_bounded(&p_full[pb], static_cast<uint32_t>(j >> 1) & 1u, abort_flag, a.err)) {
         ok = false;
         break;
       }
@@ -255,9 +253,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       tmem_ld_32x32b_x32(trow + kColO + ob * 64, *reinterpret_cast<uint32_t(*)[32]>(ov));
       tmem_ld_32x32b_x32(trow + kColO + ob * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(ov + 32));
       tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&o_free[ob]);
       const float f = ex2(m_o - m_t);             // 0 on the first fold (m_o = -inf)
 #pragma unroll
       for (int c = 0; c < kD; ++c) o[c] = fmaf(o[c], f, __uint_as_float(ov[c]));
@@ -276,35 +271,30 @@ __global__ void __launch_bounds__(kThreads, 2)
       tmem_ld_32x32b_x32(trow + kColS + sb * 64, *reinterpret_cast<uint32_t(*)[32]>(sr));
       tmem_ld_32x32b_x32(trow + kColS + sb * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
       tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[sb]);
 
+      // Raw scores; the 1/sqrt(64) scale (in log2 units) is applied to the
+      // row maximum and inside the exponent's fused multiply-add.
       const int key0 = j * kKT;
       float mx = -INFINITY;
       if (key0 + kKT - 1 > pos) {                 // this step crosses the row's diagonal
 #pragma unroll
         for (int c = 0; c < kKT; ++c) {
-          const float x = key0 + c <= pos ? __uint_as_float(sr[c]) * sl2 : -INFINITY;
+          const float x = key0 + c <= pos ? __uint_as_float(sr[c]) : -INFINITY;
           sr[c] = __float_as_uint(x);
           mx = fmaxf(mx, x);
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < kKT; ++c) {
-          const float x = __uint_as_float(sr[c]) * sl2;
-          sr[c] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
-        }
+        for (int c = 0; c < kKT; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
       }
-      const float m_new = fmaxf(m, mx);
+      const float m_new = fmaxf(m, mx * sl2);
       const float m_use = m_new == -INFINITY ? 0.f : m_new;  // a row with no key yet
       float lj = 0.f;
       uint32_t pk[kKT / 2];
 #pragma unroll
       for (int c = 0; c < kKT / 2; ++c) {
-        const float p0 = ex2(__uint_as_float(sr[2 * c]) - m_use);
-        const float p1 = ex2(__uint_as_float(sr[2 * c + 1]) - m_use);
+        const float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), sl2, -m_use));
+        const float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -m_use));
         lj += p0 + p1;
         pk[c] = pack_bf16x2(p0, p1);
       }
@@ -317,6 +307,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       fence_proxy_async_smem();
+      tc_fence_before();  // this warp's TMEM reads (S_j, and O_{j-2} last step) come first
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[sb]);
 
