@@ -120,6 +120,18 @@ def ncu_traffic(kind: str, workload: str):
     return None
 
 
+def e2e_roofline(prof, peaks, steps, ms_step):
+    """Sum over the step's kernels of each one's roofline time, max(algorithmic
+    flops / tensor peak, algorithmic bytes / HBM peak), against the measured
+    step time: the end-to-end fraction of the rooflines."""
+    t_roof = 0.0
+    for rec in prof.values():
+        t_roof += max(rec["flops"] / (peaks["bf16_tflops"] * 1e12),
+                      rec["bytes"] / (peaks["hbm_gbs"] * 1e9))
+    t_roof = t_roof / steps * 1e3  # ms per step
+    return {"sum_t_roof_ms": t_roof, "measured_ms": ms_step, "frac": t_roof / ms_step}
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -516,6 +528,7 @@ def main():
         "tflops": flops * ws / (ms / 1e3) / 1e12,
         "tflops_frac_of_bf16_peak": flops * ws / (ms / 1e3) / 1e12 / peaks["bf16_tflops"],
         "roofline": roof,
+        "e2e_roofline": e2e_roofline(prof, peaks, args.steps, ms),
         "e2e": {"value": job_throughput(r.tokens, ws, ms_e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

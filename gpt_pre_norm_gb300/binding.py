@@ -83,6 +83,9 @@ def _load() -> C.CDLL:
         "gpt2_embed": (I, [P, P, P, P, I, I, I, P, P]),
         "gpt2_attention_decode_noalloc": (I, [P, P, I, I, I, I, I, I, P, P]),
         "gpt2_ctx_cache_weights": (I, [P, I]),
+        "gpt2_selftest_wait_timeout": (I, [P, I, P]),
+        "gpt2_generate_greedy": (I, [P, P, I, I, C.POINTER(gpt2_params), I, C.POINTER(gpt2_kv), I,
+                                     P, P, P]),
         "gpt2_profile_enable": (I, [P, I]),
         "gpt2_profile_kinds": (I, []),
         "gpt2_profile_read": (I, [P, I, C.POINTER(C.c_char_p), C.POINTER(LL), C.POINTER(D),
@@ -234,6 +237,23 @@ def gpt2_forward(ctx: Context, ids: torch.Tensor, params: ModelParams, B: int, T
     return logits
 
 
+def gpt2_generate_greedy(ctx: Context, ids: torch.Tensor, params: ModelParams, n_new: int,
+                         cache: KV, logits: torch.Tensor | None = None,
+                         stream=None) -> torch.Tensor:
+    """Greedy continuation of the prompt ids [B, T] by n_new tokens (int32
+    [B, n_new]); the prompt and the generated tokens go into `cache`."""
+    B, T = ids.shape
+    if logits is None:
+        logits = torch.empty((B, T, ctx.hp.n_vocab), dtype=torch.float32, device=ids.device)
+    out = torch.empty((B, n_new), dtype=torch.int32, device=ids.device)
+    cs = cache.struct()
+    _check(LIB.gpt2_generate_greedy(ctx.handle, _ptr(ids), B, T, C.byref(params.struct),
+                                    params.n_layer, C.byref(cs), n_new, _ptr(logits), _ptr(out),
+                                    _stream(stream)), "gpt2_generate_greedy")
+    cache.T_len = cs.T_len
+    return out
+
+
 def gpt2_layer_norm(mode: int, x: torch.Tensor, g: torch.Tensor, b: torch.Tensor,
                     y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     d = x.shape[-1]
@@ -291,6 +311,13 @@ def gpt2_embed(ctx: Context, ids: torch.Tensor, wte: torch.Tensor, wpe: torch.Te
     _check(LIB.gpt2_embed(ctx.handle, _ptr(ids), _ptr(wte), _ptr(wpe), B, T, T_past, _ptr(H),
                           _stream(stream)), "gpt2_embed")
     return H
+
+
+def gpt2_selftest_wait_timeout(ctx: Context, limit_us: int, stream=None) -> None:
+    """Launches a wait that runs out after limit_us (see the header); the next
+    gpt2_sync_status reports GPT2_ERR_DEVICE_TIMEOUT."""
+    _check(LIB.gpt2_selftest_wait_timeout(ctx.handle, limit_us, _stream(stream)),
+           "gpt2_selftest_wait_timeout")
 
 
 def gpt2_profile_enable(ctx: Context, enable: bool) -> None:

@@ -92,17 +92,18 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase of parity `parity` to complete.  Gives up (returns
-// false) when *abort becomes non-zero or after kWaitLimitNs; on a timeout it
-// sets *abort and the kErrTimeout bit of the error word.
+// false) when *abort becomes non-zero or after limit_ns (default kWaitLimitNs);
+// on a timeout it sets *abort and the kErrTimeout bit of the error word.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  volatile int* abort, unsigned* err) {
+                                                  volatile int* abort, unsigned* err,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0u) {
       if (abort && *abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         if (abort) *abort = 1;
         raise_error(err, kErrTimeout);
         return false;

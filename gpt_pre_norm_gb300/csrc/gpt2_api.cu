@@ -27,7 +27,8 @@ namespace {
 const char* kKindNames[kKindCount] = {
     "embed",          "layer_norm",        "gemm_c_attn",    "attention_prefill",
     "gemm_c_proj",    "gemm_c_fc",         "gemm_mlp_c_proj", "gemm_lm_head",
-    "gemm_other",     "attention_decode",  "attention_decode_combine", "simt_fp32"};
+    "gemm_other",     "attention_decode",  "attention_decode_combine", "simt_fp32",
+    "argmax"};
 
 struct ProfRec {
   int kind;
@@ -38,7 +39,7 @@ struct ProfRec {
 
 // Offsets (bytes) of the workspace regions.
 struct WsPlan {
-  size_t err, ln, q, kv, attn, resid, fc, partials, wconv, total;
+  size_t err, ln, q, kv, attn, resid, fc, partials, wconv, ids, total;
 };
 
 // fp16 working copies of the weights (bf16 mode): per layer slot, c_attn
@@ -72,6 +73,7 @@ WsPlan plan_workspace(const gpt2_hparams& hp, int max_B, int max_T) {
   p.wconv = take(hp.dtype == GPT2_BF16 ? 2 * (hp.n_layer * layer_slot_elems(hp) +
                                               static_cast<size_t>(hp.n_vocab) * hp.n_embd)
                                        : 0);
+  p.ids = take(static_cast<size_t>(max_B) * 4);  // greedy generation: the next token ids
   p.total = off;
   return p;
 }
@@ -431,6 +433,22 @@ EncodeTiledFn get_encode() {
 
 }  // namespace
 
+namespace gpt2 {
+namespace {
+// One thread waits on an mbarrier nothing completes, with the kernels' bounded
+// wait and a short limit: the wait runs out and raises the timeout bit.
+__global__ void wait_timeout_kernel(unsigned* err, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_bounded(&bar, 0, nullptr, err, limit_ns);
+}
+}  // namespace
+}  // namespace gpt2
+
 extern "C" {
 
 const char* gpt2_status_string(int status) {
@@ -510,6 +528,13 @@ void gpt2_ctx_destroy(gpt2_ctx* c) {
   }
   for (auto e : c->free_events) cudaEventDestroy(e);
   delete c;
+}
+
+int gpt2_selftest_wait_timeout(gpt2_ctx* c, int limit_us, void* stream) {
+  if (!c || limit_us < 1 || limit_us > 1000000) return GPT2_ERR_INVALID_ARG;
+  gpt2::wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      c->env.err, static_cast<unsigned long long>(limit_us) * 1000ull);
+  return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
 int gpt2_sync_status(gpt2_ctx* c, void* stream) {
@@ -641,6 +666,40 @@ int gpt2_forward(gpt2_ctx* c, const int32_t* ids, int B, int T, const gpt2_param
   });
   if (st) return st;
   if (present) present->T_len = t_past + T;
+  return GPT2_OK;
+}
+
+int gpt2_generate_greedy(gpt2_ctx* c, const int32_t* ids, int B, int T_prompt,
+                         const gpt2_params* params, int L, gpt2_kv* cache, int n_new, float* logits,
+                         int32_t* out_ids, void* stream) {
+  if (!c || !ids || !params || !cache || !logits || !out_ids || n_new <= 0)
+    return GPT2_ERR_INVALID_ARG;
+  if (T_prompt <= 0) return GPT2_ERR_INVALID_ARG;
+  if (!aligned16(out_ids)) return GPT2_ERR_ALIGNMENT;
+  const int t0 = cache->T_len;
+  // The last generated token is not run through the model.
+  const long long t_end = static_cast<long long>(t0) + T_prompt + n_new - 1;
+  if (t_end > c->hp.n_ctx || t_end > cache->T_cap) return GPT2_ERR_CTX_OVERFLOW;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int V = c->hp.n_vocab;
+  int32_t* next = c->at<int32_t>(c->plan.ids);
+  // The prompt (after any cached prefix), then the argmax of its last position.
+  int st = gpt2_forward(c, ids, B, T_prompt, params, L, t0 > 0 ? cache : nullptr, cache, logits,
+                        stream);
+  if (st) return st;
+  for (int i = 0; i < n_new; ++i) {
+    const int T = i == 0 ? T_prompt : 1;
+    st = c->run(kKindArgmax, s, [&](double* fl, double* by) {
+      *fl = 0;
+      *by = 4.0 * B * V;
+      return launch_argmax_rows(logits + static_cast<size_t>(T - 1) * V, B, V,
+                                static_cast<long long>(T) * V, out_ids + i, n_new, next, s);
+    });
+    if (st) return st;
+    if (i + 1 < n_new &&
+        (st = gpt2_forward(c, next, B, 1, params, L, cache, cache, logits, stream)))
+      return st;
+  }
   return GPT2_OK;
 }
 

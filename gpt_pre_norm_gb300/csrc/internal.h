@@ -29,6 +29,7 @@ enum KernelKind : int {
   kKindDecodeAttention,
   kKindDecodeCombine,
   kKindSimtFp32,
+  kKindArgmax,
   kKindCount
 };
 
@@ -116,6 +117,11 @@ int launch_layer_norm(int mode, const void* x, int x_dtype, const void* g, const
                       int d, void* y, cudaStream_t stream, bool y_f16 = false,
                       const ConvSegs* side = nullptr);
 
+
+// out[r * out_stride] = next[r] = argmax over the V values of row r (rows
+// row_stride apart); the lowest index among equal maxima.
+int launch_argmax_rows(const float* x, int rows, int V, long long row_stride, int32_t* out,
+                       long long out_stride, int32_t* next, cudaStream_t stream);
 
 // H[b,t,:] = wte[ids[b,t]] + wpe[t_past + t] -> fp32.
 int launch_embed(int mode, const int32_t* ids, const void* wte, const void* wpe, int B, int T,

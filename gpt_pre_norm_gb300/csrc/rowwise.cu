@@ -386,6 +386,53 @@ __global__ void __launch_bounds__(kRowThreads)
   for (int c = lane; c < d; c += 32) h[c] = e[c] + p[c];
 }
 
+// Index of the largest value of each row (the lowest index among equal
+// values; NaN never wins).  One block per row.
+__global__ void __launch_bounds__(kRowThreads)
+    argmax_rows(const float* __restrict__ x, int V, long long row_stride, int32_t* __restrict__ out,
+                long long out_stride, int32_t* __restrict__ next) {
+  pdl_trigger();
+  pdl_wait();
+  const float* r = x + blockIdx.x * row_stride;
+  float best = -INFINITY;
+  int idx = V;  // no value seen yet
+  for (int v = threadIdx.x; v < V; v += kRowThreads) {
+    const float f = r[v];
+    if (f > best || (idx == V && !(f != f))) {
+      best = f;
+      idx = v;
+    }
+  }
+  // Reduce (value, index): larger value, then lower index.
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float ob = __shfl_xor_sync(0xffffffffu, best, off);
+    const int oi = __shfl_xor_sync(0xffffffffu, idx, off);
+    if (ob > best || (ob == best && oi < idx)) {
+      best = ob;
+      idx = oi;
+    }
+  }
+  __shared__ float sb[kRowsPerBlock];
+  __shared__ int si[kRowsPerBlock];
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    sb[w] = best;
+    si[w] = idx;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < kRowsPerBlock; ++i)
+      if (sb[i] > best || (sb[i] == best && si[i] < idx)) {
+        best = sb[i];
+        idx = si[i];
+      }
+    const int id = idx < V ? idx : 0;  // a row of NaN only: token 0
+    out[blockIdx.x * out_stride] = id;
+    next[blockIdx.x] = id;
+  }
+}
+
 }  // namespace
 
 int launch_layer_norm(int mode, const void* x, int x_dtype, const void* g, const void* b, int rows,
@@ -413,6 +460,14 @@ int launch_layer_norm(int mode, const void* x, int x_dtype, const void* g, const
     return ln_dispatch(static_cast<const float*>(x), static_cast<const float*>(g),
                        static_cast<const float*>(b), rows, d, static_cast<float*>(y), stream, job);
   return GPT2_ERR_INVALID_ARG;
+}
+
+int launch_argmax_rows(const float* x, int rows, int V, long long row_stride, int32_t* out,
+                       long long out_stride, int32_t* next, cudaStream_t stream) {
+  if (rows <= 0 || V <= 0) return GPT2_ERR_INVALID_ARG;
+  const cudaError_t e = launch_pdl(argmax_rows, dim3(rows), dim3(kRowThreads), 0, stream, x, V,
+                                   row_stride, out, out_stride, next);
+  return e == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
 int launch_embed(int mode, const int32_t* ids, const void* wte, const void* wpe, int B, int T,

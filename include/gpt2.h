@@ -178,6 +178,24 @@ int gpt2_block_forward(gpt2_ctx *ctx, const void *x, const gpt2_block_params *pa
 int gpt2_forward(gpt2_ctx *ctx, const int32_t *ids, int B, int T, const gpt2_params *params, int L,
                  const gpt2_kv *past, gpt2_kv *present, float *logits, void *stream);
 
+/* Greedy generation: the model's consumer ("GPT-2 Full Forward Pass": the
+ * logits of the last position give the next token; greedy takes their
+ * argmax, the lowest index among equal maxima).  Runs the prompt ids [B,
+ * T_prompt] through gpt2_forward after the cache's T_len positions (with the
+ * cache as past when T_len > 0, and as present), then n_new times: the argmax
+ * of the last position's logits becomes out_ids[b, i] (device int32 [B,
+ * n_new]) and, except after the last one, one cached gpt2_forward step of
+ * that token.  All work is enqueued on `stream` with no host synchronisation
+ * (the chosen ids stay on the device), so the whole loop can be captured in
+ * a CUDA graph.  logits: device fp32 scratch of at least B * T_prompt *
+ * n_vocab values (holds the last step's logits on return).  cache->T_len
+ * becomes T_len + T_prompt + n_new - 1.
+ * Errors: as gpt2_forward; CTX_OVERFLOW when T_len + T_prompt + n_new - 1
+ * exceeds n_ctx or cache->T_cap.                                             */
+int gpt2_generate_greedy(gpt2_ctx *ctx, const int32_t *ids, int B, int T_prompt,
+                         const gpt2_params *params, int L, gpt2_kv *cache, int n_new,
+                         float *logits, int32_t *out_ids, void *stream);
+
 /* ------------------------------------------------- single operations ---- */
 /* The steps of the forward, exposed one by one so each kernel can be checked
  * and timed alone.  All pointers are device pointers.                      */
@@ -241,6 +259,18 @@ int gpt2_attention_decode_noalloc(const void *q, const void *kv, int B, int n_he
  * wte [n_vocab, d], wpe [n_ctx, d] in the mode dtype.                      */
 int gpt2_embed(gpt2_ctx *ctx, const int32_t *ids, const void *wte, const void *wpe, int B, int T,
                int T_past, float *H, void *stream);
+
+/* ----------------------------------------------------------- self-test ---- */
+
+/* Exercises the device-side failure path that every kernel of the library
+ * uses: one thread waits, with the kernels' own bounded wait but a limit of
+ * limit_us microseconds, on an mbarrier that nothing completes.  The wait
+ * runs out, sets the context's error word and the kernel returns; the next
+ * gpt2_sync_status reports GPT2_ERR_DEVICE_TIMEOUT (and clears the word) and
+ * the context stays usable.  Nothing faults, traps or hangs.  The pages have
+ * no counterpart: this is test support for the library.
+ * Errors: INVALID_ARG (null ctx, limit_us outside 1 .. 1000000), CUDA.      */
+int gpt2_selftest_wait_timeout(gpt2_ctx *ctx, int limit_us, void *stream);
 
 /* ---------------------------------------------------------- profiling ---- */
 

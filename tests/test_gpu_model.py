@@ -171,6 +171,57 @@ def test_decode_equals_uncached(G):
     assert argmax_agreement(got, ref) >= ARGMAX_AGREE
 
 
+def test_forward_chunked_prefill(G):
+    """Prefill 64 tokens into a cache, then a 66-token chunk after them (T > 1
+    with T_past > 0): the chunk's logits match the oracle's uncached pass at
+    positions 64..129, and the cache holds all 130 positions."""
+    w = _small_model(n_layer=2)
+    p = S.model_params(w, seed=8)
+    ids = S.token_ids(w, seed=8, T=130)
+    ctx = G.Context(w.n_vocab, w.n_ctx, w.d, w.n_head, w.n_layer, G.GPT2_BF16, w.B, 130)
+    mp = G.ModelParams(model_to_device(p))
+    ids_d = dev(ids, torch.int32)
+    cache = _kv(G, w.B, w.n_head, 160, w.d_h, torch.bfloat16, L=w.n_layer)
+    G.gpt2_forward(ctx, ids_d[:, :64].contiguous(), mp, w.B, 64, present=cache)
+    got = host(G.gpt2_forward(ctx, ids_d[:, 64:].contiguous(), mp, w.B, 66, past=cache,
+                              present=cache))
+    assert G.gpt2_sync_status(ctx) == 0
+    assert cache.T_len == 130
+    ref, ref_present = O.forward(ids, p, w.n_head)
+    assert_bf16_close(got, ref[:, 64:], what="chunked prefill logits")
+    assert argmax_agreement(got, ref[:, 64:]) >= ARGMAX_AGREE
+    assert_bf16_close(host(cache.data)[..., :130, :], ref_present, what="cache after the chunk")
+
+
+def test_generate_greedy(G):
+    """Greedy generation on the GPU, checked step by step against the oracle
+    fed the GPU's own choices: every chosen token is a maximum of the oracle's
+    logits within the bf16 path's error, and nearly all are the exact argmax."""
+    w = _small_model(n_layer=2, V=1000)
+    p = S.model_params(w, seed=9)
+    ids = S.token_ids(w, seed=9, T=24)
+    n_new = 8
+    ctx = G.Context(w.n_vocab, w.n_ctx, w.d, w.n_head, w.n_layer, G.GPT2_BF16, w.B, 24)
+    mp = G.ModelParams(model_to_device(p))
+    cache = _kv(G, w.B, w.n_head, 64, w.d_h, torch.bfloat16, L=w.n_layer)
+    out = G.gpt2_generate_greedy(ctx, dev(ids, torch.int32), mp, n_new, cache).cpu().numpy()
+    assert G.gpt2_sync_status(ctx) == 0
+    assert cache.T_len == 24 + n_new - 1
+    assert out.shape == (w.B, n_new) and out.min() >= 0 and out.max() < w.n_vocab
+    seq = ids.copy()
+    exact = 0
+    for i in range(n_new):
+        ref, _ = O.forward(seq, p, w.n_head, positions=[seq.shape[1] - 1])
+        ref = ref[:, -1]
+        for b in range(w.B):
+            row = ref[b]
+            tol = 5e-3 * np.sqrt(np.mean(row ** 2))
+            assert row[out[b, i]] >= row.max() - tol, f"step {i}, sequence {b}"
+            exact += int(out[b, i] == np.argmax(row))
+        seq = np.concatenate([seq, out[:, i:i + 1]], axis=1)
+    assert exact >= 0.9 * w.B * n_new
+
+
 # ----------------------------------------------------------- error paths ----
 def test_errors_are_reported_before_launch(G):
     w = S.WORKLOADS["block_bf16_d768"]

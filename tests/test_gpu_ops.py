@@ -220,3 +220,20 @@ def test_embed_rejects_bad_token_on_device(G):
     G.gpt2_embed(ctx, dev(ids, torch.int32), dev(emb["wte"]), dev(emb["wpe"]))
     assert G.gpt2_sync_status(ctx) == G.GPT2_ERR_INVALID_ARG
     assert G.gpt2_sync_status(ctx) == G.GPT2_OK  # the error word was cleared
+
+
+# --------------------------------------------------------- failure path ----
+def test_bounded_wait_reports_timeout_and_context_survives(G):
+    """A wait that nothing completes runs out (2 ms limit), the context reports
+    GPT2_ERR_DEVICE_TIMEOUT once, and its next products are still right."""
+    ctx = _ctx(G, G.GPT2_BF16)
+    G.gpt2_selftest_wait_timeout(ctx, 2000)
+    assert G.gpt2_sync_status(ctx) == G.GPT2_ERR_DEVICE_TIMEOUT
+    assert G.gpt2_sync_status(ctx) == G.GPT2_OK
+    rng = np.random.default_rng(21)
+    A = _rand(rng, (300, 768))
+    W = _rand(rng, (512, 768), 0.05)
+    bias = _rand(rng, (512,), 0.1)
+    out = G.gpt2_linear(ctx, G.GPT2_EPI_BIAS, dev(A), dev(W), dev(bias))
+    assert G.gpt2_sync_status(ctx) == G.GPT2_OK
+    assert_bf16_close(host(out), O.linear(A, W, bias), what="linear after a timeout")
