@@ -9,10 +9,14 @@
 // written with heads merged, [B, T, h * d_h].
 //
 //   (causal prefill on the tcgen05 tensor cores is in attn_tc.cu)
-//   attn_decode_bf16    one new token: split over keys, 8 warps per CTA, each
-//                       8-lane group streams one key per step with 16-byte
-//                       loads; partial (max, sum, o) merged in shared memory,
-//                       and across CTAs by attn_decode_combine.
+//   attn_decode_bf16    one new token: split over keys (when there are few
+//                       sequence x head pairs), one CTA per (pair, split); the
+//                       split's key and value rows, contiguous in the cache,
+//                       stream into a 3-stage shared-memory ring by 64-row bulk
+//                       copies; 8 warps, each 8-lane group scoring one key at
+//                       a time with online softmax; partial (max, sum, o)
+//                       merged across groups by shuffles, across warps in
+//                       shared memory, and across CTAs by attn_decode_combine.
 //   attn_fp32           fp32 storage, any d_h <= 256, one warp per query.
 #include <math.h>
 
@@ -32,31 +36,64 @@ constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kPartialStride = kDh + 2;  // o[64], m, l
 
+constexpr int kDecStageKeys = 64;                        // keys per stage
+constexpr int kDecStages = 3;                           // four CTAs of 50 KB fit on an SM
+constexpr uint32_t kDecRowBytes = kDh * 2;               // one key (or value) row: 128 B
+constexpr size_t kDecSmem = 2 * kDecStages * kDecStageKeys * kDecRowBytes + 64;
+
 __global__ void __launch_bounds__(kDecThreads)
     attn_decode_bf16(const bf16* __restrict__ q, const bf16* __restrict__ kv, long long s_batch,
                      long long s_kv, long long s_head, int h, int t_len, int chunk,
-                     uint16_t* __restrict__ out, float* __restrict__ partials, int out_f16) {
+                     uint16_t* __restrict__ out, float* __restrict__ partials, int out_f16,
+                     unsigned* err) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  uint8_t* sK = dsm;                                             // [stages][64 rows]
+  uint8_t* sV = dsm + kDecStages * kDecStageKeys * kDecRowBytes;  // [stages][64 rows]
+  uint64_t* full = reinterpret_cast<uint64_t*>(sV + kDecStages * kDecStageKeys * kDecRowBytes);
   __shared__ float s_m[kDecWarps], s_l[kDecWarps];
   __shared__ float s_o[kDecWarps][kDh];
-  pdl_trigger();
-  pdl_wait();
+  __shared__ int s_abort;
 
   const int split = blockIdx.x, splits = gridDim.x;
   const int bh = blockIdx.y;
   const int b = bh / h, head = bh - b * h;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grp = lane >> 3, sub = lane & 7;  // 4 groups of 8 lanes; 8 dims per lane
 
   const int k_begin = split * chunk;
   const int k_end = min(t_len, k_begin + chunk);
-  const int per_warp = (k_end - k_begin + kDecWarps - 1) / kDecWarps;
-  const int w_begin = k_begin + warp * per_warp;
-  const int w_end = min(k_end, w_begin + per_warp);
+  const int n_keys = max(0, k_end - k_begin);
+  const int ns = (n_keys + kDecStageKeys - 1) / kDecStageKeys;
 
-  const bf16* Kg = kv + b * s_batch + head * s_head;
+  if (tid == 0) {
+    for (int i = 0; i < kDecStages; ++i) mbar_init(&full[i], 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_trigger();
+  pdl_wait();
+
+  // The split's keys of this head are one contiguous run of 128-byte rows in
+  // the cache (K, and V s_kv further on): each stage is one bulk copy of up
+  // to 64 rows of each, issued by thread 0.
+  const bf16* Kg = kv + b * s_batch + head * s_head + static_cast<size_t>(k_begin) * kDh;
   const bf16* Vg = Kg + s_kv;
-  const float sl2 = 0.125f * kLog2e;
+  auto issue = [&](int j) {
+    const int slot = j % kDecStages;
+    const int nk = min(kDecStageKeys, n_keys - j * kDecStageKeys);
+    const uint32_t bytes = static_cast<uint32_t>(nk) * kDecRowBytes;
+    mbar_arrive_expect_tx(&full[slot], 2 * bytes);
+    bulk_load(sK + slot * kDecStageKeys * kDecRowBytes,
+              Kg + static_cast<size_t>(j) * kDecStageKeys * kDh, bytes, &full[slot]);
+    bulk_load(sV + slot * kDecStageKeys * kDecRowBytes,
+              Vg + static_cast<size_t>(j) * kDecStageKeys * kDh, bytes, &full[slot]);
+  };
+  int issued = 0;
+  if (tid == 0)
+    for (; issued < min(ns, kDecStages); ++issued) issue(issued);
 
+  const float sl2 = 0.125f * kLog2e;
   float qv[8];
   {
     const uint4 qq = *reinterpret_cast<const uint4*>(q + static_cast<size_t>(bh) * kDh + sub * 8);
@@ -71,43 +108,60 @@ __global__ void __launch_bounds__(kDecThreads)
 #pragma unroll
   for (int i = 0; i < 8; ++i) o[i] = 0.f;
 
-  constexpr int kUnroll = 4;  // keys per group per step
-  for (int k0 = w_begin; k0 < w_end; k0 += 4 * kUnroll) {
-    uint4 kr[kUnroll], vr[kUnroll];
-    bool ok[kUnroll];
+  // Stage j: warp w takes keys 8w .. 8w+7 of the stage, group g keys 8w+2g
+  // and 8w+2g+1, each key read by its 8 lanes (16 bytes each).
+  int j = 0;
+  for (; j < ns; ++j) {
+    const int slot = j % kDecStages;
+    const bool got = mbar_wait_bounded(&full[slot], static_cast<uint32_t>(j / kDecStages) & 1u,
+                                       &s_abort, err);
+    if (got) {
+      const int nk = min(kDecStageKeys, n_keys - j * kDecStageKeys);
+      const uint8_t* kb = sK + slot * kDecStageKeys * kDecRowBytes;
+      const uint8_t* vb = sV + slot * kDecStageKeys * kDecRowBytes;
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int key = k0 + u * 4 + grp;
-      ok[u] = key < w_end;
-      const size_t off = static_cast<size_t>(ok[u] ? key : w_begin) * kDh + sub * 8;
-      kr[u] = *reinterpret_cast<const uint4*>(Kg + off);
-      vr[u] = *reinterpret_cast<const uint4*>(Vg + off);
-    }
+      for (int u = 0; u < 2; ++u) {
+        const int key = warp * 8 + grp * 2 + u;
+        const bool ok = key < nk;
+        const int kr = ok ? key : 0;
+        const uint4 kw4 = *reinterpret_cast<const uint4*>(kb + kr * kDecRowBytes + sub * 16);
+        const uint32_t kw[4] = {kw4.x, kw4.y, kw4.z, kw4.w};
+        float sc = 0.f;
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const uint32_t kw[4] = {kr[u].x, kr[u].y, kr[u].z, kr[u].w};
-      float sc = 0.f;
+        for (int i = 0; i < 4; ++i) {
+          sc = fmaf(qv[2 * i], bf16_lo(kw[i]), sc);
+          sc = fmaf(qv[2 * i + 1], bf16_hi(kw[i]), sc);
+        }
+        sc += __shfl_xor_sync(0xffffffffu, sc, 1);
+        sc += __shfl_xor_sync(0xffffffffu, sc, 2);
+        sc += __shfl_xor_sync(0xffffffffu, sc, 4);
+        if (!ok) continue;
+        const float mn = fmaxf(m, sc);
+        const float alpha = ex2(m - mn);
+        const float p = ex2(sc - mn);
+        m = mn;
+        l = l * alpha + p;
+        const uint4 vw4 = *reinterpret_cast<const uint4*>(vb + kr * kDecRowBytes + sub * 16);
+        const uint32_t vw[4] = {vw4.x, vw4.y, vw4.z, vw4.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        sc = fmaf(qv[2 * i], bf16_lo(kw[i]), sc);
-        sc = fmaf(qv[2 * i + 1], bf16_hi(kw[i]), sc);
+        for (int i = 0; i < 4; ++i) {
+          o[2 * i] = fmaf(p, bf16_lo(vw[i]), o[2 * i] * alpha);
+          o[2 * i + 1] = fmaf(p, bf16_hi(vw[i]), o[2 * i + 1] * alpha);
+        }
       }
-      sc += __shfl_xor_sync(0xffffffffu, sc, 1);
-      sc += __shfl_xor_sync(0xffffffffu, sc, 2);
-      sc += __shfl_xor_sync(0xffffffffu, sc, 4);
-      if (!ok[u]) continue;
-      const float mn = fmaxf(m, sc);
-      const float alpha = ex2(m - mn);
-      const float p = ex2(sc - mn);
-      m = mn;
-      l = l * alpha + p;
-      const uint32_t vw[4] = {vr[u].x, vr[u].y, vr[u].z, vr[u].w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        o[2 * i] = fmaf(p, bf16_lo(vw[i]), o[2 * i] * alpha);
-        o[2 * i + 1] = fmaf(p, bf16_hi(vw[i]), o[2 * i + 1] * alpha);
-      }
     }
+    // Every thread agrees on going on; then the stage's slot is refilled.
+    if (!__syncthreads_and(got)) break;
+    if (tid == 0 && issued < ns) issue(issued++);
+  }
+  if (j < ns) {
+    // A wait ran out: the copies still in flight must land before the CTA
+    // exits; nothing is written.
+    if (tid == 0)
+      for (int k = j; k < issued; ++k)
+        mbar_wait_bounded(&full[k % kDecStages], static_cast<uint32_t>(k / kDecStages) & 1u,
+                          nullptr, err);
+    return;
   }
   // Merge the four key groups of the warp (lanes sub, sub+8, sub+16, sub+24).
 #pragma unroll
@@ -260,14 +314,21 @@ int decode_splits(int B, int h, int t_len, int num_sms) {
 int launch_decode_attention_bf16(const bf16* q, const bf16* kv, long long s_batch, long long s_kv,
                                  long long s_head, int B, int h, int t_len, void* out,
                                  float* partials, int splits, cudaStream_t stream,
-                                 int* launches, bool out_f16) {
+                                 int* launches, bool out_f16, unsigned* err) {
   if (B <= 0 || h <= 0 || t_len <= 0 || splits <= 0 || splits > 65535) return GPT2_ERR_INVALID_ARG;
   if (splits > 1 && partials == nullptr) return GPT2_ERR_INVALID_ARG;
   const int chunk = (t_len + splits - 1) / splits;
   dim3 grid(splits, B * h);
-  cudaError_t e = launch_pdl(attn_decode_bf16, grid, dim3(kDecThreads), 0, stream, q, kv, s_batch,
-                             s_kv, s_head, h, t_len, chunk, static_cast<uint16_t*>(out), partials,
-                             out_f16 ? 1 : 0);
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(attn_decode_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kDecSmem)) != cudaSuccess)
+      return GPT2_ERR_CUDA;
+    attr_set = true;
+  }
+  cudaError_t e = launch_pdl(attn_decode_bf16, grid, dim3(kDecThreads), kDecSmem, stream, q, kv,
+                             s_batch, s_kv, s_head, h, t_len, chunk, static_cast<uint16_t*>(out),
+                             partials, out_f16 ? 1 : 0, err);
   if (e != cudaSuccess) return GPT2_ERR_CUDA;
   int n = 1;
   if (splits > 1) {
