@@ -13,20 +13,26 @@
 //               step into separate rings (128-byte swizzle): a K stage is
 //               free again once its scores are computed, a V stage only
 //               after its P V product, so K runs further ahead.  One thread
-//               polls both rings and issues whichever copy is possible.
+//               polls both rings and issues whichever copy is possible.  The
+//               rings are as deep as two CTAs per SM allow (P lives in TMEM,
+//               not in shared memory): a copy takes microseconds when the
+//               memory system is busy, and the steps in flight must cover it.
 //   warp 1      allocates 256 TMEM columns; one thread issues
 //                 S_j = Q K_j^T  (M=128, N=64, K=64; K-major operands)
 //               into one of two TMEM score buffers, one step ahead, and
-//                 O_j = P_j V_j  (M=128, N=64, K=64; P from shared memory,
-//                                 V used as stored, [key][dim]: MN-major B)
-//               into one of two TMEM partial-output buffers.
+//                 O += P_j V_j  (M=128, N=64, K=64; P from TMEM,
+//                                V used as stored, [key][dim]: MN-major B)
+//               into one TMEM output accumulator.
 //   warps 2-5   one query row per thread: S_j from TMEM, causal mask on the
 //               steps that cross the diagonal, row maximum, P = 2^(s - m)
-//               in bf16 to shared memory (the next product's A operand),
-//               then the previous step's O from TMEM folded into the
-//               registers' running output with the usual rescale by
-//               2^(m_old - m_new) ("online softmax").  At the end o / l is
-//               written through shared memory by a TMA store.
+//               in bf16 to one of two TMEM buffers (the next product's A).
+//               The reference maximum m of the online softmax moves only
+//               when a row's maximum passes it by more than 2^8: P then
+//               stays below 256 (no overflow in bf16 or in the fp32 sums),
+//               and the rescale of O and l by 2^(m_old - m_new) is rare; when
+//               a warp needs one, it waits for the last product and rescales
+//               its rows of O in TMEM.  At the end o / l is written through
+//               shared memory by a TMA store.
 // Steps entirely above the diagonal are never loaded; the query tiles with
 // the most keys start first.  Every wait on an mbarrier is bounded: one that
 // runs out raises the error word, and the CTA drains its copies and MMAs,
@@ -46,19 +52,21 @@ namespace {
 constexpr int kD = 64;
 constexpr int kQT = 128;                        // queries per CTA
 constexpr int kKT = 64;                         // keys per step
-constexpr int kSK = 4;                          // K ring
-constexpr int kSV = 3;                          // V ring
+constexpr int kSK = 5;                          // K ring
+constexpr int kSV = 6;                          // V ring
 constexpr int kThreads = 192;
 constexpr uint32_t kQBytes = kQT * kD * 2;      // 16 KB
 constexpr uint32_t kKVBytes = kKT * kD * 2;     // 8 KB: one K or V tile
-constexpr uint32_t kPBytes = kQT * kKT * 2;     // 16 KB
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0;                   // two score buffers of 64 columns
-constexpr uint32_t kColO = 128;                 // two partial-output buffers of 64
+constexpr uint32_t kColS = 0;                   // two score buffers of 64 columns (fp32)
+constexpr uint32_t kColP = 128;                 // two P buffers of 32 columns (bf16 pairs)
+constexpr uint32_t kColO = 192;                 // the output accumulator, 64 columns
+constexpr float kRescaleLog2 = 8.f;             // max. lag of the reference maximum (log2)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kBars = 1 + 2 * kSK + 2 * kSV + 3 * 2 + 1;
 constexpr size_t kSmemBytes =
-    1024 + kQBytes + (kSK + kSV) * kKVBytes + 2 * kPBytes + kBars * 8 + 16;
+    1024 + kQBytes + (kSK + kSV) * kKVBytes + kBars * 8 + 16;
+static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
 
 struct AttnArgs {
   int T, t_past, h, n_qtiles;
@@ -76,19 +84,17 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint8_t* sQ = sm;
   uint8_t* sK = sQ + kQBytes;                  // [kSK][8 KB]
   uint8_t* sV = sK + kSK * kKVBytes;           // [kSV][8 KB]
-  uint8_t* sP = sV + kSV * kKVBytes;           // [2][16 KB]
-  uint64_t* q_full = reinterpret_cast<uint64_t*>(sP + 2 * kPBytes);
+  uint64_t* q_full = reinterpret_cast<uint64_t*>(sV + kSV * kKVBytes);
   uint64_t* k_full = q_full + 1;               // [kSK] K landed
   uint64_t* k_empty = k_full + kSK;            // [kSK] its scores computed
   uint64_t* v_full = k_empty + kSK;            // [kSV] V landed
   uint64_t* v_empty = v_full + kSV;            // [kSV] its P V product done
-  // A softmax warp reads S_j, publishes P_j, then folds O_{j-1}: so P_j
-  // published by all four warps also means that S_j's buffer (next used by
-  // S_{j+2}) and O_{j-2}'s (next used by P_j V_j) have been read, and no
-  // separate "free" barriers are needed.
+  // A softmax warp reads S_j before it publishes P_j, so P_j published by
+  // all four warps also means that S_j's buffer (next used by S_{j+2}) has
+  // been read, and that any rescale of O for step j is done.
   uint64_t* s_full = v_empty + kSV;            // [2] scores ready
-  uint64_t* p_full = s_full + 2;               // [2] P written (4 warps)
-  uint64_t* pv_done = p_full + 2;              // [2] P V product done (P read, O ready)
+  uint64_t* p_full = s_full + 2;               // [2] P written, O rescaled (4 warps)
+  uint64_t* pv_done = p_full + 2;              // [2] P_j V_j done (P_j's buffer read, O updated)
   uint64_t* mma_done = pv_done + 2;            // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -211,19 +217,18 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int j = 0; ok && j < n_kt; ++j) {
       if (j + 1 < n_kt && !(ok = issue_s(j + 1))) break;
       const int pb = j & 1, s = j % kSV;
-      // P_j published: O_{j-2}, this product's buffer, has been read too.
       if (!mbar_wait_bounded(&v_full[s], static_cast<uint32_t>(j / kSV) & 1u, abort_flag, a.err) ||
           !mbar_wait_bounded(&p_full[pb], static_cast<uint32_t>(j >> 1) & 1u, abort_flag, a.err)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint64_t p_desc = sdesc_k_sw128(smem_u32(sP + pb * kPBytes));
+      const uint32_t p_tmem = tmem + kColP + pb * 32;
       const uint64_t v_desc = sdesc_mn_sw128(smem_u32(sV + s * kKVBytes));
-      const uint32_t d = tmem + kColO + pb * 64;
+      const uint32_t d = tmem + kColO;
 #pragma unroll
-      for (int k = 0; k < kKT / 16; ++k)  // 16 keys: +32 B in P's rows, +2048 B in V's
-        umma_f16kind(d, p_desc + 2 * k, v_desc + 128 * k, id_pv, k != 0 ? 1u : 0u);
+      for (int k = 0; k < kKT / 16; ++k)  // 16 keys: +8 columns of P, +2048 B in V
+        umma_f16kind_ts(d, p_tmem + 8 * k, v_desc + 128 * k, id_pv, (j | k) != 0 ? 1u : 0u);
       umma_commit(&pv_done[pb]);
       umma_commit(&v_empty[s]);
     }
@@ -237,27 +242,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int pos = a.t_past + q0 + r;           // its absolute position
     const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = 0.125f * kLog2e;           // 1/sqrt(64), in log2 units
-    float o[kD];
-#pragma unroll
-    for (int c = 0; c < kD; ++c) o[c] = 0.f;
-    float m = -INFINITY, l = 0.f, m_o = -INFINITY;
+    float m = -INFINITY, l = 0.f;                // reference maximum (log2 units), row sum
     bool ok = true;
-
-    // O_t (relative to the maximum m_t its P used) into the running output.
-    auto fold = [&](int t, float m_t) -> bool {
-      const int ob = t & 1;
-      if (!mbar_wait_bounded(&pv_done[ob], static_cast<uint32_t>(t >> 1) & 1u, abort_flag, a.err))
-        return false;
-      tc_fence_after();
-      uint32_t ov[kD];
-      tmem_ld_32x32b_x32(trow + kColO + ob * 64, *reinterpret_cast<uint32_t(*)[32]>(ov));
-      tmem_ld_32x32b_x32(trow + kColO + ob * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(ov + 32));
-      tmem_ld_wait();
-      const float f = ex2(m_o - m_t);             // 0 on the first fold (m_o = -inf)
-#pragma unroll
-      for (int c = 0; c < kD; ++c) o[c] = fmaf(o[c], f, __uint_as_float(ov[c]));
-      m_o = m_t;
-      return true;
+    // The product P_t V_t has completed (pv_done of step t; never more than
+    // one phase behind when waited for).
+    auto wait_pv = [&](int t) -> bool {
+      return mbar_wait_bounded(&pv_done[t & 1], static_cast<uint32_t>(t >> 1) & 1u, abort_flag,
+                               a.err);
     };
 
     for (int j = 0; j < n_kt; ++j) {
@@ -287,8 +278,30 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int c = 0; c < kKT; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
       }
-      const float m_new = fmaxf(m, mx * sl2);
-      const float m_use = m_new == -INFINITY ? 0.f : m_new;  // a row with no key yet
+      // A new reference maximum only when this row's passed it by more than
+      // kRescaleLog2 (always on the row's first key); O and l scale by
+      // 2^(m_old - m_new) (0 while m_old = -inf).
+      const float m_row = mx * sl2;
+      const bool bump = m_row > m + kRescaleLog2;
+      const float alpha = bump ? ex2(m - m_row) : 1.f;
+      if (bump) m = m_row;
+      l *= alpha;
+      if (j > 0 && __any_sync(0xffffffffu, bump)) {
+        // O holds P_0 V_0 + .. + P_{j-1} V_{j-1}: wait for the last product,
+        // then rescale this warp's 32 rows in place (alpha = 1 elsewhere).
+        if (!(ok = wait_pv(j - 1))) break;
+        tc_fence_after();
+        uint32_t ov[kD];
+        tmem_ld_32x32b_x32(trow + kColO, *reinterpret_cast<uint32_t(*)[32]>(ov));
+        tmem_ld_32x32b_x32(trow + kColO + 32, *reinterpret_cast<uint32_t(*)[32]>(ov + 32));
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < kD; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+        tmem_st_32x32b_x32(trow + kColO, *reinterpret_cast<uint32_t(*)[32]>(ov));
+        tmem_st_32x32b_x32(trow + kColO + 32, *reinterpret_cast<uint32_t(*)[32]>(ov + 32));
+        tmem_st_wait();
+      }
+      const float m_use = m == -INFINITY ? 0.f : m;  // a row with no key yet
       float lj = 0.f;
       uint32_t pk[kKT / 2];
 #pragma unroll
@@ -298,29 +311,31 @@ __global__ void __launch_bounds__(kThreads, 2)
         lj += p0 + p1;
         pk[c] = pack_bf16x2(p0, p1);
       }
-      // P_j: row r of a [128 x 64] bf16 K-major tile, 16-byte chunk c at
-      // c ^ (r & 7) (the 128-byte swizzle).  Its buffer was last read by
-      // P_{j-2} V_{j-2}, which the fold of step j-1 has waited for.
-      uint8_t* prow = sP + sb * kPBytes + r * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      fence_proxy_async_smem();
-      tc_fence_before();  // this warp's TMEM reads (S_j, and O_{j-2} last step) come first
+      l += lj;
+      // P_j: this row's 64 keys as 32 bf16 pairs in TMEM lane r, in the
+      // buffer P_{j-2} V_{j-2} read last.
+      if (j >= 2 && !(ok = wait_pv(j - 2))) break;
+      tmem_st_32x32b_x32(trow + kColP + sb * 32, pk);
+      tmem_st_wait();
+      tc_fence_before();  // this warp's TMEM reads and writes come first
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[sb]);
-
-      if (j >= 1 && !(ok = fold(j - 1, m))) break;
-      l = fmaf(l, ex2(m - m_new), lj);            // l = 0 before the first step
-      m = m_new;
     }
-    if (ok) ok = fold(n_kt - 1, m);
+    float o[kD];
+    if (ok && (ok = wait_pv(n_kt - 1))) {
+      tc_fence_after();
+      uint32_t ov[kD];
+      tmem_ld_32x32b_x32(trow + kColO, *reinterpret_cast<uint32_t(*)[32]>(ov));
+      tmem_ld_32x32b_x32(trow + kColO + 32, *reinterpret_cast<uint32_t(*)[32]>(ov + 32));
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < kD; ++c) o[c] = __uint_as_float(ov[c]);
+    }
     if (ok) {
-      // o / l through shared memory (P buffer 0: every product is done) and
-      // one TMA store of this warp's 32 rows; rows past T are not written.
+      // o / l through shared memory (the Q tile's: every product is done)
+      // and one TMA store of this warp's 32 rows; rows past T are not written.
       const float inv = 1.0f / l;
-      uint8_t* orow = sP + r * 128;
+      uint8_t* orow = sQ + r * 128;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         uint32_t w[4];
@@ -332,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_store_3d(&tmO, sP + quarter * 32 * 128, head * kD, q0 + quarter * 32, b);
+        tma_store_3d(&tmO, sQ + quarter * 32 * 128, head * kD, q0 + quarter * 32, b);
         bulk_commit_group();
         bulk_wait_group<0>();
       }
