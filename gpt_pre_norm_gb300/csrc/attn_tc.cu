@@ -8,11 +8,14 @@
 // V are read from the KV cache ([.., T_cap, 64] rows per head) and the output
 // goes to [B, T, h * 64] with the heads merged.
 //
-// One CTA per (sequence x head, 128-query tile), 6 warps, two CTAs per SM:
-//   warp 0      TMA: the Q tile once, then the 64-key K and V tiles of each
-//               step into separate rings (128-byte swizzle): a K stage is
-//               free again once its scores are computed, a V stage only
-//               after its P V product, so K runs further ahead.  One thread
+// A persistent kernel: two resident CTAs per SM, each walking its share of
+// the (sequence x head, 128-query tile) work items, dealt out longest first
+// in rounds that alternate direction; every role runs on into the next tile, so one tile's Q and
+// first K/V tiles load while the previous tile finishes.  6 warps:
+//   warp 0      TMA: each tile's Q (two buffers), then the 64-key K and V
+//               tiles of each step into separate rings (128-byte swizzle):
+//               a K stage is free again once its scores are computed, a V
+//               stage only after its P V product, so K runs further ahead.  One thread
 //               polls both rings and issues whichever copy is possible.  The
 //               rings are as deep as two CTAs per SM allow (P lives in TMEM,
 //               not in shared memory): a copy takes microseconds when the
@@ -31,12 +34,11 @@
 //               stays below 256 (no overflow in bf16 or in the fp32 sums),
 //               and the rescale of O and l by 2^(m_old - m_new) is rare; when
 //               a warp needs one, it waits for the last product and rescales
-//               its rows of O in TMEM.  At the end o / l is written through
-//               shared memory by a TMA store.
-// Steps entirely above the diagonal are never loaded; the query tiles with
-// the most keys start first.  Every wait on an mbarrier is bounded: one that
-// runs out raises the error word, and the CTA drains its copies and MMAs,
-// frees TMEM and returns.
+//               its rows of O in TMEM.  At the tile's end each thread
+//               writes its row of o / l (128 contiguous bytes).
+// Steps entirely above the diagonal are never loaded.  Every wait on an
+// mbarrier is bounded: one that runs out raises the error word, and the CTA
+// drains its copies and MMAs, frees TMEM and returns.
 #include <math.h>
 #include <string.h>
 
@@ -52,8 +54,8 @@ namespace {
 constexpr int kD = 64;
 constexpr int kQT = 128;                        // queries per CTA
 constexpr int kKT = 64;                         // keys per step
-constexpr int kSK = 5;                          // K ring
-constexpr int kSV = 6;                          // V ring
+constexpr int kSK = 4;                          // K ring
+constexpr int kSV = 5;                          // V ring
 constexpr int kThreads = 192;
 constexpr uint32_t kQBytes = kQT * kD * 2;      // 16 KB
 constexpr uint32_t kKVBytes = kKT * kD * 2;     // 8 KB: one K or V tile
@@ -63,52 +65,78 @@ constexpr uint32_t kColP = 128;                 // two P buffers of 32 columns (
 constexpr uint32_t kColO = 192;                 // the output accumulator, 64 columns
 constexpr float kRescaleLog2 = 8.f;             // max. lag of the reference maximum (log2)
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kBars = 1 + 2 * kSK + 2 * kSV + 3 * 2 + 1;
+constexpr int kBars = 5 * 2 + 2 * kSK + 2 * kSV + 1;
 constexpr size_t kSmemBytes =
-    1024 + kQBytes + (kSK + kSV) * kKVBytes + kBars * 8 + 16;
+    1024 + 2 * kQBytes + (kSK + kSV) * kKVBytes + kBars * 8 + 16;
 static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
 
 struct AttnArgs {
-  int T, t_past, h, n_qtiles;
+  int T, t_past, h, n_qtiles, n_bh;
+  int n_work;   // n_bh * n_qtiles query tiles
   int out_f16;  // output fp16 (else bf16)
+  void* out;    // [B, T, h * 64]
   unsigned* err;
 };
 
+// Work item w: the query tiles with the most keys first, then sequence x head.
+struct Tile {
+  int bh, b, head, q0, n_kt;
+};
+__device__ __forceinline__ Tile tile_of(const AttnArgs& a, int w) {
+  Tile t;
+  const int qt = a.n_qtiles - 1 - w / a.n_bh;
+  t.bh = w - (w / a.n_bh) * a.n_bh;
+  t.b = t.bh / a.h;
+  t.head = t.bh - t.b * a.h;
+  t.q0 = qt * kQT;
+  const int q_last = min(t.q0 + kQT, a.T) - 1;
+  t.n_kt = (a.t_past + q_last + 1 + kKT - 1) / kKT;  // steps up to the last query
+  return t;
+}
+
 __global__ void __launch_bounds__(kThreads, 2)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                   const AttnArgs a) {
+                   const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = sm;
-  uint8_t* sK = sQ + kQBytes;                  // [kSK][8 KB]
+  uint8_t* sQ = sm;                            // [2][16 KB] by tile parity
+  uint8_t* sK = sQ + 2 * kQBytes;              // [kSK][8 KB]
   uint8_t* sV = sK + kSK * kKVBytes;           // [kSV][8 KB]
-  uint64_t* q_full = reinterpret_cast<uint64_t*>(sV + kSV * kKVBytes);
-  uint64_t* k_full = q_full + 1;               // [kSK] K landed
+  uint64_t* q_full = reinterpret_cast<uint64_t*>(sV + kSV * kKVBytes);  // [2]
+  uint64_t* q_empty = q_full + 2;              // [2] the tile's last S product done
+  uint64_t* k_full = q_empty + 2;              // [kSK] K landed
   uint64_t* k_empty = k_full + kSK;            // [kSK] its scores computed
   uint64_t* v_full = k_empty + kSK;            // [kSV] V landed
   uint64_t* v_empty = v_full + kSV;            // [kSV] its P V product done
-  // A softmax warp reads S_j before it publishes P_j, so P_j published by
-  // all four warps also means that S_j's buffer (next used by S_{j+2}) has
-  // been read, and that any rescale of O for step j is done.
+  // A softmax warp reads S_g before it publishes P_g, and reads a tile's O
+  // before it publishes P of the next tile's first step: so P_g published by
+  // all four warps also means that S_g's buffer (next used by S_{g+2}) has
+  // been read, that any rescale of O for step g is done, and, on a tile's
+  // first step, that the previous tile's O has been read.  Steps g count on
+  // across the CTA's tiles.
   uint64_t* s_full = v_empty + kSV;            // [2] scores ready
-  uint64_t* p_full = s_full + 2;               // [2] P written, O rescaled (4 warps)
-  uint64_t* pv_done = p_full + 2;              // [2] P_j V_j done (P_j's buffer read, O updated)
+  uint64_t* p_full = s_full + 2;               // [2] P written, O rescaled / read (4 warps)
+  uint64_t* pv_done = p_full + 2;              // [2] P_g V_g done (P_g's buffer read, O updated)
   uint64_t* mma_done = pv_done + 2;            // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
-  const int qt = a.n_qtiles - 1 - static_cast<int>(blockIdx.y);  // most keys first
-  const int b = bh / a.h, head = bh - b * a.h;
-  const int q0 = qt * kQT;
-  const int q_last = min(q0 + kQT, a.T) - 1;
-  const int n_kt = (a.t_past + q_last + 1 + kKT - 1) / kKT;  // steps up to the last query
+  // This CTA's k-th work item: rounds of gridDim.x items, in reverse CTA
+  // order on odd rounds, so that long and short tiles pair up.
+  const int cta = static_cast<int>(blockIdx.x), n_cta = static_cast<int>(gridDim.x);
+  auto work = [&](int k) { return k * n_cta + ((k & 1) ? n_cta - 1 - cta : cta); };
+  const int w0 = cta;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&pv_done[i], 1);
+    }
     for (int s = 0; s < kSK; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -116,11 +144,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int s = 0; s < kSV; ++s) {
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 4);
-      mbar_init(&pv_done[i], 1);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -142,35 +165,59 @@ __global__ void __launch_bounds__(kThreads, 2)
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
-    mbar_arrive_expect_tx(q_full, kQBytes);
-    tma_load_3d(sQ, &tmQ, q_full, 0, q0, bh);
-    // Next K and V steps to load; a stage is free once the product that read
-    // its previous tile has completed (no wait for the first pass).
-    int kj = 0, vj = 0;
+    // Two streams over the CTA's tiles: K (with each tile's Q ahead of its
+    // first K) and V.  A stage is free once the product that read its
+    // previous tile has completed (no wait for the first pass).
+    int kw = w0, kj = 0, kt = 0, kg = 0;       // K stream: work item, step, tile count, global step
+    int vw = w0, vj = 0, vt = 0, vg = 0;       // V stream
+    Tile tk = tile_of(a, w0 < a.n_work ? w0 : 0), tv = tk;
     bool ok = true;
     unsigned long long t_idle = 0;
-    while (kj < n_kt || vj < n_kt) {
+    int q_issued = 0;                           // Q loads issued (= tiles whose Q is on its way)
+    while (kw < a.n_work || vw < a.n_work) {
       bool progress = false;
-      if (kj < n_kt && (kj < kSK || mbar_test_wait(&k_empty[kj % kSK],
-                                                   static_cast<uint32_t>(kj / kSK - 1) & 1u))) {
-        const int s = kj % kSK;
-        mbar_arrive_expect_tx(&k_full[s], kKVBytes);
-        tma_load_4d(sK + s * kKVBytes, &tmK, &k_full[s], 0, kj * kKT, head, b);
-        ++kj;
-        progress = true;
+      if (kw < a.n_work && kj == 0 && q_issued == kt) {
+        // The tile's Q goes first, into the buffer of tile kt - 2.
+        if (kt < 2 ||
+            mbar_test_wait(&q_empty[kt & 1], static_cast<uint32_t>((kt >> 1) - 1) & 1u)) {
+          mbar_arrive_expect_tx(&q_full[kt & 1], kQBytes);
+          tma_load_3d(sQ + (kt & 1) * kQBytes, &tmQ, &q_full[kt & 1], 0, tk.q0, tk.bh);
+          ++q_issued;
+          progress = true;
+        }
+      } else if (kw < a.n_work) {
+        if (kg < kSK ||
+            mbar_test_wait(&k_empty[kg % kSK], static_cast<uint32_t>(kg / kSK - 1) & 1u)) {
+          const int s = kg % kSK;
+          mbar_arrive_expect_tx(&k_full[s], kKVBytes);
+          tma_load_4d(sK + s * kKVBytes, &tmK, &k_full[s], 0, kj * kKT, tk.head, tk.b);
+          ++kg;
+          progress = true;
+          if (++kj == tk.n_kt) {
+            kj = 0;
+            ++kt;
+            kw = work(kt);
+            if (kw < a.n_work) tk = tile_of(a, kw);
+          }
+        }
       }
-      if (vj < n_kt && (vj < kSV || mbar_test_wait(&v_empty[vj % kSV],
-                                                   static_cast<uint32_t>(vj / kSV - 1) & 1u))) {
-        const int s = vj % kSV;
+      if (vw < a.n_work &&
+          (vg < kSV || mbar_test_wait(&v_empty[vg % kSV], static_cast<uint32_t>(vg / kSV - 1) & 1u))) {
+        const int s = vg % kSV;
         mbar_arrive_expect_tx(&v_full[s], kKVBytes);
-        tma_load_4d(sV + s * kKVBytes, &tmV, &v_full[s], 0, vj * kKT, head, b);
-        ++vj;
+        tma_load_4d(sV + s * kKVBytes, &tmV, &v_full[s], 0, vj * kKT, tv.head, tv.b);
+        ++vg;
         progress = true;
+        if (++vj == tv.n_kt) {
+          vj = 0;
+          vw = work(++vt);
+          if (vw < a.n_work) tv = tile_of(a, vw);
+        }
       }
       if (progress) {
         t_idle = 0;
       } else {
-        // Neither ring has a free stage: the same bounded wait as elsewhere.
+        // Nothing could be issued: the same bounded wait as elsewhere.
         __nanosleep(32);
         const unsigned long long now = global_timer_ns();
         if (t_idle == 0) {
@@ -185,25 +232,31 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     if (!ok) {
       // Drain: every copy already issued must land before the CTA exits.
-      mbar_wait_bounded(q_full, 0, nullptr, a.err);
-      for (int j = max(0, kj - kSK); j < kj; ++j)
-        mbar_wait_bounded(&k_full[j % kSK], static_cast<uint32_t>(j / kSK) & 1u, nullptr, a.err);
-      for (int j = max(0, vj - kSV); j < vj; ++j)
-        mbar_wait_bounded(&v_full[j % kSV], static_cast<uint32_t>(j / kSV) & 1u, nullptr, a.err);
+      for (int t = max(0, q_issued - 2); t < q_issued; ++t)
+        mbar_wait_bounded(&q_full[t & 1], static_cast<uint32_t>(t >> 1) & 1u, nullptr, a.err);
+      for (int g = max(0, kg - kSK); g < kg; ++g)
+        mbar_wait_bounded(&k_full[g % kSK], static_cast<uint32_t>(g / kSK) & 1u, nullptr, a.err);
+      for (int g = max(0, vg - kSV); g < vg; ++g)
+        mbar_wait_bounded(&v_full[g % kSV], static_cast<uint32_t>(g / kSV) & 1u, nullptr, a.err);
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------- MMA issuer --
     const uint32_t id_s = umma_idesc_16(kQT, kKT, false, false);
     const uint32_t id_pv = umma_idesc_16(kQT, kD, false, true);
-    const uint64_t q_desc = sdesc_k_sw128(smem_u32(sQ));
-    bool ok = mbar_wait_bounded(q_full, 0, abort_flag, a.err);
-    auto issue_s = [&](int j) -> bool {
-      const int s = j % kSK, sb = j & 1;
-      // S_{j-2}, the buffer's previous tile, was read before P_{j-2} was
+    // S cursor (one step ahead of the P V cursor), over the CTA's tiles.
+    int sw = w0, sj = 0, st = 0, sg = 0;       // work item, step, tile count, global step
+    Tile ts = tile_of(a, w0 < a.n_work ? w0 : 0);
+    auto issue_s = [&]() -> bool {
+      const int s = sg % kSK, sb = sg & 1;
+      if (sj == 0 && !mbar_wait_bounded(&q_full[st & 1], static_cast<uint32_t>(st >> 1) & 1u,
+                                        abort_flag, a.err))
+        return false;
+      // S_{g-2}, the buffer's previous tile, was read before P_{g-2} was
       // published, which this thread has already waited for.
-      if (!mbar_wait_bounded(&k_full[s], static_cast<uint32_t>(j / kSK) & 1u, abort_flag, a.err))
+      if (!mbar_wait_bounded(&k_full[s], static_cast<uint32_t>(sg / kSK) & 1u, abort_flag, a.err))
         return false;
       tc_fence_after();
+      const uint64_t q_desc = sdesc_k_sw128(smem_u32(sQ + (st & 1) * kQBytes));
       const uint64_t k_desc = sdesc_k_sw128(smem_u32(sK + s * kKVBytes));
       const uint32_t d = tmem + kColS + sb * 64;
 #pragma unroll
@@ -211,26 +264,38 @@ __global__ void __launch_bounds__(kThreads, 2)
         umma_f16kind(d, q_desc + 2 * k, k_desc + 2 * k, id_s, k != 0 ? 1u : 0u);
       umma_commit(&s_full[sb]);
       umma_commit(&k_empty[s]);
+      ++sg;
+      if (++sj == ts.n_kt) {
+        umma_commit(&q_empty[st & 1]);  // the tile's Q buffer is free once this product is done
+        sj = 0;
+        ++st;
+        sw = work(st);
+        if (sw < a.n_work) ts = tile_of(a, sw);
+      }
       return true;
     };
-    if (ok) ok = issue_s(0);
-    for (int j = 0; ok && j < n_kt; ++j) {
-      if (j + 1 < n_kt && !(ok = issue_s(j + 1))) break;
-      const int pb = j & 1, s = j % kSV;
-      if (!mbar_wait_bounded(&v_full[s], static_cast<uint32_t>(j / kSV) & 1u, abort_flag, a.err) ||
-          !mbar_wait_bounded(&p_full[pb], static_cast<uint32_t>(j >> 1) & 1u, abort_flag, a.err)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t p_tmem = tmem + kColP + pb * 32;
-      const uint64_t v_desc = sdesc_mn_sw128(smem_u32(sV + s * kKVBytes));
-      const uint32_t d = tmem + kColO;
+    bool ok = w0 >= a.n_work || issue_s();
+    int g = 0;
+    for (int t = 0, w = w0; ok && w < a.n_work; w = work(++t)) {
+      const int n_kt = tile_of(a, w).n_kt;
+      for (int j = 0; j < n_kt; ++j, ++g) {
+        if (sw < a.n_work && !(ok = issue_s())) break;
+        const int pb = g & 1, s = g % kSV;
+        if (!mbar_wait_bounded(&v_full[s], static_cast<uint32_t>(g / kSV) & 1u, abort_flag, a.err) ||
+            !mbar_wait_bounded(&p_full[pb], static_cast<uint32_t>(g >> 1) & 1u, abort_flag, a.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t p_tmem = tmem + kColP + pb * 32;
+        const uint64_t v_desc = sdesc_mn_sw128(smem_u32(sV + s * kKVBytes));
+        const uint32_t d = tmem + kColO;
 #pragma unroll
-      for (int k = 0; k < kKT / 16; ++k)  // 16 keys: +8 columns of P, +2048 B in V
-        umma_f16kind_ts(d, p_tmem + 8 * k, v_desc + 128 * k, id_pv, (j | k) != 0 ? 1u : 0u);
-      umma_commit(&pv_done[pb]);
-      umma_commit(&v_empty[s]);
+        for (int k = 0; k < kKT / 16; ++k)  // 16 keys: +8 columns of P, +2048 B in V
+          umma_f16kind_ts(d, p_tmem + 8 * k, v_desc + 128 * k, id_pv, (j | k) != 0 ? 1u : 0u);
+        umma_commit(&pv_done[pb]);
+        umma_commit(&v_empty[s]);
+      }
     }
     // Every MMA issued above must retire before TMEM is freed.
     umma_commit(mma_done);
@@ -239,10 +304,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     // ---------------------------------------------------------- softmax --
     const int quarter = warp & 3;                // TMEM lanes 32 * quarter ..
     const int r = quarter * 32 + lane;           // query row in the tile
-    const int pos = a.t_past + q0 + r;           // its absolute position
     const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = 0.125f * kLog2e;           // 1/sqrt(64), in log2 units
-    float m = -INFINITY, l = 0.f;                // reference maximum (log2 units), row sum
     bool ok = true;
     // The product P_t V_t has completed (pv_done of step t; never more than
     // one phase behind when waited for).
@@ -250,108 +313,111 @@ __global__ void __launch_bounds__(kThreads, 2)
       return mbar_wait_bounded(&pv_done[t & 1], static_cast<uint32_t>(t >> 1) & 1u, abort_flag,
                                a.err);
     };
-
-    for (int j = 0; j < n_kt; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait_bounded(&s_full[sb], static_cast<uint32_t>(j >> 1) & 1u, abort_flag, a.err)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[kKT];
-      tmem_ld_32x32b_x32(trow + kColS + sb * 64, *reinterpret_cast<uint32_t(*)[32]>(sr));
-      tmem_ld_32x32b_x32(trow + kColS + sb * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
-      tmem_ld_wait();
-
-      // Raw scores; the 1/sqrt(64) scale (in log2 units) is applied to the
-      // row maximum and inside the exponent's fused multiply-add.
-      const int key0 = j * kKT;
-      float mx = -INFINITY;
-      if (key0 + kKT - 1 > pos) {                 // this step crosses the row's diagonal
-#pragma unroll
-        for (int c = 0; c < kKT; ++c) {
-          const float x = key0 + c <= pos ? __uint_as_float(sr[c]) : -INFINITY;
-          sr[c] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
+    int g = 0;
+    for (int t = 0, w = w0; ok && w < a.n_work; w = work(++t)) {
+      const Tile tl = tile_of(a, w);
+      const int pos = a.t_past + tl.q0 + r;      // this row's absolute position
+      float m = -INFINITY, l = 0.f;              // reference maximum (log2 units), row sum
+      for (int j = 0; j < tl.n_kt; ++j) {
+        const int gj = g + j, sb = gj & 1;
+        if (!mbar_wait_bounded(&s_full[sb], static_cast<uint32_t>(gj >> 1) & 1u, abort_flag,
+                               a.err)) {
+          ok = false;
+          break;
         }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kKT; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
-      }
-      // A new reference maximum only when this row's passed it by more than
-      // kRescaleLog2 (always on the row's first key); O and l scale by
-      // 2^(m_old - m_new) (0 while m_old = -inf).
-      const float m_row = mx * sl2;
-      const bool bump = m_row > m + kRescaleLog2;
-      const float alpha = bump ? ex2(m - m_row) : 1.f;
-      if (bump) m = m_row;
-      l *= alpha;
-      if (j > 0 && __any_sync(0xffffffffu, bump)) {
-        // O holds P_0 V_0 + .. + P_{j-1} V_{j-1}: wait for the last product,
-        // then rescale this warp's 32 rows in place (alpha = 1 elsewhere).
-        if (!(ok = wait_pv(j - 1))) break;
         tc_fence_after();
-        uint32_t ov[kD];
-        tmem_ld_32x32b_x32(trow + kColO, *reinterpret_cast<uint32_t(*)[32]>(ov));
-        tmem_ld_32x32b_x32(trow + kColO + 32, *reinterpret_cast<uint32_t(*)[32]>(ov + 32));
+        uint32_t sr[kKT];
+        tmem_ld_32x32b_x32(trow + kColS + sb * 64, *reinterpret_cast<uint32_t(*)[32]>(sr));
+        tmem_ld_32x32b_x32(trow + kColS + sb * 64 + 32,
+                           *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
         tmem_ld_wait();
+
+        // Raw scores; the 1/sqrt(64) scale (in log2 units) is applied to the
+        // row maximum and inside the exponent's fused multiply-add.
+        const int key0 = j * kKT;
+        float mx = -INFINITY;
+        if (key0 + kKT - 1 > pos) {               // this step crosses the row's diagonal
 #pragma unroll
-        for (int c = 0; c < kD; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-        tmem_st_32x32b_x32(trow + kColO, *reinterpret_cast<uint32_t(*)[32]>(ov));
-        tmem_st_32x32b_x32(trow + kColO + 32, *reinterpret_cast<uint32_t(*)[32]>(ov + 32));
+          for (int c = 0; c < kKT; ++c) {
+            const float x = key0 + c <= pos ? __uint_as_float(sr[c]) : -INFINITY;
+            sr[c] = __float_as_uint(x);
+            mx = fmaxf(mx, x);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kKT; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+        }
+        // A new reference maximum only when this row's passed it by more
+        // than kRescaleLog2 (always on the row's first key); O and l scale
+        // by 2^(m_old - m_new) (0 while m_old = -inf).
+        const float m_row = mx * sl2;
+        const bool bump = m_row > m + kRescaleLog2;
+        const float alpha = bump ? ex2(m - m_row) : 1.f;
+        if (bump) m = m_row;
+        l *= alpha;
+        if (j > 0 && __any_sync(0xffffffffu, bump)) {
+          // O holds this tile's P V products so far: wait for the last one,
+          // then rescale this warp's 32 rows in place (alpha = 1 elsewhere).
+          if (!(ok = wait_pv(gj - 1))) break;
+          tc_fence_after();
+          uint32_t ov[kD];
+          tmem_ld_32x32b_x32(trow + kColO, *reinterpret_cast<uint32_t(*)[32]>(ov));
+          tmem_ld_32x32b_x32(trow + kColO + 32, *reinterpret_cast<uint32_t(*)[32]>(ov + 32));
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < kD; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+          tmem_st_32x32b_x32(trow + kColO, *reinterpret_cast<uint32_t(*)[32]>(ov));
+          tmem_st_32x32b_x32(trow + kColO + 32, *reinterpret_cast<uint32_t(*)[32]>(ov + 32));
+          tmem_st_wait();
+        }
+        const float m_use = m == -INFINITY ? 0.f : m;  // a row with no key yet
+        float lj = 0.f;
+        uint32_t pk[kKT / 2];
+#pragma unroll
+        for (int c = 0; c < kKT / 2; ++c) {
+          const float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), sl2, -m_use));
+          const float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -m_use));
+          lj += p0 + p1;
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        l += lj;
+        // P_g: this row's 64 keys as 32 bf16 pairs in TMEM lane r, in the
+        // buffer P_{g-2} V_{g-2} read last.
+        if (gj >= 2 && !(ok = wait_pv(gj - 2))) break;
+        tmem_st_32x32b_x32(trow + kColP + sb * 32, pk);
         tmem_st_wait();
+        tc_fence_before();  // this warp's TMEM reads and writes come first
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[sb]);
       }
-      const float m_use = m == -INFINITY ? 0.f : m;  // a row with no key yet
-      float lj = 0.f;
-      uint32_t pk[kKT / 2];
-#pragma unroll
-      for (int c = 0; c < kKT / 2; ++c) {
-        const float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), sl2, -m_use));
-        const float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -m_use));
-        lj += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
-      }
-      l += lj;
-      // P_j: this row's 64 keys as 32 bf16 pairs in TMEM lane r, in the
-      // buffer P_{j-2} V_{j-2} read last.
-      if (j >= 2 && !(ok = wait_pv(j - 2))) break;
-      tmem_st_32x32b_x32(trow + kColP + sb * 32, pk);
-      tmem_st_wait();
-      tc_fence_before();  // this warp's TMEM reads and writes come first
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[sb]);
-    }
-    float o[kD];
-    if (ok && (ok = wait_pv(n_kt - 1))) {
+      if (!ok) break;
+      g += tl.n_kt;
+      // o / l straight to the output: 128 contiguous bytes per row, rows
+      // past T not written.  O is read before this warp publishes the next
+      // tile's first P, which the next tile's first product waits for.
+      if (!(ok = wait_pv(g - 1))) break;
       tc_fence_after();
       uint32_t ov[kD];
       tmem_ld_32x32b_x32(trow + kColO, *reinterpret_cast<uint32_t(*)[32]>(ov));
       tmem_ld_32x32b_x32(trow + kColO + 32, *reinterpret_cast<uint32_t(*)[32]>(ov + 32));
       tmem_ld_wait();
-#pragma unroll
-      for (int c = 0; c < kD; ++c) o[c] = __uint_as_float(ov[c]);
-    }
-    if (ok) {
-      // o / l through shared memory (the Q tile's: every product is done)
-      // and one TMA store of this warp's 32 rows; rows past T are not written.
       const float inv = 1.0f / l;
-      uint8_t* orow = sQ + r * 128;
+      const int row = tl.q0 + r;
+      if (row < a.T) {
+        uint4* dst = reinterpret_cast<uint4*>(
+            static_cast<uint16_t*>(a.out) +
+            (static_cast<size_t>(tl.b) * a.T + row) * (static_cast<size_t>(a.h) * kD) +
+            tl.head * kD);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t w[4];
+        for (int c = 0; c < 8; ++c) {
+          uint32_t wv[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          w[e] = pack_16x2(o[8 * c + 2 * e] * inv, o[8 * c + 2 * e + 1] * inv, a.out_f16 != 0);
-        *reinterpret_cast<uint4*>(orow + ((c ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int e = 0; e < 4; ++e)
+            wv[e] = pack_16x2(__uint_as_float(ov[8 * c + 2 * e]) * inv,
+                              __uint_as_float(ov[8 * c + 2 * e + 1]) * inv, a.out_f16 != 0);
+          dst[c] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_3d(&tmO, sQ + quarter * 32 * 128, head * kD, q0 + quarter * 32, b);
-        bulk_commit_group();
-        bulk_wait_group<0>();
-      }
-      __syncwarp();
     }
   }
 
@@ -381,9 +447,9 @@ int launch_attention_tc(const LaunchEnv& env, const bf16* q, const bf16* kv, lon
   const int n_qtiles = (T + kQT - 1) / kQT;
   if (n_qtiles > 65535 || B * h > 0x7fffffff) return GPT2_ERR_UNSUPPORTED;
   const long long t_all = static_cast<long long>(t_past) + T;
-  CUtensorMap tmQ, tmK, tmV, tmO;
+  CUtensorMap tmQ, tmK, tmV;
   // Q [B*h, T, 64]; K and V of the cache {64 dims, t_all positions, h heads,
-  // B sequences}; the output {h*64, T, B}.
+  // B sequences}.
   const cuuint64_t qd[3] = {kD, static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B) * h};
   const cuuint64_t qs[2] = {kD * 2, static_cast<cuuint64_t>(T) * kD * 2};
   const cuuint32_t qb[3] = {kD, kQT, 1};
@@ -392,16 +458,11 @@ int launch_attention_tc(const LaunchEnv& env, const bf16* q, const bf16* kv, lon
   const cuuint64_t ks[3] = {kD * 2, static_cast<cuuint64_t>(s_head) * 2,
                             static_cast<cuuint64_t>(s_batch) * 2};
   const cuuint32_t kb[4] = {kD, kKT, 1, 1};
-  const cuuint64_t od[3] = {static_cast<cuuint64_t>(h) * kD, static_cast<cuuint64_t>(T),
-                            static_cast<cuuint64_t>(B)};
-  const cuuint64_t os[2] = {static_cast<cuuint64_t>(h) * kD * 2,
-                            static_cast<cuuint64_t>(T) * h * kD * 2};
-  const cuuint32_t ob[3] = {kD, 32, 1};
-  if ((s_head * 2) % 16 != 0 || (s_batch * 2) % 16 != 0 || (s_kv * 2) % 16 != 0)
+  if ((s_head * 2) % 16 != 0 || (s_batch * 2) % 16 != 0 || (s_kv * 2) % 16 != 0 ||
+      (reinterpret_cast<uintptr_t>(out) & 15) != 0)
     return GPT2_ERR_ALIGNMENT;
   if (!encode(env, &tmQ, q, 3, qd, qs, qb, false) || !encode(env, &tmK, kv, 4, kd, ks, kb, false) ||
-      !encode(env, &tmV, kv + s_kv, 4, kd, ks, kb, false) ||
-      !encode(env, &tmO, out, 3, od, os, ob, out_f16))
+      !encode(env, &tmV, kv + s_kv, 4, kd, ks, kb, false))
     return GPT2_ERR_CUDA;
   static bool attr_set = false;
   if (!attr_set) {
@@ -410,9 +471,14 @@ int launch_attention_tc(const LaunchEnv& env, const bf16* q, const bf16* kv, lon
       return GPT2_ERR_CUDA;
     attr_set = true;
   }
-  AttnArgs args{T, t_past, h, n_qtiles, out_f16 ? 1 : 0, env.err};
-  const cudaError_t e = launch_pdl(attn_tc_kernel, dim3(B * h, n_qtiles), dim3(kThreads),
-                                   kSmemBytes, stream, tmQ, tmK, tmV, tmO, args);
+  const long long n_work = static_cast<long long>(B) * h * n_qtiles;
+  if (n_work > 0x7fffffff) return GPT2_ERR_UNSUPPORTED;
+  AttnArgs args{T, t_past, h, n_qtiles, B * h, static_cast<int>(n_work), out_f16 ? 1 : 0, out,
+                env.err};
+  // Two resident CTAs per SM, each walking the tiles w = blockIdx.x, + grid, ...
+  const int grid = static_cast<int>(std::min<long long>(n_work, 2LL * env.num_sms));
+  const cudaError_t e = launch_pdl(attn_tc_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream,
+                                   tmQ, tmK, tmV, args);
   return e == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
