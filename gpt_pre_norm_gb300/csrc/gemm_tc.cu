@@ -774,10 +774,13 @@ bool encode_heads(const LaunchEnv& env, CUtensorMap* map, const void* base, long
          CUDA_SUCCESS;
 }
 
-// Tile width: the candidate minimising waves x (BN + 32): the busiest SM's
-// (or CTA pair's) share of the work plus a per-tile cost (operand reloads,
-// epilogue start), preferring wider tiles on ties.  Tiles have tile_rows rows
-// and `units` of them run at once.
+// Tile width: the candidate minimising waves x (width cost + 32): the busiest
+// SM's (or CTA pair's) share of the work plus a per-tile cost (operand
+// reloads, epilogue start), preferring wider tiles on ties.  Tiles have
+// tile_rows rows and `units` of them run at once.  Narrow MMAs do less work
+// per cycle, so a tile's width cost is its time relative to a 256-wide one,
+// fitted to GB300 timings of the GPT-2-small products in 256-, 192- and
+// 128-wide tiles (e.g. c_fc: 34.9, 37.0 and 50.1 us).
 int choose_bn(int M, int N, int tile_rows, int units) {
   const int num_sms = units;
   const int m_blocks = (M + tile_rows - 1) / tile_rows;
@@ -786,7 +789,8 @@ int choose_bn(int M, int N, int tile_rows, int units) {
   for (int bn : {256, 192, 128, 64}) {
     const long long tiles = static_cast<long long>(m_blocks) * ((N + bn - 1) / bn);
     const long long waves = (tiles + num_sms - 1) / num_sms;
-    const long long cost = waves * (bn + 32);
+    const int width_cost = bn == 256 ? 256 : bn == 192 ? 235 : bn == 128 ? 190 : 120;
+    const long long cost = waves * (width_cost + 32);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best = bn;
