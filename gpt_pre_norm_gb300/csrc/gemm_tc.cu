@@ -15,8 +15,9 @@
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=BN,
 //               K=16) x4 per slot into one of two TMEM accumulators.
 //   warp 2      allocates / frees 512 TMEM columns.
-//   warps 4-11  epilogue, two warps per TMEM lane quarter, each taking half
-//               of the tile's columns in chunks of 32 x 32: tcgen05.ld, bias /
+//   warps 4..   epilogue, two warps per TMEM lane quarter, each taking half
+//               of the tile's columns (one warp, all of them, for the bf16
+//               block output) in chunks of 32 x 32: tcgen05.ld, bias /
 //               GELU / residual in registers, the chunk written to a swizzled
 //               shared-memory box, and one TMA tensor store per chunk (the
 //               fp32 residual arrives the same way, by a TMA load).  Q, K and
@@ -40,16 +41,21 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;                       // one 128-byte swizzle row of bf16
-constexpr int kEpiWarps = 8;                  // two per TMEM lane quarter
-constexpr int kThreads = 128 + 32 * kEpiWarps;
+// Epilogue warps: two per TMEM lane quarter (each taking half of a tile's
+// columns), or one for the bf16 block output made from the fp32 residual
+// (measured on GB300 for the block's mlp c_proj: GPT-2-small 43.3 -> 41.2 us,
+// GPT-2-XL shape 80 -> 70 us with four; the in-place fp32 residual epilogue
+// is faster with eight).
+__host__ __device__ constexpr int epi_warps(int k) { return k == kEpiResidBf16Out ? 4 : 8; }
+__host__ __device__ constexpr int epi_threads(int k) { return 128 + 32 * epi_warps(k); }
 constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB per A slot
 constexpr int kMaxStages = 8;
 constexpr uint32_t kTmemCols = 512;           // two accumulators of up to 256 columns
 constexpr int kSmemLimit = 232448;            // 227 KB opt-in per CTA
 constexpr int kRBuf = 32 * 32 * 4;            // fp32 32x32 box, rows of 128 B, 128-byte swizzle
 constexpr int kOBuf = 32 * 32 * 2;            // bf16 32x32 box, rows of 64 B, 64-byte swizzle
-constexpr int kBiasBufs = 3;                  // bias buffers per column half, by tile index mod 3
-constexpr int kBiasBytes = 2 * kBiasBufs * 128 * 2;  // bf16 bias of each half's columns (<= 128)
+constexpr int kBiasBufs = 3;                  // bias buffers per column segment, by tile index mod 3
+constexpr int kBiasBytes = kBiasBufs * 256 * 2;  // bf16 bias of a tile's columns, per buffer
 constexpr int kLogitsLd = 33;                 // logits transpose row stride (floats)
 
 static_assert(kRBuf % 1024 == 0 && kOBuf % 1024 == 0, "staging boxes must stay 1 KB aligned");
@@ -110,8 +116,8 @@ __device__ __forceinline__ void tile_coords(const GemmArgs& a, int tile, int& m_
 __host__ __device__ inline size_t smem_bytes_for(int kind, int BN, int stages, int cg) {
   return 1024 /* alignment slack */ +
          static_cast<size_t>(stages) * (kABytes + (BN / cg) * kBK * 2) +
-         static_cast<size_t>(kEpiWarps) * epi_warp_bytes(kind) + epi_bias_bytes(kind) +
-         (2 * stages + 5 + 2 * kEpiWarps) * sizeof(uint64_t) + 16;
+         static_cast<size_t>(epi_warps(kind)) * epi_warp_bytes(kind) + epi_bias_bytes(kind) +
+         (2 * stages + 5 + 2 * epi_warps(kind)) * sizeof(uint64_t) + 16;
 }
 
 __device__ __forceinline__ void unpack8(const uint4 v, float* f) {
@@ -213,8 +219,7 @@ __device__ __forceinline__ void epilogue_prefetch(int row0, int ncol0, int ncols
                                                   const CUtensorMap* tmR) {
   if constexpr (KIND != kEpiLogits && KIND != kEpiLogitsT) {
     const int N = a.N;
-    const int j = 4 * lane;
-    if (j < ncols) {
+    for (int j = 4 * lane; j < ncols; j += 128) {
       const int col = ncol0 + j;
       const uint16_t* bp = static_cast<const uint16_t*>(a.ep.bias) + col;
       uint2 w;
@@ -473,11 +478,12 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol
 // CTA's stage barrier, the first CTA issues the pair MMA, and each CTA's
 // epilogue drains its own 128 accumulator rows.
 template <int KIND, int CG>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(epi_threads(KIND), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmR,
                    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
                    const GemmArgs args) {
+  constexpr int kEpiWarps = epi_warps(KIND);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -636,11 +642,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // accumulator is fetched before waiting for it.
     const int e = warp - 4;
     const int quarter = warp & 3;
-    const int half = e >> 2;
-    const int ncols = BN / 2;
+    const int half = e >> 2;                   // column segment
+    const int ncols = BN / (kEpiWarps / 4);
     uint8_t* epi = sEpi + static_cast<size_t>(e) * epi_warp_bytes(KIND);
     uint16_t* bias_half = reinterpret_cast<uint16_t*>(sEpi + kEpiWarps * epi_warp_bytes(KIND)) +
-                          half * kBiasBufs * 128;
+                          half * kBiasBufs * (256 / (kEpiWarps / 4));
     uint64_t* rbar = rbars + 2 * e;
     EpiState st;
     st.chunk = 0;
@@ -660,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tile_coords(args, tile, m_blk, n_blk);
       const int row0 = m_blk * tile_rows + static_cast<int>(rank) * kBM + quarter * 32;
       const int ncol0 = n_blk * BN + half * ncols;
-      uint16_t* bias_s = bias_half + (it % kBiasBufs) * 128;
+      uint16_t* bias_s = bias_half + (it % kBiasBufs) * (256 / (kEpiWarps / 4));
       epilogue_prefetch<KIND>(row0, ncol0, ncols, lane, epi, bias_s, rbar, st, args, &tmR);
       if (!mbar_wait_bounded(&tfull[acc], acc_par, abort_flag, args.err)) break;
       tc_fence_after();
@@ -900,7 +906,7 @@ int launch_gemm_tc(const LaunchEnv& env, int kind_in, const void* A_in, const vo
   void* params[] = {&tmA, &tmB, &tmO, &tmR, &tmQ, &tmKV, &args};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(static_cast<unsigned>(epi_threads(kind)));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
