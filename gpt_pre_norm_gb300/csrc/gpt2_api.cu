@@ -271,7 +271,7 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int slot, int B, int
   void* attn = c->ws + c->plan.attn;
   float* resid = c->at<float>(c->plan.resid);
   void* fc = c->ws + c->plan.fc;
-  int st;
+  int st = GPT2_OK;
 
   // bf16 mode: the GEMM operands are fp16 (activations written by the
   // producing kernels; weights converted from bf16 per call, or cached).
