@@ -38,6 +38,9 @@ Linear weights are stored [out, in] (nn.Linear convention of the TorchCode
 page) and the fused c_attn rows are Q | K | V, head j at columns
 [j*d_h, (j+1)*d_h) of each.
 
+The post-norm block (the arrangement the pages contrast with GPT-2's) is
+the one variant written out besides the pre-norm path.
+
 Pins: every function here is checked against values fixed by the pages or by
 mathematics (printed parameter counts, closed forms, invariants, brute force on
 tiny inputs, library special cases) in tests/test_oracle_pins.py.
@@ -213,6 +216,22 @@ def block_forward(x: np.ndarray, p: dict, n_head: int, past: np.ndarray | None =
     m = mlp(layer_norm(x, p["ln2_g"], p["ln2_b"]), p, gelu_form)
     x = x + m
     return x, present
+
+
+def block_forward_postnorm(x: np.ndarray, p: dict, n_head: int, gelu_form: str = "tanh"):
+    """The post-norm arrangement the pages contrast with GPT-2's ([DB]
+    "Overview": the original Transformer applies LayerNorm after the residual
+    add): x = LN1(x + Attn(x)); x = LN2(x + MLP(x)), with the same parameters
+    as the pre-norm block and no cache.  x [B, T, d] -> [B, T, d]."""
+    x = np.asarray(x, np.float64)
+    d = x.shape[-1]
+    if d % n_head != 0:
+        raise ValueError("d must be a multiple of n_head")
+    _check_block_shapes(p, d)
+    a, _ = attn(x, p, n_head)
+    x = layer_norm(x + a, p["ln1_g"], p["ln1_b"])
+    m = mlp(x, p, gelu_form)
+    return layer_norm(x + m, p["ln2_g"], p["ln2_b"])
 
 
 def embed(ids: np.ndarray, wte: np.ndarray, wpe: np.ndarray, t_past: int = 0) -> np.ndarray:

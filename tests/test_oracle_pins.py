@@ -242,6 +242,70 @@ def test_block_causality():
         assert np.all(np.abs(out[:, t] - base[:, t]).max(axis=-1) > 1e-6)
 
 
+# ------------------------------------------------------- post-norm variant
+def test_postnorm_zero_sublayers_is_two_layer_norms():
+    """With every Linear map zero, both sublayers add zero, so the post-norm
+    block is LN2(LN1(x)); distinct LN1 / LN2 parameters make the order of the
+    two normalisations and the residual adds visible (pre-norm would return x,
+    a missing residual would return LN of a constant row)."""
+    rng = _rng(21)
+    d, h = 16, 4
+    p = _block_params(d, rng)
+    for k in ("attn_w", "attn_b", "proj_w", "proj_b", "fc_w", "fc_b", "mlp_proj_w", "mlp_proj_b"):
+        p[k] = np.zeros_like(p[k])
+    x = 3.0 * rng.standard_normal((2, 5, d)) + 1.0
+    out = O.block_forward_postnorm(x, p, h)
+    two = O.layer_norm(O.layer_norm(x, p["ln1_g"], p["ln1_b"]), p["ln2_g"], p["ln2_b"])
+    np.testing.assert_allclose(out, two, rtol=0, atol=1e-12)
+    assert np.abs(out - x).max() > 0.1
+
+
+def test_postnorm_output_rows_are_normalised():
+    """With LN2's gain 1 and bias 0 every output row has mean 0 and a biased
+    variance of s / (s + eps) < 1, whatever the sublayers did."""
+    rng = _rng(22)
+    d, h = 32, 4
+    p = _block_params(d, rng, 0.3)
+    p["ln2_g"] = np.ones(d)
+    p["ln2_b"] = np.zeros(d)
+    x = rng.standard_normal((2, 6, d))
+    out = O.block_forward_postnorm(x, p, h)
+    np.testing.assert_allclose(out.mean(-1), 0.0, atol=1e-12)
+    var = out.var(-1)
+    assert np.all(var < 1.0) and np.all(var > 1.0 - 1e-3)
+
+
+def test_postnorm_mlp_sees_the_normalised_stream():
+    """With the attention maps zero, the MLP's input and the second residual
+    are LN1(x), which does not change under x -> a x + c (a > 0, c per row)
+    except through eps (a relative change of about eps / var(x) ~ 1e-5 here):
+    the block output must not change beyond that either (an MLP or a residual
+    fed x instead of LN1(x) would change it by O(1))."""
+    rng = _rng(23)
+    d, h = 16, 4
+    p = _block_params(d, rng, 0.5)
+    for k in ("attn_w", "attn_b", "proj_w", "proj_b"):
+        p[k] = np.zeros_like(p[k])
+    x = rng.standard_normal((2, 5, d))
+    base = O.block_forward_postnorm(x, p, h)
+    moved = O.block_forward_postnorm(2.5 * x + rng.standard_normal((2, 5, 1)), p, h)
+    np.testing.assert_allclose(moved, base, rtol=0, atol=1e-4)
+
+
+def test_postnorm_block_causality():
+    rng = _rng(24)
+    d, h, T = 16, 4, 7
+    p = _block_params(d, rng, 0.3)
+    x = rng.standard_normal((2, T, d))
+    base = O.block_forward_postnorm(x, p, h)
+    for t in (0, 3, T - 1):
+        x2 = x.copy()
+        x2[:, t] += rng.standard_normal(d)
+        out = O.block_forward_postnorm(x2, p, h)
+        np.testing.assert_array_equal(out[:, :t], base[:, :t])
+        assert np.all(np.abs(out[:, t] - base[:, t]).max(axis=-1) > 1e-6)
+
+
 @pytest.mark.parametrize("form", ["tanh", "erf"])
 def test_block_library_special_case(form):
     """torch's pre-norm TransformerEncoderLayer (norm_first, causal mask, 4d MLP,
