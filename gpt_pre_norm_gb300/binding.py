@@ -75,6 +75,8 @@ def _load() -> C.CDLL:
         "gpt2_status_string": (C.c_char_p, [I]),
         "gpt2_block_forward": (I, [P, P, C.POINTER(gpt2_block_params), I, I, I, I,
                                    C.POINTER(gpt2_kv), C.POINTER(gpt2_kv), P, P]),
+        "gpt2_block_forward_postnorm": (I, [P, P, C.POINTER(gpt2_block_params), I, I, I, I, P,
+                                            P]),
         "gpt2_forward": (I, [P, P, I, I, C.POINTER(gpt2_params), I, C.POINTER(gpt2_kv),
                              C.POINTER(gpt2_kv), P, P]),
         "gpt2_layer_norm": (I, [I, P, I, P, P, I, I, P, P]),
@@ -206,6 +208,18 @@ def gpt2_block_forward(ctx: Context, x: torch.Tensor, params: dict, B: int, T: i
     _check(st, "gpt2_block_forward")
     if present is not None:
         present.T_len = pr.T_len
+    return out
+
+
+def gpt2_block_forward_postnorm(ctx: Context, x: torch.Tensor, params: dict, B: int, T: int,
+                                d: int, n_head: int, out: torch.Tensor | None = None,
+                                stream=None) -> torch.Tensor:
+    if out is None:
+        out = torch.empty_like(x)
+    bp = block_params_struct(params)
+    st = LIB.gpt2_block_forward_postnorm(ctx.handle, _ptr(x), C.byref(bp), B, T, d, n_head,
+                                         _ptr(out), _stream(stream))
+    _check(st, "gpt2_block_forward_postnorm")
     return out
 
 

@@ -588,6 +588,114 @@ int gpt2_block_forward(gpt2_ctx* c, const void* x, const gpt2_block_params* para
   return GPT2_OK;
 }
 
+int gpt2_block_forward_postnorm(gpt2_ctx* c, const void* x, const gpt2_block_params* p, int B,
+                                int T, int d, int n_head, void* out, void* stream) {
+  if (!c || !x || !out) return GPT2_ERR_INVALID_ARG;
+  if (d != c->hp.n_embd || n_head != c->hp.n_head) return GPT2_ERR_INVALID_ARG;
+  int st = check_ctx_shapes(c, B, T);
+  if (st) return st;
+  if ((st = validate_block_params(p))) return st;
+  if (!aligned16(x) || !aligned16(out)) return GPT2_ERR_ALIGNMENT;
+  if (T > c->hp.n_ctx) return GPT2_ERR_CTX_OVERFLOW;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const gpt2_hparams& hp = c->hp;
+  const int h = n_head, dh = d / h, M = B * T;
+  const bool bf = hp.dtype == GPT2_BF16;
+  const size_t es = bf ? 2 : 4;
+  const KvView kv = layer_view(c->ws + c->plan.kv, hp.n_ctx, 1, 0, h, dh, es);
+  void* x1 = c->ws + c->plan.ln;      // LN1 output: the normalised stream
+  void* q = c->ws + c->plan.q;
+  void* attn = c->ws + c->plan.attn;
+  float* pre = c->at<float>(c->plan.resid);  // x + a, then x1 + m (fp32)
+  void* fc = c->ws + c->plan.fc;
+
+  // c_attn on x itself -> Q and the block's K/V
+  EpiParams e{};
+  e.bias = p->attn_b;
+  e.q = q;
+  e.kv.base = kv.base;
+  e.kv.s_batch = kv.s_batch;
+  e.kv.s_kv = kv.s_kv;
+  e.kv.s_head = kv.s_head;
+  e.kv.t_past = 0;
+  e.T = T;
+  e.d = d;
+  e.ldo = 3 * d;
+  st = c->run(bf ? kKindGemmQkv : kKindSimtFp32, s, [&](double* fl, double* by) {
+    if (bf)
+      return launch_gemm_tc(c->env, kEpiQkv, x, p->attn_w, M, 3 * d, d, e, s, fl, by, false, false);
+    return launch_gemm_fp32(c->env, kEpiQkv, static_cast<const float*>(x),
+                            static_cast<const float*>(p->attn_w), M, 3 * d, d, e, dh, s);
+  });
+  if (st) return st;
+  st = c->run(bf ? kKindAttention : kKindSimtFp32, s, [&](double* fl, double* by) {
+    *fl = 4.0 * B * h * (0.5 * T * (T + 1.0)) * dh;
+    *by = static_cast<double>(B) * h * (2.0 * T * dh * 2 + 2.0 * T * dh * 2);
+    if (bf)
+      return launch_attention_tc(c->env, static_cast<const bf16*>(q),
+                                 reinterpret_cast<const bf16*>(kv.base), kv.s_batch, kv.s_kv,
+                                 kv.s_head, B, h, T, 0, attn, s, false);
+    return launch_attention_fp32(static_cast<const float*>(q),
+                                 reinterpret_cast<const float*>(kv.base), kv.s_batch, kv.s_kv,
+                                 kv.s_head, B, h, T, 0, dh, static_cast<float*>(attn), s);
+  });
+  if (st) return st;
+  // pre = x + c_proj(attn) + b (fp32)
+  EpiParams e2{};
+  e2.bias = p->proj_b;
+  e2.ldo = d;
+  e2.resid = x;
+  e2.out = pre;
+  st = c->run(bf ? kKindGemmProj : kKindSimtFp32, s, [&](double* fl, double* by) {
+    if (bf)
+      return launch_gemm_tc(c->env, kEpiResidBf16In, attn, p->proj_w, M, d, d, e2, s, fl, by,
+                            false, false);
+    return launch_gemm_fp32(c->env, kEpiResidF32, static_cast<const float*>(attn),
+                            static_cast<const float*>(p->proj_w), M, d, d, e2, dh, s);
+  });
+  if (st) return st;
+  // x1 = LN1(pre)
+  st = c->run(kKindLayerNorm, s, [&](double* fl, double* by) {
+    *fl = 0;
+    *by = static_cast<double>(M) * d * (4 + es);
+    return launch_layer_norm(hp.dtype, pre, GPT2_FP32, p->ln1_g, p->ln1_b, M, d, x1, s, false);
+  });
+  if (st) return st;
+  // fc = GELU(c_fc(x1))
+  EpiParams e3{};
+  e3.bias = p->fc_b;
+  e3.out = fc;
+  e3.ldo = 4 * d;
+  st = c->run(bf ? kKindGemmFc : kKindSimtFp32, s, [&](double* fl, double* by) {
+    if (bf)
+      return launch_gemm_tc(c->env, kEpiGelu, x1, p->fc_w, M, 4 * d, d, e3, s, fl, by, false,
+                            false);
+    return launch_gemm_fp32(c->env, kEpiGelu, static_cast<const float*>(x1),
+                            static_cast<const float*>(p->fc_w), M, 4 * d, d, e3, dh, s);
+  });
+  if (st) return st;
+  // pre = x1 + mlp_proj(fc) + b (fp32)
+  EpiParams e4{};
+  e4.bias = p->mlp_proj_b;
+  e4.ldo = d;
+  e4.resid = x1;
+  e4.out = pre;
+  st = c->run(bf ? kKindGemmMlpProj : kKindSimtFp32, s, [&](double* fl, double* by) {
+    if (bf)
+      return launch_gemm_tc(c->env, kEpiResidBf16In, fc, p->mlp_proj_w, M, d, 4 * d, e4, s, fl,
+                            by, false, false);
+    return launch_gemm_fp32(c->env, kEpiResidF32, static_cast<const float*>(fc),
+                            static_cast<const float*>(p->mlp_proj_w), M, d, 4 * d, e4, dh, s);
+  });
+  if (st) return st;
+  // out = LN2(pre)
+  return c->run(kKindLayerNorm, s, [&](double* fl, double* by) {
+    *fl = 0;
+    *by = static_cast<double>(M) * d * (4 + es);
+    return launch_layer_norm(hp.dtype, pre, GPT2_FP32, p->ln2_g, p->ln2_b, M, d, out, s, false);
+  });
+}
+
 int gpt2_forward(gpt2_ctx* c, const int32_t* ids, int B, int T, const gpt2_params* params, int L,
                  const gpt2_kv* past, gpt2_kv* present, float* logits, void* stream) {
   if (!c || !ids || !params || !logits || !params->blocks) return GPT2_ERR_INVALID_ARG;

@@ -166,6 +166,17 @@ int gpt2_block_forward(gpt2_ctx *ctx, const void *x, const gpt2_block_params *pa
                        int d, int n_head, const gpt2_kv *past, gpt2_kv *present, void *out,
                        void *stream);
 
+/* The post-norm arrangement of the same block, which the pages contrast
+ * with GPT-2's pre-norm ("GPT-2 Decoder Block", "Overview": the original
+ * Transformer normalises after each residual add):
+ *   x1 = LN1(x + c_proj(causal_MHA(c_attn(x))));
+ *   out = LN2(x1 + mlp_proj(GELU_tanh(c_fc(x1)))).
+ * Same parameters, arguments, layouts and errors as gpt2_block_forward, with
+ * no cache.  In bf16 mode the products take the bf16 weights as they are and
+ * the normalised stream x1 is kept in bf16 (no fp16 working copies).       */
+int gpt2_block_forward_postnorm(gpt2_ctx *ctx, const void *x, const gpt2_block_params *params,
+                                int B, int T, int d, int n_head, void *out, void *stream);
+
 /* The full forward ("GPT-2 Full Forward Pass", "How it works"):
  * H = wte[ids] + wpe[T_past + t]; L blocks; logits = LN_f(H) wte^T.
  * ids: device int32 [B, T], each in [0, n_vocab).

@@ -78,6 +78,7 @@ def test_hparams_validation(G, kw, status):
 def test_null_arguments_rejected_without_launch(G):
     assert G.LIB.gpt2_block_forward(None, None, None, 1, 1, 768, 12, None, None, None, None) == 1
     assert G.LIB.gpt2_forward(None, None, 1, 1, None, 12, None, None, None, None) == 1
+    assert G.LIB.gpt2_block_forward_postnorm(None, None, None, 1, 1, 768, 12, None, None) == 1
     assert G.LIB.gpt2_layer_norm(0, None, 0, None, None, 1, 768, None, None) == 1
     assert G.LIB.gpt2_sync_status(None, None) == 1
     assert G.LIB.gpt2_linear(None, 0, None, None, None, None, None, 1, 1, 1, None) == 1

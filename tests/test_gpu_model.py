@@ -67,6 +67,38 @@ def test_block_bf16(G, name, B, T):
     assert_bf16_close(got_present[:, 1], ref_present[:, 1], what="present V")
 
 
+def test_block_postnorm_fp32_debug_shape(G):
+    """The post-norm arrangement (LayerNorm after each residual add) on the
+    TorchCode debug shapes, fp32, against the oracle's post-norm block."""
+    w = S.WORKLOADS["block_fp32_d64"]
+    for seed in (0, 1):
+        p = S.block_params(w, seed)
+        x = S.block_input(w, seed)
+        ctx = G.Context(50257, 1024, w.d, w.n_head, 1, G.GPT2_FP32, w.B, w.T)
+        out = G.gpt2_block_forward_postnorm(ctx, dev(x, torch.float32),
+                                            block_to_device(p, torch.float32), w.B, w.T, w.d,
+                                            w.n_head)
+        assert G.gpt2_sync_status(ctx) == 0
+        ref = O.block_forward_postnorm(x, p, w.n_head)
+        assert_fp32_close(host(out), ref, what="fp32 post-norm block")
+
+
+@pytest.mark.parametrize("name,B,T", [("block_bf16_d768", 2, 300), ("block_bf16_d1600", 1, 130),
+                                      ("block_bf16_d768", 3, 1), ("block_bf16_d768", 2, 1024)])
+def test_block_postnorm_bf16(G, name, B, T):
+    w = S.WORKLOADS[name]
+    p = S.block_params(w, seed=4)
+    x = S.block_input(w, seed=4, B=B, T=T)
+    ctx = G.Context(50257, 1024, w.d, w.n_head, 1, G.GPT2_BF16, B, T)
+    out = G.gpt2_block_forward_postnorm(ctx, dev(x), block_to_device(p), B, T, w.d, w.n_head)
+    assert G.gpt2_sync_status(ctx) == 0
+    ref = O.block_forward_postnorm(x, p, w.n_head)
+    assert_bf16_close(host(out), ref, what="post-norm block out")
+    # The pre-norm block differs from it by O(1): the two are not confused.
+    pre, _ = O.block_forward(x, p, w.n_head)
+    assert np.abs(host(out) - pre).max() > 0.5
+
+
 @pytest.mark.parametrize("mode", ["in_place", "copy", "no_present"])
 def test_block_with_cache_equals_uncached(G, mode):
     w = S.WORKLOADS["block_bf16_d768"]
