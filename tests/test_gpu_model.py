@@ -67,6 +67,30 @@ def test_block_bf16(G, name, B, T):
     assert_bf16_close(got_present[:, 1], ref_present[:, 1], what="present V")
 
 
+def test_block_four_linear_form_by_concatenation(G):
+    """A block given as four separate attention Linear maps (W_q, W_k, W_v,
+    W_o) runs through the same entry point once W_q | W_k | W_v are stacked by
+    rows into c_attn (the oracle pins that identity against the separate
+    form)."""
+    w = S.WORKLOADS["block_bf16_d768"]
+    B, T, d = 2, 200, w.d
+    p = S.block_params(w, seed=6)
+    rng = np.random.default_rng(6)
+    sep = {k: (0.02 * rng.standard_normal((d, d))).astype(np.float32) for k in ("q", "k", "v")}
+    sep_b = {k: (0.02 * rng.standard_normal(d)).astype(np.float32) for k in ("q", "k", "v")}
+    # bf16-representable values, as the device receives them
+    rt = lambda a: torch.from_numpy(np.asarray(a, np.float32)).bfloat16().double().numpy()
+    p["attn_w"] = rt(np.concatenate([sep["q"], sep["k"], sep["v"]], 0))
+    p["attn_b"] = rt(np.concatenate([sep_b["q"], sep_b["k"], sep_b["v"]]))
+    x = S.block_input(w, seed=6, B=B, T=T)
+    ctx = G.Context(50257, 1024, d, w.n_head, 1, G.GPT2_BF16, B, T)
+    out = G.gpt2_block_forward(ctx, dev(x), block_to_device(p), B, T, d, w.n_head)
+    assert G.gpt2_sync_status(ctx) == 0
+    ref, _ = O.block_forward(x, p, w.n_head)
+    assert_bf16_close(host(out), ref, what="four-Linear block")
+    assert_bf16_close(host(out) - x, ref - x, tol=5e-2, what="four-Linear block branch")
+
+
 def test_block_postnorm_fp32_debug_shape(G):
     """The post-norm arrangement (LayerNorm after each residual add) on the
     TorchCode debug shapes, fp32, against the oracle's post-norm block."""
@@ -252,6 +276,36 @@ def test_generate_greedy(G):
             exact += int(out[b, i] == np.argmax(row))
         seq = np.concatenate([seq, out[:, i:i + 1]], axis=1)
     assert exact >= 0.9 * w.B * n_new
+
+
+def test_generate_greedy_graph_captured(G):
+    """The generation loop makes no host round trip (each argmax feeds the
+    next step on the device), so it captures into one CUDA graph; replaying
+    the graph gives the eager run's tokens and (to rounding) its cache."""
+    w = _small_model(n_layer=2, V=1000)
+    p = S.model_params(w, seed=10)
+    ids = dev(S.token_ids(w, seed=10, T=20), torch.int32)
+    n_new = 6
+    ctx = G.Context(w.n_vocab, w.n_ctx, w.d, w.n_head, w.n_layer, G.GPT2_BF16, w.B, 20)
+    mp = G.ModelParams(model_to_device(p))
+    eager_cache = _kv(G, w.B, w.n_head, 64, w.d_h, torch.bfloat16, L=w.n_layer)
+    eager = G.gpt2_generate_greedy(ctx, ids, mp, n_new, eager_cache).cpu().numpy()
+    assert G.gpt2_sync_status(ctx) == 0
+    cache = _kv(G, w.B, w.n_head, 64, w.d_h, torch.bfloat16, L=w.n_layer)
+    logits = torch.empty((w.B, 20, w.n_vocab), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        out = G.gpt2_generate_greedy(ctx, ids, mp, n_new, cache, logits=logits)
+    g.replay()
+    torch.cuda.synchronize()
+    assert G.gpt2_sync_status(ctx) == 0
+    np.testing.assert_array_equal(out.cpu().numpy(), eager)
+    # The decode steps' fp32 residual adds of the K-chunked products are
+    # atomic (their order varies run to run), so the cache agrees to rounding.
+    T_all = 20 + n_new - 1
+    assert_bf16_close(cache.data[..., :T_all, :].float().cpu().numpy(),
+                      eager_cache.data[..., :T_all, :].float().cpu().numpy(), what="graph cache")
 
 
 # ----------------------------------------------------------- error paths ----

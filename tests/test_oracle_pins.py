@@ -242,6 +242,40 @@ def test_block_causality():
         assert np.all(np.abs(out[:, t] - base[:, t]).max(axis=-1) > 1e-6)
 
 
+def _four_linear_attention(x, wq, bq, wk, bk, wv, bv, wo, bo, h):
+    """The separate-projection form (TorchCode "Requirements": W_q, W_k, W_v,
+    W_o as four Linear maps), written with torch's causal scaled-dot-product
+    attention: [B, T, d] -> [B, T, d]."""
+    xt = torch.from_numpy(x)
+    B, T, d = x.shape
+
+    def heads(t):
+        return t.view(B, T, h, d // h).transpose(1, 2)
+
+    q = heads(F.linear(xt, torch.from_numpy(wq), torch.from_numpy(bq)))
+    k = heads(F.linear(xt, torch.from_numpy(wk), torch.from_numpy(bk)))
+    v = heads(F.linear(xt, torch.from_numpy(wv), torch.from_numpy(bv)))
+    o = F.scaled_dot_product_attention(q, k, v, is_causal=True)
+    o = o.transpose(1, 2).reshape(B, T, d)
+    return F.linear(o, torch.from_numpy(wo), torch.from_numpy(bo)).numpy()
+
+
+def test_four_linear_form_equals_fused_c_attn():
+    """Separate W_q, W_k, W_v concatenated by rows (Q | K | V) are the fused
+    c_attn, W_o is c_proj: the oracle's attention reproduces the four-Linear
+    form exactly (a wrong concatenation order or head split would not)."""
+    rng = _rng(26)
+    d, h, B, T = 32, 4, 2, 9
+    w = {k: 0.3 * rng.standard_normal((d, d)) for k in ("q", "k", "v", "o")}
+    b = {k: 0.1 * rng.standard_normal(d) for k in ("q", "k", "v", "o")}
+    x = rng.standard_normal((B, T, d))
+    ref = _four_linear_attention(x, w["q"], b["q"], w["k"], b["k"], w["v"], b["v"], w["o"], b["o"], h)
+    p = {"attn_w": np.concatenate([w["q"], w["k"], w["v"]], 0),
+         "attn_b": np.concatenate([b["q"], b["k"], b["v"]]), "proj_w": w["o"], "proj_b": b["o"]}
+    got, _ = O.attn(x, p, h)
+    np.testing.assert_allclose(got, ref, rtol=1e-11, atol=1e-11)
+
+
 # ------------------------------------------------------- post-norm variant
 def test_postnorm_zero_sublayers_is_two_layer_norms():
     """With every Linear map zero, both sublayers add zero, so the post-norm
@@ -290,6 +324,34 @@ def test_postnorm_mlp_sees_the_normalised_stream():
     base = O.block_forward_postnorm(x, p, h)
     moved = O.block_forward_postnorm(2.5 * x + rng.standard_normal((2, 5, 1)), p, h)
     np.testing.assert_allclose(moved, base, rtol=0, atol=1e-4)
+
+
+@pytest.mark.parametrize("form", ["tanh", "erf"])
+def test_postnorm_library_special_case(form):
+    """torch's TransformerEncoderLayer with norm_first=False is the post-norm
+    arrangement (norm1(x + attention), then norm2(x + feed-forward)) and, with
+    the same weights, computes the oracle's post-norm block."""
+    rng = _rng(25)
+    d, h, B, T = 32, 4, 2, 7
+    p = _block_params(d, rng, 0.2)
+    x = rng.standard_normal((B, T, d))
+    act = (lambda t: F.gelu(t, approximate="tanh")) if form == "tanh" else F.gelu
+    layer = torch.nn.TransformerEncoderLayer(d, h, dim_feedforward=4 * d, dropout=0.0, activation=act,
+                                             layer_norm_eps=1e-5, batch_first=True, norm_first=False,
+                                             dtype=torch.float64)
+    sd = {"self_attn.in_proj_weight": p["attn_w"], "self_attn.in_proj_bias": p["attn_b"],
+          "self_attn.out_proj.weight": p["proj_w"], "self_attn.out_proj.bias": p["proj_b"],
+          "linear1.weight": p["fc_w"], "linear1.bias": p["fc_b"],
+          "linear2.weight": p["mlp_proj_w"], "linear2.bias": p["mlp_proj_b"],
+          "norm1.weight": p["ln1_g"], "norm1.bias": p["ln1_b"],
+          "norm2.weight": p["ln2_g"], "norm2.bias": p["ln2_b"]}
+    layer.load_state_dict({k: torch.from_numpy(np.ascontiguousarray(v)) for k, v in sd.items()})
+    layer.train(False)
+    mask = torch.nn.Transformer.generate_square_subsequent_mask(T, dtype=torch.float64)
+    with torch.no_grad():
+        ref = layer(torch.from_numpy(x), src_mask=mask, is_causal=True).numpy()
+    out = O.block_forward_postnorm(x, p, h, gelu_form=form)
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-11)
 
 
 def test_postnorm_block_causality():
