@@ -268,3 +268,24 @@ def forward(ids: np.ndarray, params: dict, n_head: int, past: np.ndarray | None 
     hf = layer_norm(h, params["lnf_g"], params["lnf_b"])
     logits = linear(hf, params["wte"], None)  # tied head, no bias
     return logits, np.stack(presents, axis=1)
+
+
+# --------------------------------------------------------------------------
+# Next-token cross-entropy and greedy choice on the logits
+# --------------------------------------------------------------------------
+def next_token_loss(logits: np.ndarray, targets: np.ndarray):
+    """Per position: the cross-entropy of the next token, -log softmax(z)[y] =
+    logsumexp(z) - z[y], and the greedy choice argmax(z) (the lowest index
+    among equal maxima).  ([FF] "Overview": training is next-token language
+    modelling of p(s_i | s_<i); "How it works": callers take the logits and a
+    next-token cross-entropy themselves.)  A negative target marks a position
+    without a loss (0).  logits [..., V], targets [...] int.
+    Returns (loss [...], argmax [...])."""
+    z = np.asarray(logits, np.float64)
+    y = np.asarray(targets)
+    m = z.max(axis=-1)
+    lse = m + np.log(np.exp(z - m[..., None]).sum(axis=-1))
+    safe = np.where(y >= 0, y, 0)
+    zy = np.take_along_axis(z, safe[..., None], axis=-1)[..., 0]
+    loss = np.where(y >= 0, lse - zy, 0.0)
+    return loss, np.argmax(z, axis=-1)

@@ -565,3 +565,37 @@ def test_planted_position_offset_mistake_is_caught(monkeypatch):
     monkeypatch.setattr(O, "embed", lambda ids, wte, wpe, t_past=0: orig(ids, wte, wpe, 0))
     with pytest.raises(AssertionError):
         test_cached_decode_equals_uncached()
+
+
+# ------------------------------------------------------- next-token loss ----
+def test_loss_closed_forms():
+    """Equal logits give log V; one logit c above V-1 equal others gives
+    log(1 + (V-1) e^-c) for that target and c + log(1 + (V-1) e^-c) for any
+    other; a negative target gives 0; the argmax is the lowest maximal index."""
+    V = 7
+    z = np.zeros((3, V))
+    z[1, 4] = 2.5
+    z[2, [2, 5]] = 1.0
+    loss, am = O.next_token_loss(z, np.array([3, 4, -1]))
+    np.testing.assert_allclose(loss[0], math.log(V), rtol=1e-15)
+    np.testing.assert_allclose(loss[1], math.log(1 + (V - 1) * math.exp(-2.5)), rtol=1e-14)
+    assert loss[2] == 0.0
+    loss2, _ = O.next_token_loss(z[1:2], np.array([0]))
+    np.testing.assert_allclose(loss2[0], 2.5 + math.log(1 + (V - 1) * math.exp(-2.5)), rtol=1e-14)
+    assert list(am) == [0, 4, 2]
+
+
+def test_loss_shift_invariance_and_library_special_case():
+    """Adding a constant to a row of logits changes neither the loss nor the
+    argmax; the values equal torch's cross_entropy (reduction none)."""
+    rng = _rng(27)
+    z = 3.0 * rng.standard_normal((4, 5, 50))
+    y = rng.integers(0, 50, size=(4, 5))
+    loss, am = O.next_token_loss(z, y)
+    loss2, am2 = O.next_token_loss(z + 100.0 * rng.standard_normal((4, 5, 1)), y)
+    np.testing.assert_allclose(loss2, loss, rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(am2, am)
+    ref = F.cross_entropy(torch.from_numpy(z.reshape(-1, 50)), torch.from_numpy(y.reshape(-1)),
+                          reduction="none").numpy().reshape(4, 5)
+    np.testing.assert_allclose(loss, ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(am, torch.from_numpy(z).argmax(-1).numpy())
