@@ -79,6 +79,8 @@ def _load() -> C.CDLL:
                                             P]),
         "gpt2_forward": (I, [P, P, I, I, C.POINTER(gpt2_params), I, C.POINTER(gpt2_kv),
                              C.POINTER(gpt2_kv), P, P]),
+        "gpt2_forward_loss": (I, [P, P, P, I, I, C.POINTER(gpt2_params), I, C.POINTER(gpt2_kv),
+                                  C.POINTER(gpt2_kv), P, P, P]),
         "gpt2_layer_norm": (I, [I, P, I, P, P, I, I, P, P]),
         "gpt2_linear": (I, [P, I, P, P, P, P, P, I, I, I, P]),
         "gpt2_attention": (I, [P, P, P, I, I, I, I, I, I, P, P]),
@@ -249,6 +251,25 @@ def gpt2_forward(ctx: Context, ids: torch.Tensor, params: ModelParams, B: int, T
     if present is not None:
         present.T_len = pr.T_len
     return logits
+
+
+def gpt2_forward_loss(ctx: Context, ids: torch.Tensor, params: ModelParams, B: int, T: int,
+                      targets: torch.Tensor | None = None, past: KV | None = None,
+                      present: KV | None = None, want_next: bool = True, stream=None):
+    """(loss [B, T] fp32 or None, next_ids [B, T] int32 or None) without the
+    logits; loss needs targets."""
+    loss = (torch.empty((B, T), dtype=torch.float32, device=ids.device)
+            if targets is not None else None)
+    nxt = torch.empty((B, T), dtype=torch.int32, device=ids.device) if want_next else None
+    ps = past.struct() if past is not None else None
+    pr = present.struct() if present is not None else None
+    _check(LIB.gpt2_forward_loss(ctx.handle, _ptr(ids), _ptr(targets), B, T, C.byref(params.struct),
+                                 params.n_layer, C.byref(ps) if ps is not None else None,
+                                 C.byref(pr) if pr is not None else None, _ptr(loss), _ptr(nxt),
+                                 _stream(stream)), "gpt2_forward_loss")
+    if present is not None:
+        present.T_len = pr.T_len
+    return loss, nxt
 
 
 def gpt2_generate_greedy(ctx: Context, ids: torch.Tensor, params: ModelParams, n_new: int,

@@ -77,10 +77,13 @@ __host__ __device__ constexpr int slot_bytes(int k) {
 // another (the most the two accumulators allow) never overwrites a buffer
 // still being read.
 __host__ __device__ constexpr int epi_warp_bytes(int k) {
-  return k == kEpiLogits ? 32 * kLogitsLd * 4 : k == kEpiLogitsT ? 0 : 2 * slot_bytes(k);
+  return k == kEpiLogits ? 32 * kLogitsLd * 4
+         : k == kEpiLogitsT ? 0
+         : k == kEpiHeadLoss ? 32 * 12  // its 32 tokens' (max, sum, index) partials
+                             : 2 * slot_bytes(k);
 }
 __host__ __device__ constexpr int epi_bias_bytes(int k) {
-  return k == kEpiLogits || k == kEpiLogitsT ? 0 : kBiasBytes;
+  return k == kEpiLogits || k == kEpiLogitsT || k == kEpiHeadLoss ? 0 : kBiasBytes;
 }
 
 struct GemmArgs {
@@ -217,7 +220,7 @@ __device__ __forceinline__ void epilogue_prefetch(int row0, int ncol0, int ncols
                                                   uint8_t* epi, uint16_t* bias_s, uint64_t* rbar,
                                                   EpiState& s, const GemmArgs& a,
                                                   const CUtensorMap* tmR) {
-  if constexpr (KIND != kEpiLogits && KIND != kEpiLogitsT) {
+  if constexpr (KIND != kEpiLogits && KIND != kEpiLogitsT && KIND != kEpiHeadLoss) {
     const int N = a.N;
     for (int j = 4 * lane; j < ncols; j += 128) {
       const int col = ncol0 + j;
@@ -249,6 +252,116 @@ __device__ __forceinline__ void epilogue_prefetch(int row0, int ncol0, int ncols
     if constexpr (KIND == kEpiResidBf16In) resid16_fetch(a, row0 + lane, ncol0, s.rnext);
     __syncwarp();
   }
+}
+
+// (m, s, i) <- the merge of two partials of a softmax normaliser: maxima m,
+// sums of 2^((z - m) log2 e), lowest index of the maximum.  -inf maxima (no
+// entry) merge without producing NaN.
+__device__ __forceinline__ void lse_merge(float& m, float& s, int& i, float m2, float s2, int i2) {
+  const bool take = m2 > m || (m2 == m && i2 < i);
+  const float hi = take ? m2 : m, lo = take ? m : m2;
+  const float s_hi = take ? s2 : s, s_lo = take ? s : s2;
+  i = take ? i2 : i;
+  m = hi;
+  s = s_hi + (lo == -INFINITY ? 0.f : s_lo * ex2((lo - hi) * 1.4426950408889634f));
+}
+
+// kEpiHeadLoss, one warp's share of a tile of the transposed head: its 32
+// vocabulary entries (TMEM lanes, rows row0 .. row0+31) x its token columns.
+// Per chunk of 32 tokens: the lane holding a token's target entry stores the
+// target logit; a five-round butterfly over the warp leaves lane j with token
+// j's (max, sum, index) over the warp's 32 entries; the four warps of the
+// column segment meet in shared memory (a bounded mbarrier handshake: `full`
+// counts the four slots written, `free` the quarter-0 warp done reading), and
+// the quarter-0 warp writes the partial of the CTA's 128-entry block.  cc
+// counts the warp's chunks across tiles (the barriers' phases).  Returns false
+// when a wait ran out.
+__device__ __forceinline__ bool head_loss_tile(uint32_t tbase, int row0, int ncol0, int ncols,
+                                               int lane, int quarter, uint8_t* seg_epi,
+                                               uint64_t* hl_full, uint64_t* hl_free, int& cc,
+                                               const GemmArgs& a, volatile int* abort_flag) {
+  const EpiParams& ep = a.ep;
+  const int M = a.M, N = a.N;  // vocabulary entries, tokens
+  const int v = row0 + lane;
+  const bool vok = v < M;
+  const int vblk = (row0 - quarter * 32) / kBM;
+  // A CTA whose 128 rows all lie past the vocabulary (the second CTA of a
+  // pair's last tile) has no block: it takes part in the handshake but
+  // writes nothing.
+  const bool blk_ok = vblk * kBM < M;
+  const int seg_end = min(ncols, N - ncol0);
+  for (int c = 0; c < seg_end; c += 32, ++cc) {
+    const int col = ncol0 + c;
+    const int nt = min(32, N - col);
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), r);
+    tmem_ld_wait();
+    if (ep.tgt && vok) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < nt && ep.tgt[col + j] == v) ep.tgt_logit[col + j] = __uint_as_float(r[j]);
+    }
+    float bm[32], bs[32];
+    int bi[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      bm[j] = vok ? __uint_as_float(r[j]) : -INFINITY;
+      bs[j] = vok ? 1.f : 0.f;
+      bi[j] = v;
+    }
+    // Round with offset o: a lane keeps the tokens whose bit o equals its own
+    // (slots [o, 2o) if set, [0, o) if not), sends the others to lane ^ o and
+    // merges what it receives into the kept slots, renumbered [0, o).
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const bool up = (lane & o) != 0;
+#pragma unroll
+      for (int k = 0; k < o; ++k) {
+        const float sm = up ? bm[k] : bm[k + o], ss = up ? bs[k] : bs[k + o];
+        const int si = up ? bi[k] : bi[k + o];
+        float km = up ? bm[k + o] : bm[k], ks = up ? bs[k + o] : bs[k];
+        int ki = up ? bi[k + o] : bi[k];
+        const float rm = __shfl_xor_sync(0xffffffffu, sm, o);
+        const float rs = __shfl_xor_sync(0xffffffffu, ss, o);
+        const int ri = __shfl_xor_sync(0xffffffffu, si, o);
+        lse_merge(km, ks, ki, rm, rs, ri);
+        bm[k] = km;
+        bs[k] = ks;
+        bi[k] = ki;
+      }
+    }
+    // Lane j now holds token col + j over this warp's entries.  The slots of
+    // the previous chunk must have been read before they are overwritten.
+    if (quarter != 0 && cc > 0 &&
+        !mbar_wait_bounded(hl_free, static_cast<uint32_t>(cc - 1) & 1u, abort_flag, a.err))
+      return false;
+    float* slot = reinterpret_cast<float*>(seg_epi + quarter * 32 * 12);
+    slot[lane] = bm[0];
+    slot[32 + lane] = bs[0];
+    reinterpret_cast<int*>(slot)[64 + lane] = bi[0];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(hl_full);
+    if (quarter == 0) {
+      if (!mbar_wait_bounded(hl_full, static_cast<uint32_t>(cc) & 1u, abort_flag, a.err))
+        return false;
+      float m = bm[0], sum = bs[0];
+      int idx = bi[0];
+#pragma unroll
+      for (int q = 1; q < 4; ++q) {
+        const float* sq = reinterpret_cast<const float*>(seg_epi + q * 32 * 12);
+        lse_merge(m, sum, idx, sq[lane], sq[32 + lane], reinterpret_cast<const int*>(sq)[64 + lane]);
+      }
+      if (blk_ok && lane < nt) {
+        const size_t o = static_cast<size_t>(vblk) * N + col + lane;
+        ep.part_m[o] = m;
+        ep.part_s[o] = sum;
+        ep.part_i[o] = idx;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(hl_free);
+    }
+  }
+  return true;
 }
 
 // Epilogue of one warp's share of a tile: rows row0 .. row0+31 (this thread:
@@ -521,7 +634,9 @@ __global__ void __launch_bounds__(epi_threads(KIND), 1)
       mbar_init(&tempty[i], kEpiWarps * CG);
     }
     mbar_init(mma_done, 1);
-    for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(&rbars[i], 1);
+    // (kEpiHeadLoss uses the first four as the segments' full / free pairs.)
+    for (int i = 0; i < 2 * kEpiWarps; ++i)
+      mbar_init(&rbars[i], KIND == kEpiHeadLoss && i < 2 ? 4 : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -659,6 +774,7 @@ __global__ void __launch_bounds__(epi_threads(KIND), 1)
     // The accumulator-drained barrier lives in the pair's first CTA.
     const uint32_t tempty_addr = CG == 2 ? mapa_shared(smem_u32(tempty), 0u) : 0u;
     int it = 0;
+    int hl_cc = 0;  // kEpiHeadLoss: chunks handled so far
     for (int tile = first_tile; tile < args.num_tiles; tile += tile_step, ++it) {
       const int acc = it & 1;
       const uint32_t acc_par = static_cast<uint32_t>((it >> 1) & 1);
@@ -672,8 +788,15 @@ __global__ void __launch_bounds__(epi_threads(KIND), 1)
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc * 256 + half * ncols);
-      epilogue_tile<KIND>(tbase, row0, ncol0, ncols, lane, epi, bias_s, rbar, st, args, &tmO,
-                          &tmR, &tmQ, &tmKV, abort_flag);
+      if constexpr (KIND == kEpiHeadLoss) {
+        if (!head_loss_tile(tbase, row0, ncol0, ncols, lane, quarter,
+                            sEpi + static_cast<size_t>(half) * 4 * epi_warp_bytes(KIND),
+                            &rbars[half], &rbars[2 + half], hl_cc, args, abort_flag))
+          break;
+      } else {
+        epilogue_tile<KIND>(tbase, row0, ncol0, ncols, lane, epi, bias_s, rbar, st, args, &tmO,
+                            &tmR, &tmQ, &tmKV, abort_flag);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -721,6 +844,7 @@ void* kernel_for(int kind, int cg) {
     case kEpiResidBf16Out: return kernel_ptr<kEpiResidBf16Out>(cg);
     case kEpiLogits: return kernel_ptr<kEpiLogits>(cg);
     case kEpiLogitsT: return kernel_ptr<kEpiLogitsT>(cg);
+    case kEpiHeadLoss: return kernel_ptr<kEpiHeadLoss>(cg);
     case kEpiQkv: return kernel_ptr<kEpiQkv>(cg);
     default: return nullptr;
   }
@@ -810,10 +934,12 @@ int choose_bn(int M, int N, int tile_rows, int units) {
 int launch_gemm_tc(const LaunchEnv& env, int kind_in, const void* A_in, const void* W_in,
                    int M_in, int N_in, int K, const EpiParams& ep, cudaStream_t stream,
                    double* flops, double* bytes, bool operands_f16, bool out_f16) {
-  if (M_in <= 0 || N_in <= 0 || K <= 0 || kind_in < 0 || kind_in >= kEpiLogitsT)
+  if (M_in <= 0 || N_in <= 0 || K <= 0 || kind_in < 0 || kind_in == kEpiLogitsT ||
+      kind_in >= kEpiCount)
     return GPT2_ERR_INVALID_ARG;
   if (K % 8 != 0) return GPT2_ERR_UNSUPPORTED;
-  if (kind_in != kEpiLogits && (N_in % 2 != 0)) return GPT2_ERR_UNSUPPORTED;
+  if (kind_in != kEpiLogits && kind_in != kEpiHeadLoss && (N_in % 2 != 0))
+    return GPT2_ERR_UNSUPPORTED;
   if (kind_in == kEpiQkv && (ep.d % 64 != 0 || N_in != 3 * ep.d)) return GPT2_ERR_UNSUPPORTED;
   // The tied head runs transposed, logits^T = W_e H^T: vocabulary entries on
   // the TMEM lanes and tokens on the columns, so the epilogue stores each
@@ -822,9 +948,9 @@ int launch_gemm_tc(const LaunchEnv& env, int kind_in, const void* A_in, const vo
   int kind = kind_in, M = M_in, N = N_in;
   const void* A = A_in;
   const void* W = W_in;
-  const bool transposed = kind_in == kEpiLogits;
+  const bool transposed = kind_in == kEpiLogits || kind_in == kEpiHeadLoss;
   if (transposed) {
-    kind = kEpiLogitsT;
+    if (kind_in == kEpiLogits) kind = kEpiLogitsT;
     std::swap(A, W);
     std::swap(M, N);
   }
@@ -833,7 +959,8 @@ int launch_gemm_tc(const LaunchEnv& env, int kind_in, const void* A_in, const vo
   // (measured on GB300: faster from K = 1600 up, no gain at K = 768), and for
   // the transposed head, whose 256-entry vocabulary tiles give each token row
   // 1 KB of contiguous logits per tile (GPT-2-small head 564 -> 542 us).
-  const int cg = (M > kBM && (K >= 1024 || kind == kEpiLogitsT) && env.num_sms >= 2) ? 2 : 1;
+  const int cg =
+      (M > kBM && (K >= 1024 || transposed) && env.num_sms >= 2) ? 2 : 1;
   void* fn = kernel_for(kind, cg);
   if (!fn) return GPT2_ERR_INVALID_ARG;
 
@@ -930,6 +1057,7 @@ int launch_gemm_tc(const LaunchEnv& env, int kind_in, const void* A_in, const vo
       case kEpiResidBf16In: b += 6.0 * mn + 2.0 * N; break;
       case kEpiResidBf16Out: b += 6.0 * mn + 2.0 * N; break;
       case kEpiLogits: b += 4.0 * mn; break;
+      case kEpiHeadLoss: b += 12.0 * mn / kBM; break;  // the per-block partials
     }
     *bytes = b;
   }

@@ -28,7 +28,7 @@ const char* kKindNames[kKindCount] = {
     "embed",          "layer_norm",        "gemm_c_attn",    "attention_prefill",
     "gemm_c_proj",    "gemm_c_fc",         "gemm_mlp_c_proj", "gemm_lm_head",
     "gemm_other",     "attention_decode",  "attention_decode_combine", "simt_fp32",
-    "argmax"};
+    "argmax",         "loss_combine"};
 
 struct ProfRec {
   int kind;
@@ -39,8 +39,12 @@ struct ProfRec {
 
 // Offsets (bytes) of the workspace regions.
 struct WsPlan {
-  size_t err, ln, q, kv, attn, resid, fc, partials, wconv, ids, total;
+  size_t err, ln, q, kv, attn, resid, fc, partials, wconv, ids, hloss, total;
 };
+
+// Vocabulary blocks of the fused head's per-token partials (128 entries each,
+// one per CTA tile of the transposed head).
+int loss_vblocks(const gpt2_hparams& hp) { return (hp.n_vocab + 127) / 128; }
 
 // fp16 working copies of the weights (bf16 mode): per layer slot, c_attn
 // [3d, d] at 0, c_proj [d, d] at 3d^2, c_fc [4d, d] at 4d^2, mlp c_proj
@@ -74,6 +78,11 @@ WsPlan plan_workspace(const gpt2_hparams& hp, int max_B, int max_T) {
                                               static_cast<size_t>(hp.n_vocab) * hp.n_embd)
                                        : 0);
   p.ids = take(static_cast<size_t>(max_B) * 4);  // greedy generation: the next token ids
+  // fused head + loss (bf16 mode): target logits [M], then the partials'
+  // maxima, sums and indices [vocab blocks][M]
+  p.hloss = take(hp.dtype == GPT2_BF16
+                     ? M * 4 * (1 + 3 * static_cast<size_t>(loss_vblocks(hp)))
+                     : 0);
   p.total = off;
   return p;
 }
@@ -696,9 +705,16 @@ int gpt2_block_forward_postnorm(gpt2_ctx* c, const void* x, const gpt2_block_par
   });
 }
 
-int gpt2_forward(gpt2_ctx* c, const int32_t* ids, int B, int T, const gpt2_params* params, int L,
-                 const gpt2_kv* past, gpt2_kv* present, float* logits, void* stream) {
-  if (!c || !ids || !params || !logits || !params->blocks) return GPT2_ERR_INVALID_ARG;
+namespace {
+
+// Everything of the full forward before the head: validation, the embedding,
+// the L blocks and LN_f into the workspace's `ln` rows (fp16 in bf16 mode);
+// *wte16 receives the tied embedding's fp16 copy (bf16 mode).  *t_past_out is
+// the position of the first new token.
+int forward_trunk(gpt2_ctx* c, const int32_t* ids, int B, int T, const gpt2_params* params, int L,
+                  const gpt2_kv* past, gpt2_kv* present, cudaStream_t s, const __half** wte16,
+                  int* t_past_out) {
+  if (!c || !ids || !params || !params->blocks) return GPT2_ERR_INVALID_ARG;
   if (L != c->hp.n_layer) return GPT2_ERR_INVALID_ARG;
   int st = check_ctx_shapes(c, B, T);
   if (st) return st;
@@ -710,12 +726,12 @@ int gpt2_forward(gpt2_ctx* c, const int32_t* ids, int B, int T, const gpt2_param
   for (int l = 0; l < L; ++l)
     if ((st = validate_block_params(&params->blocks[l]))) return st;
   if ((st = validate_kv(past, false)) || (st = validate_kv(present, true))) return st;
-  if (!aligned16(ids) || !aligned16(logits)) return GPT2_ERR_ALIGNMENT;
+  if (!aligned16(ids)) return GPT2_ERR_ALIGNMENT;
   const int t_past = past ? past->T_len : 0;
   if (t_past + T > c->hp.n_ctx) return GPT2_ERR_CTX_OVERFLOW;
   if (present && t_past + T > present->T_cap) return GPT2_ERR_CTX_OVERFLOW;
+  *t_past_out = t_past;
 
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   const gpt2_hparams& hp = c->hp;
   const int d = hp.n_embd, h = hp.n_head, dh = d / h, V = hp.n_vocab;
   const int M = B * T;
@@ -751,18 +767,33 @@ int gpt2_forward(gpt2_ctx* c, const int32_t* ids, int B, int T, const gpt2_param
   }
 
   // LN_f, with the tied embedding's fp16 conversion in the same launch
-  const __half* wte16 = nullptr;
+  *wte16 = nullptr;
   ConvSegs conv{};
-  if (bf) wte_conversion(c, params->wte, &wte16, &conv);
+  if (bf) wte_conversion(c, params->wte, wte16, &conv);
   void* ln = c->ws + c->plan.ln;
-  st = c->run(kKindLayerNorm, s, [&](double* fl, double* by) {
+  return c->run(kKindLayerNorm, s, [&](double* fl, double* by) {
     *fl = 0;
     *by = static_cast<double>(M) * d * (4 + es) + conversion_bytes(conv);
     return launch_layer_norm(hp.dtype, H, GPT2_FP32, params->lnf_g, params->lnf_b, M, d, ln, s,
                              bf, conv.count ? &conv : nullptr);
   });
-  if (st) return st;
+}
 
+}  // namespace
+
+int gpt2_forward(gpt2_ctx* c, const int32_t* ids, int B, int T, const gpt2_params* params, int L,
+                 const gpt2_kv* past, gpt2_kv* present, float* logits, void* stream) {
+  if (!c || !logits) return GPT2_ERR_INVALID_ARG;
+  if (!aligned16(logits)) return GPT2_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const __half* wte16 = nullptr;
+  int t_past = 0;
+  int st = forward_trunk(c, ids, B, T, params, L, past, present, s, &wte16, &t_past);
+  if (st) return st;
+  const gpt2_hparams& hp = c->hp;
+  const int d = hp.n_embd, dh = d / hp.n_head, V = hp.n_vocab, M = B * T;
+  const bool bf = hp.dtype == GPT2_BF16;
+  void* ln = c->ws + c->plan.ln;
   EpiParams e{};
   e.out = logits;
   e.ldo = V;
@@ -771,6 +802,46 @@ int gpt2_forward(gpt2_ctx* c, const int32_t* ids, int B, int T, const gpt2_param
       return gemm16(c, kEpiLogits, ln, wte16, M, V, d, e, false, s, fl, by);
     return launch_gemm_fp32(c->env, kEpiLogits, static_cast<const float*>(ln),
                             static_cast<const float*>(params->wte), M, V, d, e, dh, s);
+  });
+  if (st) return st;
+  if (present) present->T_len = t_past + T;
+  return GPT2_OK;
+}
+
+int gpt2_forward_loss(gpt2_ctx* c, const int32_t* ids, const int32_t* targets, int B, int T,
+                      const gpt2_params* params, int L, const gpt2_kv* past, gpt2_kv* present,
+                      float* loss, int32_t* next_ids, void* stream) {
+  if (!c || (!loss && !next_ids)) return GPT2_ERR_INVALID_ARG;
+  if (loss && !targets) return GPT2_ERR_INVALID_ARG;
+  if (c->hp.dtype != GPT2_BF16) return GPT2_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const __half* wte16 = nullptr;
+  int t_past = 0;
+  int st = forward_trunk(c, ids, B, T, params, L, past, present, s, &wte16, &t_past);
+  if (st) return st;
+  const gpt2_hparams& hp = c->hp;
+  const int d = hp.n_embd, V = hp.n_vocab, M = B * T;
+  const int nvb = loss_vblocks(hp);
+  float* tl = c->at<float>(c->plan.hloss);
+  float* pm = tl + M;
+  float* ps = pm + static_cast<size_t>(nvb) * M;
+  int32_t* pi = reinterpret_cast<int32_t*>(ps + static_cast<size_t>(nvb) * M);
+  EpiParams e{};
+  e.tgt = loss ? targets : nullptr;
+  e.tgt_logit = tl;
+  e.part_m = pm;
+  e.part_s = ps;
+  e.part_i = pi;
+  st = c->run(kKindGemmLogits, s, [&](double* fl, double* by) {
+    return launch_gemm_tc(c->env, kEpiHeadLoss, c->ws + c->plan.ln, wte16, M, V, d, e, s, fl,
+                          by, true, false);
+  });
+  if (st) return st;
+  st = c->run(kKindLossCombine, s, [&](double* fl, double* by) {
+    *fl = 0;
+    *by = 12.0 * nvb * M + 12.0 * M;
+    return launch_head_loss_combine(pm, ps, pi, nvb, M, V, loss ? targets : nullptr, tl, loss,
+                                    next_ids, c->env.err, s);
   });
   if (st) return st;
   if (present) present->T_len = t_past + T;

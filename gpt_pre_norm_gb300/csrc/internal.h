@@ -30,6 +30,7 @@ enum KernelKind : int {
   kKindDecodeCombine,
   kKindSimtFp32,
   kKindArgmax,
+  kKindLossCombine,
   kKindCount
 };
 
@@ -43,6 +44,7 @@ enum EpiKind : int {
   kEpiLogits,         // out_f32  = acc (no bias, N tail masked)
   kEpiQkv,            // acc + bias scattered to Q [B,h,T,64] and the K/V cache
   kEpiLogitsT,        // (internal) kEpiLogits computed as W A^T: TMEM lanes = vocabulary
+  kEpiHeadLoss,       // the tied head as in kEpiLogitsT, reduced to per-token partials
   kEpiCount
 };
 
@@ -65,6 +67,15 @@ struct EpiParams {
   KvDst kv;                 // K/V destination (kEpiQkv)
   int T;                    // tokens per sequence (kEpiQkv)
   int d;                    // model width (kEpiQkv)
+  // kEpiHeadLoss: per token t and vocabulary block j of 128 entries, the
+  // maximum logit part_m[j * n_tok + t], the sum over the block of
+  // 2^((z - max) log2 e) part_s[..], the lowest index of the maximum part_i[..];
+  // tgt_logit[t] = the logit of entry tgt[t] (written only for 0 <= tgt[t] < V).
+  const int32_t* tgt;
+  float* tgt_logit;
+  float* part_m;
+  float* part_s;
+  int32_t* part_i;
 };
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -117,6 +128,15 @@ int launch_layer_norm(int mode, const void* x, int x_dtype, const void* g, const
                       int d, void* y, cudaStream_t stream, bool y_f16 = false,
                       const ConvSegs* side = nullptr);
 
+
+// Per token t < n_tok: merges the n_vblk partials of kEpiHeadLoss into
+// logsumexp L and the argmax; loss[t] = L - tgt_logit[t] for 0 <= tgt[t] < V,
+// 0 for tgt[t] < 0 (NaN and the bad-token error bit for tgt[t] >= V);
+// next[t] = the argmax.  loss, next and tgt may be null.
+int launch_head_loss_combine(const float* part_m, const float* part_s, const int32_t* part_i,
+                             int n_vblk, int n_tok, int V, const int32_t* tgt,
+                             const float* tgt_logit, float* loss, int32_t* next, unsigned* err,
+                             cudaStream_t stream);
 
 // out[r * out_stride] = next[r] = argmax over the V values of row r (rows
 // row_stride apart); the lowest index among equal maxima.

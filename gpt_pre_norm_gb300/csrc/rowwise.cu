@@ -433,7 +433,73 @@ __global__ void __launch_bounds__(kRowThreads)
   }
 }
 
+// Next-token loss from the fused head's partials: 32 tokens per block (one per
+// lane), eight warps each merging every eighth vocabulary block (reads of 32
+// consecutive tokens' partials), then the eight results in shared memory.
+constexpr int kLossSlices = 8;
+
+__device__ __forceinline__ void lse_merge_rw(float& m, float& s, int& i, float m2, float s2,
+                                             int i2) {
+  const bool take = m2 > m || (m2 == m && i2 < i);
+  const float hi = take ? m2 : m, lo = take ? m : m2;
+  const float s_hi = take ? s2 : s, s_lo = take ? s : s2;
+  i = take ? i2 : i;
+  m = hi;
+  s = s_hi + (lo == -INFINITY ? 0.f : s_lo * exp2f((lo - hi) * 1.4426950408889634f));
+}
+
+__global__ void __launch_bounds__(32 * kLossSlices)
+    head_loss_combine(const float* __restrict__ pm, const float* __restrict__ ps,
+                      const int32_t* __restrict__ pi, int n_vblk, int n_tok, int V,
+                      const int32_t* __restrict__ tgt, const float* __restrict__ tl,
+                      float* __restrict__ loss, int32_t* __restrict__ next, unsigned* err) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float sm[kLossSlices][32], ss[kLossSlices][32];
+  __shared__ int si[kLossSlices][32];
+  const int lane = threadIdx.x & 31, slice = threadIdx.x >> 5;
+  const int t = blockIdx.x * 32 + lane;
+  float m = -INFINITY, sum = 0.f;
+  int idx = 0x7fffffff;
+  if (t < n_tok) {
+    for (int j = slice; j < n_vblk; j += kLossSlices) {
+      const size_t o = static_cast<size_t>(j) * n_tok + t;
+      lse_merge_rw(m, sum, idx, pm[o], ps[o], pi[o]);
+    }
+  }
+  sm[slice][lane] = m;
+  ss[slice][lane] = sum;
+  si[slice][lane] = idx;
+  __syncthreads();
+  if (slice != 0 || t >= n_tok) return;
+  for (int k = 1; k < kLossSlices; ++k) lse_merge_rw(m, sum, idx, sm[k][lane], ss[k][lane], si[k][lane]);
+  if (next) next[t] = idx < V ? idx : 0;  // all logits NaN: token 0
+  if (loss) {
+    const int y = tgt ? tgt[t] : -1;
+    if (y < 0) {
+      loss[t] = 0.f;
+    } else if (y >= V) {
+      loss[t] = __int_as_float(0x7fc00000);  // NaN
+      raise_error(err, kErrBadToken);
+    } else {
+      loss[t] = m + logf(sum) - tl[t];
+    }
+  }
+}
+
 }  // namespace
+
+int launch_head_loss_combine(const float* part_m, const float* part_s, const int32_t* part_i,
+                             int n_vblk, int n_tok, int V, const int32_t* tgt,
+                             const float* tgt_logit, float* loss, int32_t* next, unsigned* err,
+                             cudaStream_t stream) {
+  if (n_vblk <= 0 || n_tok <= 0 || V <= 0 || !part_m || !part_s || !part_i)
+    return GPT2_ERR_INVALID_ARG;
+  const cudaError_t e =
+      launch_pdl(head_loss_combine, dim3((n_tok + 31) / 32), dim3(32 * kLossSlices), 0, stream,
+                 part_m, part_s, part_i, n_vblk, n_tok, V, tgt, tgt_logit, loss, next, err);
+  return e == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+}
 
 int launch_layer_norm(int mode, const void* x, int x_dtype, const void* g, const void* b, int rows,
                       int d, void* y, cudaStream_t stream, bool y_f16, const ConvSegs* side) {

@@ -189,6 +189,23 @@ int gpt2_block_forward_postnorm(gpt2_ctx *ctx, const void *x, const gpt2_block_p
 int gpt2_forward(gpt2_ctx *ctx, const int32_t *ids, int B, int T, const gpt2_params *params, int L,
                  const gpt2_kv *past, gpt2_kv *present, float *logits, void *stream);
 
+/* The next-token loss of the full forward without the logits ("GPT-2 Full
+ * Forward Pass", "Overview": next-token language modelling of p(s_i | s_<i);
+ * "How it works": callers take the logits and a next-token cross-entropy).
+ * Runs as gpt2_forward up to LN_f, then reduces the tied head on the fly, per
+ * position t of [B, T]:
+ *   loss[t]     = logsumexp_v z[t, v] - z[t, targets[t]]  (0 where targets[t] < 0)
+ *   next_ids[t] = argmax_v z[t, v]  (the lowest index among equal maxima)
+ * without writing the [B, T, V] logits.  targets: device int32 [B, T] with
+ * entries in [0, n_vocab) or negative (required when loss is given); loss:
+ * device fp32 [B, T] or NULL; next_ids: device int32 [B, T] or NULL (not both
+ * NULL).  bf16 mode only (UNSUPPORTED in fp32 mode).  A target >= n_vocab
+ * gives a NaN loss and INVALID_ARG from gpt2_sync_status.  Other errors: as
+ * gpt2_forward.                                                             */
+int gpt2_forward_loss(gpt2_ctx *ctx, const int32_t *ids, const int32_t *targets, int B, int T,
+                      const gpt2_params *params, int L, const gpt2_kv *past, gpt2_kv *present,
+                      float *loss, int32_t *next_ids, void *stream);
+
 /* Greedy generation: the model's consumer ("GPT-2 Full Forward Pass": the
  * logits of the last position give the next token; greedy takes their
  * argmax, the lowest index among equal maxima).  Runs the prompt ids [B,

@@ -3,6 +3,7 @@
 import numpy as np
 import pytest
 import torch
+import torch.nn.functional as F
 
 from oracle import gpt2_oracle as O
 from gpt_pre_norm_gb300 import synthetic as S
@@ -306,6 +307,61 @@ def test_generate_greedy_graph_captured(G):
     T_all = 20 + n_new - 1
     assert_bf16_close(cache.data[..., :T_all, :].float().cpu().numpy(),
                       eager_cache.data[..., :T_all, :].float().cpu().numpy(), what="graph cache")
+
+
+@pytest.mark.parametrize("V,L,B,T", [(1000, 2, 2, 130), (50257, 1, 2, 64), (777, 1, 3, 1)])
+def test_forward_loss_without_logits(G, V, L, B, T):
+    """The fused head + next-token loss: against torch's cross-entropy on this
+    library's own logits (same products, so tight) and against the oracle
+    (bf16 tolerance); the greedy choices equal the logits' argmax.  V = 50257
+    leaves a ragged last block of 81 entries, V = 777 a small one."""
+    w = _small_model(n_layer=L, V=V)
+    p = S.model_params(w, seed=11)
+    rng = np.random.default_rng(11)
+    ids = rng.integers(0, V, size=(B, T)).astype(np.int32)
+    targets = rng.integers(0, V, size=(B, T)).astype(np.int32)
+    targets[0, 0] = -1  # no loss at this position
+    ctx = G.Context(w.n_vocab, w.n_ctx, w.d, w.n_head, w.n_layer, G.GPT2_BF16, B, T)
+    mp = G.ModelParams(model_to_device(p))
+    ids_d = dev(ids, torch.int32)
+    loss, nxt = G.gpt2_forward_loss(ctx, ids_d, mp, B, T, targets=dev(targets, torch.int32))
+    logits = G.gpt2_forward(ctx, ids_d, mp, B, T)
+    assert G.gpt2_sync_status(ctx) == 0
+    loss, nxt, logits = host(loss), nxt.cpu().numpy(), host(logits)
+    assert loss[0, 0] == 0.0
+    mine = F.cross_entropy(torch.from_numpy(logits.reshape(-1, V)).double(),
+                           torch.from_numpy(np.maximum(targets, 0).reshape(-1)).long(),
+                           reduction="none").numpy().reshape(B, T)
+    mine[0, 0] = 0.0
+    np.testing.assert_allclose(loss, mine, rtol=1e-5, atol=1e-4)
+    np.testing.assert_array_equal(nxt, logits.argmax(-1))
+    ref_logits, _ = O.forward(ids, p, w.n_head)
+    ref_loss, _ = O.next_token_loss(ref_logits, targets)
+    np.testing.assert_allclose(loss, ref_loss, rtol=2e-3, atol=5e-3)
+
+
+def test_forward_loss_cached_positions(G):
+    """With a cache, the loss covers the new positions only and equals the
+    uncached pass's loss there; present is filled as by gpt2_forward."""
+    w = _small_model(n_layer=2, V=1000)
+    p = S.model_params(w, seed=12)
+    B, T0, T1 = 2, 50, 30
+    rng = np.random.default_rng(12)
+    ids = rng.integers(0, 1000, size=(B, T0 + T1)).astype(np.int32)
+    targets = rng.integers(0, 1000, size=(B, T0 + T1)).astype(np.int32)
+    ctx = G.Context(w.n_vocab, w.n_ctx, w.d, w.n_head, w.n_layer, G.GPT2_BF16, B, T0 + T1)
+    mp = G.ModelParams(model_to_device(p))
+    full, _ = G.gpt2_forward_loss(ctx, dev(ids, torch.int32), mp, B, T0 + T1,
+                                  targets=dev(targets, torch.int32))
+    cache = _kv(G, B, w.n_head, 128, w.d_h, torch.bfloat16, L=w.n_layer)
+    G.gpt2_forward_loss(ctx, dev(ids[:, :T0], torch.int32), mp, B, T0,
+                        targets=dev(targets[:, :T0], torch.int32), present=cache)
+    part, nxt = G.gpt2_forward_loss(ctx, dev(ids[:, T0:], torch.int32), mp, B, T1,
+                                    targets=dev(targets[:, T0:], torch.int32), past=cache,
+                                    present=cache)
+    assert G.gpt2_sync_status(ctx) == 0
+    assert cache.T_len == T0 + T1
+    np.testing.assert_allclose(host(part), host(full)[:, T0:], rtol=1e-3, atol=5e-3)
 
 
 # ----------------------------------------------------------- error paths ----
