@@ -236,8 +236,18 @@ class Runner:
             ids = S.token_ids(w, seed)
             self.ids = torch.from_numpy(ids).to(device)
             self.ids_host = self.ids.cpu().pin_memory()
-            self.logits = torch.empty((w.B, w.T, w.n_vocab), dtype=torch.float32, device=device)
-            self.logits_host = torch.empty(self.logits.shape, dtype=torch.float32).pin_memory()
+            if w.kind == "forward_loss":
+                # targets: the next token of each sequence, none (-1) at the last position
+                tg = np.concatenate([ids[:, 1:], np.full((w.B, 1), -1, ids.dtype)], axis=1)
+                self.targets = torch.from_numpy(np.ascontiguousarray(tg)).to(device)
+                self.targets_host = self.targets.cpu().pin_memory()
+                self.loss_host = torch.empty((w.B, w.T), dtype=torch.float32).pin_memory()
+                self.loss = None
+            else:
+                self.logits = torch.empty((w.B, w.T, w.n_vocab), dtype=torch.float32,
+                                          device=device)
+                self.logits_host = torch.empty(self.logits.shape,
+                                               dtype=torch.float32).pin_memory()
             self.tokens = w.B * w.T
             self.cache = None
             if w.kind == "decode":
@@ -262,6 +272,9 @@ class Runner:
                                  out=self.out)
         elif w.kind == "forward":
             G.gpt2_forward(self.ctx, self.ids, self.mp, w.B, w.T, logits=self.logits)
+        elif w.kind == "forward_loss":
+            self.loss, _ = G.gpt2_forward_loss(self.ctx, self.ids, self.mp, w.B, w.T,
+                                               targets=self.targets, want_next=False)
         else:
             self.cache.T_len = w.t_past
             G.gpt2_forward(self.ctx, self.ids, self.mp, w.B, w.T, past=self.cache,
@@ -289,6 +302,11 @@ class Runner:
             self.x.copy_(self.x_host, non_blocking=True)
             self.run()
             self.out_host.copy_(self.out, non_blocking=True)
+        elif w.kind == "forward_loss":
+            self.ids.copy_(self.ids_host, non_blocking=True)
+            self.targets.copy_(self.targets_host, non_blocking=True)
+            self.run()
+            self.loss_host.copy_(self.loss, non_blocking=True)
         else:
             self.ids.copy_(self.ids_host, non_blocking=True)
             self.run()
@@ -298,6 +316,8 @@ class Runner:
         if self.w.kind == "block":
             n = self.x.numel() * self.x.element_size()
             return n, n
+        if self.w.kind == "forward_loss":
+            return self.ids.numel() * 8, self.loss_host.numel() * 4
         return self.ids.numel() * 4, self.logits.numel() * 4
 
 
@@ -345,9 +365,12 @@ def oracle_sample(w: S.Workload, seed: int, T_sample: int):
         return (lambda: O.block_forward(x, p, w.n_head)), T_sample
     p = S.model_params(w, seed)
     ids = S.token_ids(w, seed)[:1]
-    if w.kind == "forward":
+    if w.kind in ("forward", "forward_loss"):
         ids = ids[:, :T_sample]
-        return (lambda: O.forward(ids, p, w.n_head)), T_sample
+        if w.kind == "forward":
+            return (lambda: O.forward(ids, p, w.n_head)), T_sample
+        tg = np.concatenate([ids[:, 1:], np.full((1, 1), -1, ids.dtype)], axis=1)
+        return (lambda: O.next_token_loss(O.forward(ids, p, w.n_head)[0], tg)), T_sample
     past = np.stack([S.past_kv(w, seed, 0, layer) for layer in range(w.n_layer)])[None]
     return (lambda: O.forward(ids, p, w.n_head, past=past)), 1
 

@@ -57,6 +57,7 @@ constexpr int kOBuf = 32 * 32 * 2;            // bf16 32x32 box, rows of 64 B, 6
 constexpr int kBiasBufs = 3;                  // bias buffers per column segment, by tile index mod 3
 constexpr int kBiasBytes = kBiasBufs * 256 * 2;  // bf16 bias of a tile's columns, per buffer
 constexpr int kLogitsLd = 33;                 // logits transpose row stride (floats)
+constexpr int kHlPitch = 33;                  // head + loss tile: floats per vocabulary row
 
 static_assert(kRBuf % 1024 == 0 && kOBuf % 1024 == 0, "staging boxes must stay 1 KB aligned");
 
@@ -79,7 +80,7 @@ __host__ __device__ constexpr int slot_bytes(int k) {
 __host__ __device__ constexpr int epi_warp_bytes(int k) {
   return k == kEpiLogits ? 32 * kLogitsLd * 4
          : k == kEpiLogitsT ? 0
-         : k == kEpiHeadLoss ? 32 * 12  // its 32 tokens' (max, sum, index) partials
+         : k == kEpiHeadLoss ? 32 * kHlPitch * 4  // its quarter of the segment's tile
                              : 2 * slot_bytes(k);
 }
 __host__ __device__ constexpr int epi_bias_bytes(int k) {
@@ -268,97 +269,92 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, int& i, float m2, 
 
 // kEpiHeadLoss, one warp's share of a tile of the transposed head: its 32
 // vocabulary entries (TMEM lanes, rows row0 .. row0+31) x its token columns.
-// Per chunk of 32 tokens: the lane holding a token's target entry stores the
-// target logit; a five-round butterfly over the warp leaves lane j with token
-// j's (max, sum, index) over the warp's 32 entries; the four warps of the
-// column segment meet in shared memory (a bounded mbarrier handshake: `full`
-// counts the four slots written, `free` the quarter-0 warp done reading), and
-// the quarter-0 warp writes the partial of the CTA's 128-entry block.  cc
-// counts the warp's chunks across tiles (the barriers' phases).  Returns false
-// when a wait ran out.
+// Per chunk of 32 tokens the four warps of the column segment put their
+// 32 x 32 values into one shared [128 entries][32 tokens] tile (a bounded
+// mbarrier handshake: `full` counts the four warps' writes, `free` their
+// reads), then each warp reduces 8 of the tokens over the 128 entries, four
+// lanes per token (32 entries each: maximum and lowest index of it, then the
+// sum of 2^((z - max) log2 e)), merged by two shuffle rounds; the lane whose
+// entries hold a token's target stores the target logit.  cc counts the
+// warp's chunks across tiles (the barriers' phases).  Returns false when a
+// wait ran out.
 __device__ __forceinline__ bool head_loss_tile(uint32_t tbase, int row0, int ncol0, int ncols,
                                                int lane, int quarter, uint8_t* seg_epi,
                                                uint64_t* hl_full, uint64_t* hl_free, int& cc,
                                                const GemmArgs& a, volatile int* abort_flag) {
   const EpiParams& ep = a.ep;
   const int M = a.M, N = a.N;  // vocabulary entries, tokens
-  const int v = row0 + lane;
-  const bool vok = v < M;
-  const int vblk = (row0 - quarter * 32) / kBM;
+  const int blk0 = row0 - quarter * 32;        // the CTA's first entry
+  const int vblk = blk0 / kBM;
   // A CTA whose 128 rows all lie past the vocabulary (the second CTA of a
   // pair's last tile) has no block: it takes part in the handshake but
   // writes nothing.
-  const bool blk_ok = vblk * kBM < M;
+  const bool blk_ok = blk0 < M;
   const int seg_end = min(ncols, N - ncol0);
+  float* tile = reinterpret_cast<float*>(seg_epi);  // [128][kHlPitch]
+  // Reduction role: token 8 * quarter + (lane >> 2) of the chunk, entries
+  // g*32 .. g*32+31 of the block, g = lane & 3.
+  const int tk = 8 * quarter + (lane >> 2), g = lane & 3;
   for (int c = 0; c < seg_end; c += 32, ++cc) {
     const int col = ncol0 + c;
     const int nt = min(32, N - col);
     uint32_t r[32];
     tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), r);
-    tmem_ld_wait();
-    if (ep.tgt && vok) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < nt && ep.tgt[col + j] == v) ep.tgt_logit[col + j] = __uint_as_float(r[j]);
-    }
-    float bm[32], bs[32];
-    int bi[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      bm[j] = vok ? __uint_as_float(r[j]) : -INFINITY;
-      bs[j] = vok ? 1.f : 0.f;
-      bi[j] = v;
-    }
-    // Round with offset o: a lane keeps the tokens whose bit o equals its own
-    // (slots [o, 2o) if set, [0, o) if not), sends the others to lane ^ o and
-    // merges what it receives into the kept slots, renumbered [0, o).
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      const bool up = (lane & o) != 0;
-#pragma unroll
-      for (int k = 0; k < o; ++k) {
-        const float sm = up ? bm[k] : bm[k + o], ss = up ? bs[k] : bs[k + o];
-        const int si = up ? bi[k] : bi[k + o];
-        float km = up ? bm[k + o] : bm[k], ks = up ? bs[k + o] : bs[k];
-        int ki = up ? bi[k + o] : bi[k];
-        const float rm = __shfl_xor_sync(0xffffffffu, sm, o);
-        const float rs = __shfl_xor_sync(0xffffffffu, ss, o);
-        const int ri = __shfl_xor_sync(0xffffffffu, si, o);
-        lse_merge(km, ks, ki, rm, rs, ri);
-        bm[k] = km;
-        bs[k] = ks;
-        bi[k] = ki;
-      }
-    }
-    // Lane j now holds token col + j over this warp's entries.  The slots of
-    // the previous chunk must have been read before they are overwritten.
-    if (quarter != 0 && cc > 0 &&
+    // The tile's previous contents must have been read by all four warps.
+    if (cc > 0 &&
         !mbar_wait_bounded(hl_free, static_cast<uint32_t>(cc - 1) & 1u, abort_flag, a.err))
       return false;
-    float* slot = reinterpret_cast<float*>(seg_epi + quarter * 32 * 12);
-    slot[lane] = bm[0];
-    slot[32 + lane] = bs[0];
-    reinterpret_cast<int*>(slot)[64 + lane] = bi[0];
+    tmem_ld_wait();
+    float* my = tile + (quarter * 32 + lane) * kHlPitch;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) my[j] = __uint_as_float(r[j]);
     __syncwarp();
     if (lane == 0) mbar_arrive(hl_full);
-    if (quarter == 0) {
-      if (!mbar_wait_bounded(hl_full, static_cast<uint32_t>(cc) & 1u, abort_flag, a.err))
-        return false;
-      float m = bm[0], sum = bs[0];
-      int idx = bi[0];
+    if (!mbar_wait_bounded(hl_full, static_cast<uint32_t>(cc) & 1u, abort_flag, a.err))
+      return false;
+    float v[32];
 #pragma unroll
-      for (int q = 1; q < 4; ++q) {
-        const float* sq = reinterpret_cast<const float*>(seg_epi + q * 32 * 12);
-        lse_merge(m, sum, idx, sq[lane], sq[32 + lane], reinterpret_cast<const int*>(sq)[64 + lane]);
+    for (int i = 0; i < 32; ++i) v[i] = tile[(g * 32 + i) * kHlPitch + tk];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(hl_free);
+    // entries past the vocabulary do not count
+    const int e0 = blk0 + g * 32;
+    float m = -INFINITY;
+    int idx = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (e0 + i < M && v[i] > m) {
+        m = v[i];
+        idx = e0 + i;
       }
-      if (blk_ok && lane < nt) {
-        const size_t o = static_cast<size_t>(vblk) * N + col + lane;
-        ep.part_m[o] = m;
-        ep.part_s[o] = sum;
-        ep.part_i[o] = idx;
+    float sum = 0.f;
+    if (m != -INFINITY) {
+      const float ml = m * 1.4426950408889634f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (e0 + i < M) sum += ex2(fmaf(v[i], 1.4426950408889634f, -ml));
+    }
+    if (ep.tgt && tk < nt) {
+      const int y = ep.tgt[col + tk] - e0;
+      if (y >= 0 && y < 32 && e0 + y < M) {
+        float z = v[0];
+#pragma unroll
+        for (int i = 1; i < 32; ++i) z = y == i ? v[i] : z;
+        ep.tgt_logit[col + tk] = z;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(hl_free);
+    }
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+      lse_merge(m, sum, idx, m2, s2, i2);
+    }
+    if (blk_ok && g == 0 && tk < nt) {
+      const size_t o = static_cast<size_t>(vblk) * N + col + tk;
+      ep.part_m[o] = m;
+      ep.part_s[o] = sum;
+      ep.part_i[o] = idx;
     }
   }
   return true;
@@ -636,7 +632,7 @@ __global__ void __launch_bounds__(epi_threads(KIND), 1)
     mbar_init(mma_done, 1);
     // (kEpiHeadLoss uses the first four as the segments' full / free pairs.)
     for (int i = 0; i < 2 * kEpiWarps; ++i)
-      mbar_init(&rbars[i], KIND == kEpiHeadLoss && i < 2 ? 4 : 1);
+      mbar_init(&rbars[i], KIND == kEpiHeadLoss && i < 4 ? 4 : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }

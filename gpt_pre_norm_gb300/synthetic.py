@@ -35,7 +35,7 @@ BLOCK_TENSORS = ("ln1_g", "ln1_b", "attn_w", "attn_b", "proj_w", "proj_b",
 class Workload:
     """Shape and value distribution of one synthetic workload."""
     name: str
-    kind: str            # "block" | "forward" | "decode"
+    kind: str            # "block" | "forward" | "forward_loss" | "decode"
     dtype: str           # "bf16" | "fp32"
     d: int
     n_head: int
@@ -80,6 +80,11 @@ WORKLOADS = {
     "forward_bf16_gpt2_small": Workload("forward_bf16_gpt2_small", "forward", "bf16", d=768,
                                         n_head=12, B=8, T=1024, n_layer=12,
                                         resid_scale_layers=12),
+    # The same forward ending in the next-token loss instead of the logits
+    # (targets: the next token id, none at the last position).
+    "forward_loss_bf16_gpt2_small": Workload("forward_loss_bf16_gpt2_small", "forward_loss",
+                                             "bf16", d=768, n_head=12, B=8, T=1024, n_layer=12,
+                                             resid_scale_layers=12),
     # GPT-2-XL-shaped block.
     "block_bf16_d1600": Workload("block_bf16_d1600", "block", "bf16", d=1600, n_head=25, B=4,
                                  T=1024, resid_scale_layers=48),
