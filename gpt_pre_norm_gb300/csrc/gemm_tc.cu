@@ -315,32 +315,44 @@ __device__ __forceinline__ bool head_loss_tile(uint32_t tbase, int row0, int nco
     float v[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = tile[(g * 32 + i) * kHlPitch + tk];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(hl_free);
-    // entries past the vocabulary do not count
     const int e0 = blk0 + g * 32;
-    float m = -INFINITY;
-    int idx = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (e0 + i < M && v[i] > m) {
-        m = v[i];
-        idx = e0 + i;
-      }
-    float sum = 0.f;
-    if (m != -INFINITY) {
-      const float ml = m * 1.4426950408889634f;
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (e0 + i < M) sum += ex2(fmaf(v[i], 1.4426950408889634f, -ml));
-    }
     if (ep.tgt && tk < nt) {
       const int y = ep.tgt[col + tk] - e0;
-      if (y >= 0 && y < 32 && e0 + y < M) {
-        float z = v[0];
+      if (y >= 0 && y < 32 && e0 + y < M)
+        ep.tgt_logit[col + tk] = tile[(g * 32 + y) * kHlPitch + tk];
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(hl_free);
+    // Entries past the vocabulary (in the last block only) do not count.
+    float m = -INFINITY;
+    int idx = 0x7fffffff;
+    float sum = 0.f;
+    if (e0 + 32 <= M) {
+      int im = 0;
 #pragma unroll
-        for (int i = 1; i < 32; ++i) z = y == i ? v[i] : z;
-        ep.tgt_logit[col + tk] = z;
+      for (int i = 0; i < 32; ++i)
+        if (v[i] > m) {
+          m = v[i];
+          im = i;
+        }
+      idx = e0 + im;
+      const float ml = m * 1.4426950408889634f;
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < 32; ++i) s4[i & 3] += ex2(fmaf(v[i], 1.4426950408889634f, -ml));
+      sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (e0 + i < M && v[i] > m) {
+          m = v[i];
+          idx = e0 + i;
+        }
+      if (m != -INFINITY) {
+        const float ml = m * 1.4426950408889634f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (e0 + i < M) sum += ex2(fmaf(v[i], 1.4426950408889634f, -ml));
       }
     }
 #pragma unroll
