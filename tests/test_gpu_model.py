@@ -340,6 +340,32 @@ def test_forward_loss_without_logits(G, V, L, B, T):
     np.testing.assert_allclose(loss, ref_loss, rtol=2e-3, atol=5e-3)
 
 
+def test_forward_loss_bad_target_reported(G):
+    """A target outside the vocabulary yields a NaN loss at its position and
+    INVALID_ARG from the device error word; other positions are unaffected."""
+    w = _small_model(n_layer=1, V=500)
+    p = S.model_params(w, seed=13)
+    B, T = 2, 40
+    rng = np.random.default_rng(13)
+    ids = rng.integers(0, 500, size=(B, T)).astype(np.int32)
+    targets = rng.integers(0, 500, size=(B, T)).astype(np.int32)
+    ctx = G.Context(w.n_vocab, w.n_ctx, w.d, w.n_head, w.n_layer, G.GPT2_BF16, B, T)
+    mp = G.ModelParams(model_to_device(p))
+    good, _ = G.gpt2_forward_loss(ctx, dev(ids, torch.int32), mp, B, T,
+                                  targets=dev(targets, torch.int32))
+    assert G.gpt2_sync_status(ctx) == 0
+    bad_t = targets.copy()
+    bad_t[1, 7] = 500
+    bad, _ = G.gpt2_forward_loss(ctx, dev(ids, torch.int32), mp, B, T,
+                                 targets=dev(bad_t, torch.int32))
+    assert G.gpt2_sync_status(ctx) == G.GPT2_ERR_INVALID_ARG
+    bad, good = host(bad), host(good)
+    assert np.isnan(bad[1, 7])
+    mask = np.ones_like(bad, dtype=bool)
+    mask[1, 7] = False
+    np.testing.assert_array_equal(bad[mask], good[mask])
+
+
 def test_forward_loss_cached_positions(G):
     """With a cache, the loss covers the new positions only and equals the
     uncached pass's loss there; present is filled as by gpt2_forward."""
