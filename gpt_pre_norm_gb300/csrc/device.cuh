@@ -1,7 +1,8 @@
 // device.cuh -- inline-PTX helpers for sm_103a: mbarriers with bounded waits,
 // TMA tile loads and stores, tcgen05 (TMEM alloc, single-CTA and CTA-pair
-// UMMA issue/commit, K-major and MN-major shared-memory descriptors, TMEM
-// loads), cluster addressing, and small numeric helpers.
+// UMMA issue/commit with A from shared memory or from TMEM, K-major and
+// MN-major shared-memory descriptors, TMEM loads and stores), cluster
+// addressing, and small numeric helpers.
 #pragma once
 
 #include <cuda.h>
