@@ -66,6 +66,38 @@ def test_forward_full_size(G):
                           what=f"full-size present, layer {layer}")
 
 
+def test_forward_loss_full_size(G):
+    """The fused head + next-token loss at the benchmark's configuration (B=8,
+    T=1024, V=50257, targets = the next token, none at the last position):
+    every position against torch's cross-entropy on this library's own logits,
+    sequence 2 against the oracle's loss, and the greedy choices against the
+    logits' argmax."""
+    import torch.nn.functional as F
+    w = S.WORKLOADS["forward_loss_bf16_gpt2_small"]
+    seed = 0
+    p = S.model_params(w, seed)
+    ids = S.token_ids(w, seed)
+    targets = np.concatenate([ids[:, 1:], np.full((w.B, 1), -1, ids.dtype)], axis=1)
+    ctx = G.Context(w.n_vocab, w.n_ctx, w.d, w.n_head, w.n_layer, G.GPT2_BF16, w.B, w.T)
+    mp = G.ModelParams(model_to_device(p))
+    ids_d = dev(ids, torch.int32)
+    loss, nxt = G.gpt2_forward_loss(ctx, ids_d, mp, w.B, w.T, targets=dev(targets, torch.int32))
+    assert G.gpt2_sync_status(ctx) == G.GPT2_OK
+    loss, nxt = host(loss), nxt.cpu().numpy()
+    assert np.all(np.isfinite(loss)) and np.all(loss[:, -1] == 0.0)
+    for b in range(w.B):  # one sequence's logits at a time (1.65 GB for all of them)
+        lg = G.gpt2_forward(ctx, ids_d, mp, w.B, w.T)[b].double()
+        mine = F.cross_entropy(lg[:-1], torch.from_numpy(targets[b, :-1]).long().cuda(),
+                               reduction="none").cpu().numpy()
+        np.testing.assert_allclose(loss[b, :-1], mine, rtol=1e-5, atol=2e-4)
+        np.testing.assert_array_equal(nxt[b], lg.argmax(-1).cpu().numpy())
+        del lg
+    b = 2
+    ref_logits, _ = O.forward(ids[b:b + 1], p, w.n_head)
+    ref_loss, _ = O.next_token_loss(ref_logits, targets[b:b + 1])
+    np.testing.assert_allclose(loss[b], ref_loss[0], rtol=2e-3, atol=5e-3)
+
+
 def test_decode_full_size(G):
     """Cached single-token decode, GPT-2-medium shape, B=32, L=24, new token at
     position 1023 over a random past: sequences 0 and 31 against the oracle."""
