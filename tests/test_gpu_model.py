@@ -411,6 +411,10 @@ def test_errors_are_reported_before_launch(G):
     with pytest.raises(G.Gpt2Error) as e:
         G.gpt2_block_forward(ctx, x, p, 2, 64, w.d, 16)  # n_head differs from the context
     assert e.value.status == G.GPT2_ERR_INVALID_ARG
+    for B0, T0 in ((0, 64), (2, 0)):  # empty batch or sequence: rejected, nothing launched
+        with pytest.raises(G.Gpt2Error) as e:
+            G.gpt2_block_forward(ctx, x, p, B0, T0, w.d, w.n_head)
+        assert e.value.status == G.GPT2_ERR_INVALID_ARG
     xm = torch.empty(2 * 64 * w.d + 1, dtype=torch.bfloat16, device="cuda")[1:].view(2, 64, w.d)
     with pytest.raises(G.Gpt2Error) as e:
         G.gpt2_block_forward(ctx, xm, p, 2, 64, w.d, w.n_head)
