@@ -24,7 +24,9 @@
 //               V chunks go to their head-major destinations by 3-D TMA
 //               stores.  fp32 logits rows are only 4-byte aligned, so that
 //               epilogue transposes through shared memory and each store
-//               instruction writes one row's 32 consecutive columns.
+//               instruction writes one row's 32 consecutive columns.  The
+//               head reduced to the next-token loss writes no logits: each
+//               thread reduces its token's 128 entries of the tile.
 // Two accumulators let the epilogue of tile i overlap the mainloop of i+1.
 // Every mbarrier wait is bounded; a wait that runs out raises the context's
 // error word and the CTA drains its copies, frees TMEM and returns.
@@ -57,7 +59,7 @@ constexpr int kOBuf = 32 * 32 * 2;            // bf16 32x32 box, rows of 64 B, 6
 constexpr int kBiasBufs = 3;                  // bias buffers per column segment, by tile index mod 3
 constexpr int kBiasBytes = kBiasBufs * 256 * 2;  // bf16 bias of a tile's columns, per buffer
 constexpr int kLogitsLd = 33;                 // logits transpose row stride (floats)
-constexpr int kHlPitch = 33;                  // head + loss tile: floats per vocabulary row
+constexpr int kHlBlock = 128;                 // head + loss: vocabulary entries per partial
 
 static_assert(kRBuf % 1024 == 0 && kOBuf % 1024 == 0, "staging boxes must stay 1 KB aligned");
 
@@ -80,7 +82,7 @@ __host__ __device__ constexpr int slot_bytes(int k) {
 __host__ __device__ constexpr int epi_warp_bytes(int k) {
   return k == kEpiLogits ? 32 * kLogitsLd * 4
          : k == kEpiLogitsT ? 0
-         : k == kEpiHeadLoss ? 32 * kHlPitch * 4  // its quarter of the segment's tile
+         : k == kEpiHeadLoss ? 0
                              : 2 * slot_bytes(k);
 }
 __host__ __device__ constexpr int epi_bias_bytes(int k) {
@@ -255,121 +257,84 @@ __device__ __forceinline__ void epilogue_prefetch(int row0, int ncol0, int ncols
   }
 }
 
-// (m, s, i) <- the merge of two partials of a softmax normaliser: maxima m,
-// sums of 2^((z - m) log2 e), lowest index of the maximum.  -inf maxima (no
-// entry) merge without producing NaN.
-__device__ __forceinline__ void lse_merge(float& m, float& s, int& i, float m2, float s2, int i2) {
-  const bool take = m2 > m || (m2 == m && i2 < i);
-  const float hi = take ? m2 : m, lo = take ? m : m2;
-  const float s_hi = take ? s2 : s, s_lo = take ? s : s2;
-  i = take ? i2 : i;
-  m = hi;
-  s = s_hi + (lo == -INFINITY ? 0.f : s_lo * ex2((lo - hi) * 1.4426950408889634f));
-}
-
-// kEpiHeadLoss, one warp's share of a tile of the transposed head: its 32
-// vocabulary entries (TMEM lanes, rows row0 .. row0+31) x its token columns.
-// Per chunk of 32 tokens the four warps of the column segment put their
-// 32 x 32 values into one shared [128 entries][32 tokens] tile (a bounded
-// mbarrier handshake: `full` counts the four warps' writes, `free` their
-// reads), then each warp reduces 8 of the tokens over the 128 entries, four
-// lanes per token (32 entries each: maximum and lowest index of it, then the
-// sum of 2^((z - max) log2 e)), merged by two shuffle rounds; the lane whose
-// entries hold a token's target stores the target logit.  cc counts the
-// warp's chunks across tiles (the barriers' phases).  Returns false when a
-// wait ran out.
-__device__ __forceinline__ bool head_loss_tile(uint32_t tbase, int row0, int ncol0, int ncols,
-                                               int lane, int quarter, uint8_t* seg_epi,
-                                               uint64_t* hl_full, uint64_t* hl_free, int& cc,
-                                               const GemmArgs& a, volatile int* abort_flag) {
+// kEpiHeadLoss, one warp's share of a tile of the head: tokens on the TMEM
+// lanes (this thread: token row0 + lane), vocabulary entries on the columns
+// (this warp: the kHlBlock entries from ncol0).  Each thread reduces its
+// token's entries, 32 at a time, to the maximum, the lowest index of it and
+// the sum of 2^((z - max) log2 e), rescaling the sum when a later chunk
+// raises the maximum, and stores the block's partial; the thread whose
+// entries hold its token's target stores the target logit.  No data leaves
+// the thread: no shared memory, no shuffles.
+__device__ __forceinline__ void head_loss_rows(uint32_t tbase, int row0, int ncol0, int lane,
+                                               const GemmArgs& a) {
+  constexpr float kL2e = 1.4426950408889634f;
   const EpiParams& ep = a.ep;
-  const int M = a.M, N = a.N;  // vocabulary entries, tokens
-  const int blk0 = row0 - quarter * 32;        // the CTA's first entry
-  const int vblk = blk0 / kBM;
-  // A CTA whose 128 rows all lie past the vocabulary (the second CTA of a
-  // pair's last tile) has no block: it takes part in the handshake but
-  // writes nothing.
-  const bool blk_ok = blk0 < M;
-  const int seg_end = min(ncols, N - ncol0);
-  float* tile = reinterpret_cast<float*>(seg_epi);  // [128][kHlPitch]
-  // Reduction role: token 8 * quarter + (lane >> 2) of the chunk, entries
-  // g*32 .. g*32+31 of the block, g = lane & 3.
-  const int tk = 8 * quarter + (lane >> 2), g = lane & 3;
-  for (int c = 0; c < seg_end; c += 32, ++cc) {
-    const int col = ncol0 + c;
-    const int nt = min(32, N - col);
+  const int n_tok = a.M, V = a.N;
+  const int row = row0 + lane;
+  const bool row_ok = row < n_tok;
+  if (ncol0 >= V) return;  // a half tile past the vocabulary (warp-uniform)
+  const int y = (ep.tgt && row_ok) ? ep.tgt[row] : -1;
+  float m = -INFINITY, sum = 0.f;
+  int idx = 0x7fffffff;
+  for (int c = 0; c < kHlBlock; c += 32) {
+    const int col0 = ncol0 + c;
+    if (col0 >= V) break;  // warp-uniform
     uint32_t r[32];
     tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), r);
-    // The tile's previous contents must have been read by all four warps.
-    if (cc > 0 &&
-        !mbar_wait_bounded(hl_free, static_cast<uint32_t>(cc - 1) & 1u, abort_flag, a.err))
-      return false;
     tmem_ld_wait();
-    float* my = tile + (quarter * 32 + lane) * kHlPitch;
+    if (col0 + 32 > V) {  // the vocabulary's ragged end: entries past it do not count
 #pragma unroll
-    for (int j = 0; j < 32; ++j) my[j] = __uint_as_float(r[j]);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(hl_full);
-    if (!mbar_wait_bounded(hl_full, static_cast<uint32_t>(cc) & 1u, abort_flag, a.err))
-      return false;
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = tile[(g * 32 + i) * kHlPitch + tk];
-    const int e0 = blk0 + g * 32;
-    if (ep.tgt && tk < nt) {
-      const int y = ep.tgt[col + tk] - e0;
-      if (y >= 0 && y < 32 && e0 + y < M)
-        ep.tgt_logit[col + tk] = tile[(g * 32 + y) * kHlPitch + tk];
+      for (int i = 0; i < 32; ++i)
+        if (col0 + i >= V) r[i] = __float_as_uint(-INFINITY);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(hl_free);
-    // Entries past the vocabulary (in the last block only) do not count.
-    float m = -INFINITY;
-    int idx = 0x7fffffff;
-    float sum = 0.f;
-    if (e0 + 32 <= M) {
-      int im = 0;
+    if (y >= col0 && y < col0 + 32) {
+      float t = 0.f;
 #pragma unroll
       for (int i = 0; i < 32; ++i)
-        if (v[i] > m) {
-          m = v[i];
-          im = i;
-        }
-      idx = e0 + im;
-      const float ml = m * 1.4426950408889634f;
-      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+        if (i == y - col0) t = __uint_as_float(r[i]);
+      ep.tgt_logit[row] = t;
+    }
+    // Chunk maximum and its first index: four interleaved running maxima
+    // (strictly greater, so each keeps its first index), merged lowest index
+    // first on ties.
+    float cm[4];
+    int ci[4];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) s4[i & 3] += ex2(fmaf(v[i], 1.4426950408889634f, -ml));
-      sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-    } else {
+    for (int k = 0; k < 4; ++k) {
+      cm[k] = __uint_as_float(r[k]);
+      ci[k] = k;
+    }
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (e0 + i < M && v[i] > m) {
-          m = v[i];
-          idx = e0 + i;
-        }
-      if (m != -INFINITY) {
-        const float ml = m * 1.4426950408889634f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (e0 + i < M) sum += ex2(fmaf(v[i], 1.4426950408889634f, -ml));
+    for (int i = 4; i < 32; ++i) {
+      const float v = __uint_as_float(r[i]);
+      if (v > cm[i & 3]) {
+        cm[i & 3] = v;
+        ci[i & 3] = i;
       }
     }
 #pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-      const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
-      const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
-      lse_merge(m, sum, idx, m2, s2, i2);
+    for (int k = 1; k < 4; ++k)
+      if (cm[k] > cm[0] || (cm[k] == cm[0] && ci[k] < ci[0])) {
+        cm[0] = cm[k];
+        ci[0] = ci[k];
+      }
+    if (cm[0] > m) {  // a new maximum (strictly: earlier chunks keep ties)
+      sum = m == -INFINITY ? 0.f : sum * ex2((m - cm[0]) * kL2e);
+      m = cm[0];
+      idx = col0 + ci[0];
     }
-    if (blk_ok && g == 0 && tk < nt) {
-      const size_t o = static_cast<size_t>(vblk) * N + col + tk;
-      ep.part_m[o] = m;
-      ep.part_s[o] = sum;
-      ep.part_i[o] = idx;
-    }
+    const float ml = m * kL2e;
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 32; ++i) s4[i & 3] += ex2(fmaf(__uint_as_float(r[i]), kL2e, -ml));
+    sum += (s4[0] + s4[1]) + (s4[2] + s4[3]);
   }
-  return true;
+  if (row_ok) {
+    const size_t o = static_cast<size_t>(ncol0 / kHlBlock) * n_tok + row;
+    ep.part_m[o] = m;
+    ep.part_s[o] = sum;
+    ep.part_i[o] = idx;
+  }
 }
 
 // Epilogue of one warp's share of a tile: rows row0 .. row0+31 (this thread:
@@ -642,9 +607,7 @@ __global__ void __launch_bounds__(epi_threads(KIND), 1)
       mbar_init(&tempty[i], kEpiWarps * CG);
     }
     mbar_init(mma_done, 1);
-    // (kEpiHeadLoss uses the first four as the segments' full / free pairs.)
-    for (int i = 0; i < 2 * kEpiWarps; ++i)
-      mbar_init(&rbars[i], KIND == kEpiHeadLoss && i < 4 ? 4 : 1);
+    for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(&rbars[i], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -782,7 +745,6 @@ __global__ void __launch_bounds__(epi_threads(KIND), 1)
     // The accumulator-drained barrier lives in the pair's first CTA.
     const uint32_t tempty_addr = CG == 2 ? mapa_shared(smem_u32(tempty), 0u) : 0u;
     int it = 0;
-    int hl_cc = 0;  // kEpiHeadLoss: chunks handled so far
     for (int tile = first_tile; tile < args.num_tiles; tile += tile_step, ++it) {
       const int acc = it & 1;
       const uint32_t acc_par = static_cast<uint32_t>((it >> 1) & 1);
@@ -797,10 +759,7 @@ __global__ void __launch_bounds__(epi_threads(KIND), 1)
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc * 256 + half * ncols);
       if constexpr (KIND == kEpiHeadLoss) {
-        if (!head_loss_tile(tbase, row0, ncol0, ncols, lane, quarter,
-                            sEpi + static_cast<size_t>(half) * 4 * epi_warp_bytes(KIND),
-                            &rbars[half], &rbars[2 + half], hl_cc, args, abort_flag))
-          break;
+        head_loss_rows(tbase, row0, ncol0, lane, args);
       } else {
         epilogue_tile<KIND>(tbase, row0, ncol0, ncols, lane, epi, bias_s, rbar, st, args, &tmO,
                             &tmR, &tmQ, &tmKV, abort_flag);
@@ -949,14 +908,18 @@ int launch_gemm_tc(const LaunchEnv& env, int kind_in, const void* A_in, const vo
   if (kind_in != kEpiLogits && kind_in != kEpiHeadLoss && (N_in % 2 != 0))
     return GPT2_ERR_UNSUPPORTED;
   if (kind_in == kEpiQkv && (ep.d % 64 != 0 || N_in != 3 * ep.d)) return GPT2_ERR_UNSUPPORTED;
-  // The tied head runs transposed, logits^T = W_e H^T: vocabulary entries on
-  // the TMEM lanes and tokens on the columns, so the epilogue stores each
-  // token's logits row segment straight from registers; the tile index runs
-  // over token blocks first, so each block of W_e is streamed from HBM once.
+  // The tied head that writes logits runs transposed, logits^T = W_e H^T:
+  // vocabulary entries on the TMEM lanes and tokens on the columns, so the
+  // epilogue stores each token's logits row segment straight from registers;
+  // the tile index runs over token blocks first, so each block of W_e is
+  // streamed from HBM once.  The head reduced to the loss keeps tokens on the
+  // lanes (each thread reduces its own token's entries); its tile index runs
+  // over token blocks first by the default order, with the same effect.
   int kind = kind_in, M = M_in, N = N_in;
   const void* A = A_in;
   const void* W = W_in;
-  const bool transposed = kind_in == kEpiLogits || kind_in == kEpiHeadLoss;
+  const bool transposed = kind_in == kEpiLogits;
+  const bool head = transposed || kind_in == kEpiHeadLoss;
   if (transposed) {
     if (kind_in == kEpiLogits) kind = kEpiLogitsT;
     std::swap(A, W);
@@ -968,12 +931,14 @@ int launch_gemm_tc(const LaunchEnv& env, int kind_in, const void* A_in, const vo
   // the transposed head, whose 256-entry vocabulary tiles give each token row
   // 1 KB of contiguous logits per tile (GPT-2-small head 564 -> 542 us).
   const int cg =
-      (M > kBM && (K >= 1024 || transposed) && env.num_sms >= 2) ? 2 : 1;
+      (M > kBM && (K >= 1024 || head) && env.num_sms >= 2) ? 2 : 1;
   void* fn = kernel_for(kind, cg);
   if (!fn) return GPT2_ERR_INVALID_ARG;
 
   const int units = cg == 2 ? env.num_sms / 2 : env.num_sms;
-  const int BN = choose_bn(M, N, kBM * cg, units);
+  // The loss epilogue's partials cover kHlBlock entries: one half of a
+  // 256-wide tile per column segment.
+  const int BN = kind == kEpiHeadLoss ? 2 * kHlBlock : choose_bn(M, N, kBM * cg, units);
   int stages = kMaxStages;
   while (stages > 2 && smem_bytes_for(kind, BN, stages, cg) > static_cast<size_t>(kSmemLimit))
     --stages;

@@ -44,7 +44,7 @@ enum EpiKind : int {
   kEpiLogits,         // out_f32  = acc (no bias, N tail masked)
   kEpiQkv,            // acc + bias scattered to Q [B,h,T,64] and the K/V cache
   kEpiLogitsT,        // (internal) kEpiLogits computed as W A^T: TMEM lanes = vocabulary
-  kEpiHeadLoss,       // the tied head as in kEpiLogitsT, reduced to per-token partials
+  kEpiHeadLoss,       // the tied head (tokens on TMEM lanes) reduced to per-token partials
   kEpiCount
 };
 
