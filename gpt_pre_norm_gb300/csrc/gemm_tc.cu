@@ -26,7 +26,7 @@
 //               epilogue transposes through shared memory and each store
 //               instruction writes one row's 32 consecutive columns.  The
 //               head reduced to the next-token loss writes no logits: each
-//               thread reduces its token's 128 entries of the tile.
+//               thread reduces its token's 256 entries of the tile.
 // Two accumulators let the epilogue of tile i overlap the mainloop of i+1.
 // Every mbarrier wait is bounded; a wait that runs out raises the context's
 // error word and the CTA drains its copies, frees TMEM and returns.
@@ -48,7 +48,9 @@ constexpr int kBK = 64;                       // one 128-byte swizzle row of bf1
 // (measured on GB300 for the block's mlp c_proj: GPT-2-small 43.3 -> 41.2 us,
 // GPT-2-XL shape 80 -> 70 us with four; the in-place fp32 residual epilogue
 // is faster with eight).
-__host__ __device__ constexpr int epi_warps(int k) { return k == kEpiResidBf16Out ? 4 : 8; }
+__host__ __device__ constexpr int epi_warps(int k) {
+  return k == kEpiResidBf16Out || k == kEpiHeadLoss ? 4 : 8;
+}
 __host__ __device__ constexpr int epi_threads(int k) { return 128 + 32 * epi_warps(k); }
 constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB per A slot
 constexpr int kMaxStages = 8;
@@ -59,7 +61,6 @@ constexpr int kOBuf = 32 * 32 * 2;            // bf16 32x32 box, rows of 64 B, 6
 constexpr int kBiasBufs = 3;                  // bias buffers per column segment, by tile index mod 3
 constexpr int kBiasBytes = kBiasBufs * 256 * 2;  // bf16 bias of a tile's columns, per buffer
 constexpr int kLogitsLd = 33;                 // logits transpose row stride (floats)
-constexpr int kHlBlock = 128;                 // head + loss: vocabulary entries per partial
 
 static_assert(kRBuf % 1024 == 0 && kOBuf % 1024 == 0, "staging boxes must stay 1 KB aligned");
 
@@ -259,7 +260,7 @@ __device__ __forceinline__ void epilogue_prefetch(int row0, int ncol0, int ncols
 
 // kEpiHeadLoss, one warp's share of a tile of the head: tokens on the TMEM
 // lanes (this thread: token row0 + lane), vocabulary entries on the columns
-// (this warp: the kHlBlock entries from ncol0).  Each thread reduces its
+// (this warp: the kHeadLossBlock entries from ncol0, the whole tile).  Each thread reduces its
 // token's entries, 32 at a time, to the maximum, the lowest index of it and
 // the sum of 2^((z - max) log2 e), rescaling the sum when a later chunk
 // raises the maximum, and stores the block's partial; the thread whose
@@ -276,7 +277,7 @@ __device__ __forceinline__ void head_loss_rows(uint32_t tbase, int row0, int nco
   const int y = (ep.tgt && row_ok) ? ep.tgt[row] : -1;
   float m = -INFINITY, sum = 0.f;
   int idx = 0x7fffffff;
-  for (int c = 0; c < kHlBlock; c += 32) {
+  for (int c = 0; c < kHeadLossBlock; c += 32) {
     const int col0 = ncol0 + c;
     if (col0 >= V) break;  // warp-uniform
     uint32_t r[32];
@@ -330,7 +331,7 @@ __device__ __forceinline__ void head_loss_rows(uint32_t tbase, int row0, int nco
     sum += (s4[0] + s4[1]) + (s4[2] + s4[3]);
   }
   if (row_ok) {
-    const size_t o = static_cast<size_t>(ncol0 / kHlBlock) * n_tok + row;
+    const size_t o = static_cast<size_t>(ncol0 / kHeadLossBlock) * n_tok + row;
     ep.part_m[o] = m;
     ep.part_s[o] = sum;
     ep.part_i[o] = idx;
@@ -936,9 +937,8 @@ int launch_gemm_tc(const LaunchEnv& env, int kind_in, const void* A_in, const vo
   if (!fn) return GPT2_ERR_INVALID_ARG;
 
   const int units = cg == 2 ? env.num_sms / 2 : env.num_sms;
-  // The loss epilogue's partials cover kHlBlock entries: one half of a
-  // 256-wide tile per column segment.
-  const int BN = kind == kEpiHeadLoss ? 2 * kHlBlock : choose_bn(M, N, kBM * cg, units);
+  // The loss epilogue's partials cover one whole tile's kHeadLossBlock entries.
+  const int BN = kind == kEpiHeadLoss ? kHeadLossBlock : choose_bn(M, N, kBM * cg, units);
   int stages = kMaxStages;
   while (stages > 2 && smem_bytes_for(kind, BN, stages, cg) > static_cast<size_t>(kSmemLimit))
     --stages;
@@ -1030,7 +1030,7 @@ int launch_gemm_tc(const LaunchEnv& env, int kind_in, const void* A_in, const vo
       case kEpiResidBf16In: b += 6.0 * mn + 2.0 * N; break;
       case kEpiResidBf16Out: b += 6.0 * mn + 2.0 * N; break;
       case kEpiLogits: b += 4.0 * mn; break;
-      case kEpiHeadLoss: b += 12.0 * mn / kBM; break;  // the per-block partials
+      case kEpiHeadLoss: b += 12.0 * mn / kHeadLossBlock; break;  // the per-block partials
     }
     *bytes = b;
   }

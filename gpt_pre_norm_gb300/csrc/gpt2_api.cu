@@ -42,9 +42,11 @@ struct WsPlan {
   size_t err, ln, q, kv, attn, resid, fc, partials, wconv, ids, hloss, total;
 };
 
-// Vocabulary blocks of the fused head's per-token partials (128 entries each,
-// one per CTA tile of the transposed head).
-int loss_vblocks(const gpt2_hparams& hp) { return (hp.n_vocab + 127) / 128; }
+// Vocabulary blocks of the fused head's per-token partials (kHeadLossBlock
+// entries each, one per tile of the head).
+int loss_vblocks(const gpt2_hparams& hp) {
+  return (hp.n_vocab + kHeadLossBlock - 1) / kHeadLossBlock;
+}
 
 // fp16 working copies of the weights (bf16 mode): per layer slot, c_attn
 // [3d, d] at 0, c_proj [d, d] at 3d^2, c_fc [4d, d] at 4d^2, mlp c_proj

@@ -58,6 +58,10 @@ struct KvDst {
   int t_past;         // first position written
 };
 
+// Vocabulary entries per partial of the head reduced to the loss (one
+// 256-wide tile of the head per token).
+constexpr int kHeadLossBlock = 256;
+
 struct EpiParams {
   const void* bias;         // [N], mode dtype
   const void* resid;        // [M, ldo] (fp32 or bf16 by kind)
@@ -67,7 +71,7 @@ struct EpiParams {
   KvDst kv;                 // K/V destination (kEpiQkv)
   int T;                    // tokens per sequence (kEpiQkv)
   int d;                    // model width (kEpiQkv)
-  // kEpiHeadLoss: per token t and vocabulary block j of 128 entries, the
+  // kEpiHeadLoss: per token t and vocabulary block j of kHeadLossBlock entries, the
   // maximum logit part_m[j * n_tok + t], the sum over the block of
   // 2^((z - max) log2 e) part_s[..], the lowest index of the maximum part_i[..];
   // tgt_logit[t] = the logit of entry tgt[t] (written only for 0 <= tgt[t] < V).

@@ -434,9 +434,10 @@ __global__ void __launch_bounds__(kRowThreads)
 }
 
 // Next-token loss from the fused head's partials: 32 tokens per block (one per
-// lane), eight warps each merging every eighth vocabulary block (reads of 32
-// consecutive tokens' partials), then the eight results in shared memory.
-constexpr int kLossSlices = 8;
+// lane), kLossSlices warps each merging every kLossSlices-th vocabulary block
+// (reads of 32 consecutive tokens' partials), then their results in shared
+// memory.
+constexpr int kLossSlices = 16;
 
 __device__ __forceinline__ void lse_merge_rw(float& m, float& s, int& i, float m2, float s2,
                                              int i2) {
