@@ -26,7 +26,11 @@ One JSON line is printed by rank 0.  Beside the device-timed value it carries:
               bytes per launch over its CUDA-event duration, measured in a
               second, profiled pass of K steps) against the measured peak;
   cpu_baseline  the fp64 oracle timed on the host cores on a bounded sample;
-  clocks      SM clocks and throttle reasons sampled during the timed steps.
+  clocks      SM clocks and throttle reasons sampled during the timed steps;
+  ms_per_step_median  the median of the K step times (ms_per_step is their
+              mean);
+  eager_ms_per_step  for the graph-replayed decode step, the same step with
+              its kernels launched one by one.
 --impl reference times the oracle itself as the reference arm.
 """
 from __future__ import annotations
@@ -488,6 +492,14 @@ def main():
     with ClockSampler(torch.cuda.current_device()) as clk:
         times = timed_steps(r.run, args.steps, flush, barrier, torch)
     ms = sum(times) / len(times)
+    ms_med = statistics.median(times)
+
+    # A graph-replayed workload (decode) is also timed launching its kernels
+    # one by one, for the graph's gain.
+    ms_eager = None
+    if r.graph is not None:
+        times_eager = timed_steps(r.step, args.steps, flush, barrier, torch)
+        ms_eager = sum(times_eager) / len(times_eager)
 
     # End to end through the C ABI: pinned host buffers, copies inside the step.
     times_e2e = timed_steps(r.step_e2e, args.steps, flush, barrier, torch)
@@ -503,7 +515,9 @@ def main():
     if st != G.GPT2_OK:
         raise SystemExit(f"device error in the timed region: {G.status_string(st)}")
 
-    ms, ms_e2e = reduce_over_ranks([ms, ms_e2e], device)
+    ms, ms_e2e, ms_med = reduce_over_ranks([ms, ms_e2e, ms_med], device)
+    if ms_eager is not None:
+        ms_eager = reduce_over_ranks([ms_eager], device)[0]
     if rank != 0:
         return 0
 
@@ -545,7 +559,8 @@ def main():
     launches = sum(v["launches"] for v in prof.values())
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_median": ms_med,
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": workload_config(w, args),
         "tflops": flops * ws / (ms / 1e3) / 1e12,
@@ -559,6 +574,8 @@ def main():
         "clocks": clk.summary(),
         "kernels": kernels,
     }
+    if ms_eager is not None:
+        line["eager_ms_per_step"] = ms_eager  # the same step without the CUDA graph
     if not args.no_cpu_baseline and ws == 1:
         line["cpu_baseline"] = time_oracle(w, args.seed)
     print(json.dumps(line), flush=True)
