@@ -103,3 +103,28 @@ def test_ctx_create_rejects_small_or_misaligned_workspace(G):
     G.LIB.gpt2_workspace_bytes(C.byref(_hp(G)), 2, 8, C.byref(n))
     assert G.LIB.gpt2_ctx_create(C.byref(_hp(G)), 2, 8, 0x10010, n.value, C.byref(h)) == G.GPT2_ERR_ALIGNMENT
     assert G.LIB.gpt2_ctx_create(C.byref(_hp(G)), 2, 8, 0x10000, n.value - 1, C.byref(h)) == G.GPT2_ERR_WORKSPACE
+
+
+def test_noalloc_decode_validates_on_the_host(G):
+    # Every check below returns before the device is touched (fake, never
+    # dereferenced 16-byte aligned addresses; no GPU needed).
+    f = G.LIB.gpt2_attention_decode_noalloc
+    a16, bad = 0x10000, 0x10004
+    assert f(None, a16, 1, 4, 10, 16, 64, 0, a16, None) == G.GPT2_ERR_INVALID_ARG
+    assert f(a16, a16, 0, 4, 10, 16, 64, 0, a16, None) == G.GPT2_ERR_INVALID_ARG    # B = 0
+    assert f(a16, a16, 1, 4, 0, 16, 64, 0, a16, None) == G.GPT2_ERR_INVALID_ARG     # no past
+    assert f(a16, a16, 1, 4, 10, 16, 64, -1, a16, None) == G.GPT2_ERR_INVALID_ARG   # splits < 0
+    assert f(a16, a16, 1, 4, 10, 16, 32, 0, a16, None) == G.GPT2_ERR_UNSUPPORTED    # d_h != 64
+    assert f(a16, a16, 1, 4, 16, 16, 64, 0, a16, None) == G.GPT2_ERR_CTX_OVERFLOW   # T_past + 1 > T_cap
+    assert f(bad, a16, 1, 4, 10, 16, 64, 0, a16, None) == G.GPT2_ERR_ALIGNMENT
+
+
+def test_profiler_kinds_and_null_context(G):
+    n = G.LIB.gpt2_profile_kinds()
+    assert n >= 8  # embed, LayerNorm, four block products, head, attention, ...
+    name = C.c_char_p()
+    ll, d1, d2, d3 = C.c_longlong(), C.c_double(), C.c_double(), C.c_double()
+    assert G.LIB.gpt2_profile_read(None, 0, C.byref(name), C.byref(ll), C.byref(d1), C.byref(d2),
+                                   C.byref(d3)) == G.GPT2_ERR_INVALID_ARG
+    assert G.LIB.gpt2_profile_reset(None) == G.GPT2_ERR_INVALID_ARG
+    assert G.LIB.gpt2_selftest_wait_timeout(None, 1000, None) == G.GPT2_ERR_INVALID_ARG
