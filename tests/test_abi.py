@@ -128,3 +128,16 @@ def test_profiler_kinds_and_null_context(G):
                                    C.byref(d3)) == G.GPT2_ERR_INVALID_ARG
     assert G.LIB.gpt2_profile_reset(None) == G.GPT2_ERR_INVALID_ARG
     assert G.LIB.gpt2_selftest_wait_timeout(None, 1000, None) == G.GPT2_ERR_INVALID_ARG
+
+
+def test_binding_refuses_to_load_without_the_library():
+    # No fallback: with the library missing, importing the binding raises.
+    import subprocess
+    import sys
+    code = ("import gpt_pre_norm_gb300.build as b; b.LIB = '/nonexistent/libgpt2fwd.so'\n"
+            "try:\n    import gpt_pre_norm_gb300.binding\nexcept ImportError as e:\n"
+            "    print('refused:', 'no fallback' in str(e))\nelse:\n    print('loaded')\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == "refused: True"
