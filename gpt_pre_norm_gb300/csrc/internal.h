@@ -74,7 +74,9 @@ struct EpiParams {
   // kEpiHeadLoss: per token t and vocabulary block j of kHeadLossBlock entries, the
   // maximum logit part_m[j * n_tok + t], the sum over the block of
   // 2^((z - max) log2 e) part_s[..], the lowest index of the maximum part_i[..];
-  // tgt_logit[t] = the logit of entry tgt[t] (written only for 0 <= tgt[t] < V).
+  // tgt_logit[t] = the logit of entry tgt[t] for 0 <= tgt[t] < V (a target
+  // past V may leave -inf there, which the combine ignores: it reports the
+  // target as bad).
   const int32_t* tgt;
   float* tgt_logit;
   float* part_m;
