@@ -19,9 +19,15 @@ replica of the workload (the forward has no cross-sequence exchange), so the
 whole-job value is the sum of the ranks' tokens over the slowest rank's time.
 
 One JSON line is printed by rank 0.  Beside the device-timed value it carries:
-  e2e         the same metric through the C ABI with pinned host buffers, the
-              host->device copy of the inputs and the device->host copy of the
-              result inside each timed step;
+  e2e         the same metric through the C ABI with pinned host buffers: every
+              step copies its input from pinned host memory and its result
+              back; steps are pipelined over two device buffers (copies on
+              their own streams overlap the previous step's compute) and the
+              L2 flush runs inside the timed region;
+  workloads   the other configurations timed in the same run (the full
+              GPT-2-small forward, the GPT-2-XL-shaped block, cached decode
+              of the GPT-2-medium shape), each with its step time, tokens/s,
+              end-to-end roofline fraction, top kernel and clock sample;
   roofline    the dominant kernel's achieved rate (its algorithmic flops or
               bytes per launch over its CUDA-event duration, measured in a
               second, profiled pass of K steps) against the measured peak;
@@ -42,12 +48,14 @@ import os
 os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
 
 import argparse  # noqa: E402
+import gc  # noqa: E402
 import hashlib  # noqa: E402
 import json  # noqa: E402
 import statistics  # noqa: E402
 import subprocess  # noqa: E402
 import sys  # noqa: E402
 import time  # noqa: E402
+from concurrent.futures import ThreadPoolExecutor  # noqa: E402
 
 import numpy as np  # noqa: E402
 
@@ -62,6 +70,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 TENSOR_KINDS = {"gemm_c_attn", "gemm_c_proj", "gemm_c_fc", "gemm_mlp_c_proj", "gemm_lm_head",
                 "gemm_other", "attention_prefill"}
 L2_FLUSH_BYTES = 256 << 20
+# Configurations timed beside the default one (the GPT-2-small block).
+EXTRA_WORKLOADS = ("forward_bf16_gpt2_small", "block_bf16_d1600", "decode_bf16_gpt2_medium")
+# What the bf16 path computes in.
+DTYPE_DETAIL = ("bf16 storage (weights, block input/output, KV cache); fp16 operands in the "
+                "Linear products (activations written as fp16, weights converted from bf16); "
+                "bf16 Q/K/V and probabilities in attention; fp32 accumulation and fp32 "
+                "residual stream")
 
 
 # ------------------------------------------------------------------ helpers --
@@ -208,9 +223,13 @@ def to_dev_bf16(a: np.ndarray, torch, device):
 
 
 class Runner:
-    """Builds one workload's device state and exposes step functions."""
+    """Builds one workload's device state and exposes step functions.
 
-    def __init__(self, w: S.Workload, seed: int, device):
+    Host-side generation of the synthetic weights (and of the decode
+    workload's 1.6e9-value KV cache) runs on a thread pool: each tensor has
+    its own random stream, so the values do not depend on the pool."""
+
+    def __init__(self, w: S.Workload, seed: int, device, pool: ThreadPoolExecutor):
         import torch
         from gpt_pre_norm_gb300 import binding as G
         self.G, self.torch, self.w, self.device = G, torch, w, device
@@ -221,68 +240,78 @@ class Runner:
             return to_dev_bf16(a, torch, device) if mode == G.GPT2_BF16 else \
                 torch.from_numpy(a).to(device)
 
-        T_ctx = w.T
-        self.ctx = G.Context(w.n_vocab, w.n_ctx, w.d, w.n_head, w.n_layer, mode, w.B, T_ctx)
+        self.ctx = G.Context(w.n_vocab, w.n_ctx, w.d, w.n_head, w.n_layer, mode, w.B, w.T)
+        self.tokens = w.B * w.T
+        self.cache = None
+        self.graph = None
+        # Two device buffers for each step input and result, so that the
+        # end-to-end steps can overlap copies with the previous step's compute;
+        # a step replayed from a CUDA graph has fixed buffers (one slot).
+        self.slots = 2
         if w.kind == "block":
             p = S.block_params(w, seed)
             self.params = {k: todev(v) for k, v in p.items()}
-            x = S.block_input(w, seed)
-            self.x = todev(x)
-            self.out = torch.empty_like(self.x)
-            self.x_host = self.x.cpu().pin_memory()
-            self.out_host = torch.empty(self.out.shape, dtype=dt).pin_memory()
-            self.tokens = w.B * w.T
+            x = todev(S.block_input(w, seed))
+            self.inp = [{"x": x}, {"x": torch.empty_like(x)}]
+            self.res = [torch.empty_like(x) for _ in range(2)]
+            self.inp_host = {"x": x.cpu().pin_memory()}
+            self.res_host = [torch.empty(x.shape, dtype=dt).pin_memory() for _ in range(2)]
+            return
+        blocks = list(pool.map(lambda layer: S.block_params(w, seed, layer), range(w.n_layer)))
+        p = S.embeddings(w, seed)
+        tp = {k: todev(p[k]) for k in ("wte", "wpe", "lnf_g", "lnf_b")}
+        tp["blocks"] = [{k: todev(v) for k, v in b.items()} for b in blocks]
+        self.mp = G.ModelParams(tp)
+        ids = S.token_ids(w, seed)
+        ids_dev = torch.from_numpy(ids).to(device)
+        self.inp = [{"ids": ids_dev}, {"ids": torch.empty_like(ids_dev)}]
+        self.inp_host = {"ids": ids_dev.cpu().pin_memory()}
+        if w.kind == "forward_loss":
+            # targets: the next token of each sequence, none (-1) at the last position
+            tg = np.concatenate([ids[:, 1:], np.full((w.B, 1), -1, ids.dtype)], axis=1)
+            tg_dev = torch.from_numpy(np.ascontiguousarray(tg)).to(device)
+            self.inp[0]["targets"] = tg_dev
+            self.inp[1]["targets"] = torch.empty_like(tg_dev)
+            self.inp_host["targets"] = tg_dev.cpu().pin_memory()
+            self.res = [torch.empty((w.B, w.T), dtype=torch.float32, device=device)
+                        for _ in range(2)]
         else:
-            p = S.model_params(w, seed)
-            tp = {k: todev(p[k]) for k in ("wte", "wpe", "lnf_g", "lnf_b")}
-            tp["blocks"] = [{k: todev(v) for k, v in b.items()} for b in p["blocks"]]
-            self.mp = G.ModelParams(tp)
-            ids = S.token_ids(w, seed)
-            self.ids = torch.from_numpy(ids).to(device)
-            self.ids_host = self.ids.cpu().pin_memory()
-            if w.kind == "forward_loss":
-                # targets: the next token of each sequence, none (-1) at the last position
-                tg = np.concatenate([ids[:, 1:], np.full((w.B, 1), -1, ids.dtype)], axis=1)
-                self.targets = torch.from_numpy(np.ascontiguousarray(tg)).to(device)
-                self.targets_host = self.targets.cpu().pin_memory()
-                self.loss_host = torch.empty((w.B, w.T), dtype=torch.float32).pin_memory()
-                self.loss = None
-            else:
-                self.logits = torch.empty((w.B, w.T, w.n_vocab), dtype=torch.float32,
-                                          device=device)
-                self.logits_host = torch.empty(self.logits.shape,
-                                               dtype=torch.float32).pin_memory()
-            self.tokens = w.B * w.T
-            self.cache = None
-            if w.kind == "decode":
-                # A generation loop reuses its weights every step: their fp16
-                # working copies are made once (on the first step, before timing).
-                G.gpt2_ctx_cache_weights(self.ctx, True)
-                shape = (w.B, w.n_layer, 2, w.n_head, w.n_ctx, w.d_h)
-                host = torch.empty(shape, dtype=torch.int16).pin_memory()
-                hv = host.numpy()
-                for b in range(w.B):
-                    for layer in range(w.n_layer):
-                        pk = S.past_kv(w, seed, b, layer)
-                        hv[b, layer, :, :, :w.t_past] = S.bf16_bits(pk).view(np.int16)
-                self.cache = G.KV(host.to(device).view(torch.bfloat16), w.t_past)
-        self.graph = None
+            n_res = 1 if w.kind == "decode" else 2
+            self.res = [torch.empty((w.B, w.T, w.n_vocab), dtype=torch.float32, device=device)
+                        for _ in range(n_res)]
+        self.res_host = [torch.empty(r.shape, dtype=r.dtype).pin_memory() for r in self.res]
+        if w.kind == "decode":
+            self.slots = 1
+            # A generation loop reuses its weights every step: their fp16
+            # working copies are made once (on the first step, before timing).
+            G.gpt2_ctx_cache_weights(self.ctx, True)
+            shape = (w.B, w.n_layer, 2, w.n_head, w.n_ctx, w.d_h)
+            host = torch.empty(shape, dtype=torch.int16).pin_memory()
+            hv = host.numpy()
 
-    # One step, inputs resident on the device.
-    def step(self):
+            def fill(bl):
+                b, layer = bl
+                pk = S.past_kv(w, seed, b, layer)
+                hv[b, layer, :, :, :w.t_past] = S.bf16_bits(pk).view(np.int16)
+
+            list(pool.map(fill, [(b, layer) for b in range(w.B) for layer in range(w.n_layer)]))
+            self.cache = G.KV(host.to(device).view(torch.bfloat16), w.t_past)
+
+    # One step on input/result slot `s`, inputs resident on the device.
+    def step(self, s: int = 0):
         G, w = self.G, self.w
+        inp, res = self.inp[s], self.res[s]
         if w.kind == "block":
-            G.gpt2_block_forward(self.ctx, self.x, self.params, w.B, w.T, w.d, w.n_head,
-                                 out=self.out)
+            G.gpt2_block_forward(self.ctx, inp["x"], self.params, w.B, w.T, w.d, w.n_head, out=res)
         elif w.kind == "forward":
-            G.gpt2_forward(self.ctx, self.ids, self.mp, w.B, w.T, logits=self.logits)
+            G.gpt2_forward(self.ctx, inp["ids"], self.mp, w.B, w.T, logits=res)
         elif w.kind == "forward_loss":
-            self.loss, _ = G.gpt2_forward_loss(self.ctx, self.ids, self.mp, w.B, w.T,
-                                               targets=self.targets, want_next=False)
+            G.gpt2_forward_loss(self.ctx, inp["ids"], self.mp, w.B, w.T, targets=inp["targets"],
+                                want_next=False, loss=res)
         else:
             self.cache.T_len = w.t_past
-            G.gpt2_forward(self.ctx, self.ids, self.mp, w.B, w.T, past=self.cache,
-                           present=self.cache, logits=self.logits)
+            G.gpt2_forward(self.ctx, inp["ids"], self.mp, w.B, w.T, past=self.cache,
+                           present=self.cache, logits=res)
 
     def capture_graph(self):
         torch = self.torch
@@ -293,36 +322,30 @@ class Runner:
             self.step()
         self.graph = g
 
-    def run(self):
+    def run(self, s: int = 0):
         if self.graph is not None:
             self.graph.replay()
         else:
-            self.step()
+            self.step(s)
 
-    # One step end to end: pinned host inputs in, result back to pinned host.
-    def step_e2e(self):
-        w = self.w
-        if w.kind == "block":
-            self.x.copy_(self.x_host, non_blocking=True)
-            self.run()
-            self.out_host.copy_(self.out, non_blocking=True)
-        elif w.kind == "forward_loss":
-            self.ids.copy_(self.ids_host, non_blocking=True)
-            self.targets.copy_(self.targets_host, non_blocking=True)
-            self.run()
-            self.loss_host.copy_(self.loss, non_blocking=True)
-        else:
-            self.ids.copy_(self.ids_host, non_blocking=True)
-            self.run()
-            self.logits_host.copy_(self.logits, non_blocking=True)
+    # The end-to-end step's copies: the step's inputs from pinned host memory
+    # into slot s, and slot s's result back to pinned host memory.
+    def stage_input(self, s: int):
+        for k, t in self.inp[s].items():
+            t.copy_(self.inp_host[k], non_blocking=True)
+
+    def fetch_result(self, s: int):
+        self.res_host[s].copy_(self.res[s], non_blocking=True)
 
     def e2e_bytes(self):
-        if self.w.kind == "block":
-            n = self.x.numel() * self.x.element_size()
-            return n, n
-        if self.w.kind == "forward_loss":
-            return self.ids.numel() * 8, self.loss_host.numel() * 4
-        return self.ids.numel() * 4, self.logits.numel() * 4
+        h2d = sum(t.numel() * t.element_size() for t in self.inp[0].values())
+        d2h = self.res[0].numel() * self.res[0].element_size()
+        return h2d, d2h
+
+    def close(self):
+        self.torch.cuda.synchronize()
+        self.graph = None
+        self.ctx.close()
 
 
 def reduce_over_ranks(times_ms, device):
@@ -355,6 +378,51 @@ def timed_steps(fn, K, flush, barrier, torch):
     torch.cuda.synchronize()
     barrier()
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def timed_e2e(r, K, flush, barrier, torch):
+    """Mean time of K end-to-end steps: step i copies its input from pinned
+    host memory into device slot i % slots (own stream), runs after that copy
+    and after the L2 flush (compute stream), and copies its result back to
+    pinned host memory (own stream); with two slots the copies of one step
+    overlap the compute of its neighbours.  One event pair brackets all K
+    steps, the last result copy included, so every copy and every flush is
+    inside the timed region."""
+    comp = torch.cuda.current_stream()
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    n = r.slots
+    ev_in = [torch.cuda.Event() for _ in range(K)]
+    ev_done = [torch.cuda.Event() for _ in range(K)]
+    ev_out = [torch.cuda.Event() for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    start.record(comp)
+    h2d.wait_stream(comp)
+    d2h.wait_stream(comp)
+    for i in range(K):
+        s = i % n
+        with torch.cuda.stream(h2d):
+            if i >= n:
+                h2d.wait_event(ev_done[i - n])  # step i - n no longer reads slot s
+            r.stage_input(s)
+            ev_in[i].record(h2d)
+        if i >= n:
+            comp.wait_event(ev_out[i - n])      # slot s's last result copied out
+        flush.zero_()
+        comp.wait_event(ev_in[i])
+        r.run(s)
+        ev_done[i].record(comp)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(ev_done[i])
+            r.fetch_result(s)
+            ev_out[i].record(d2h)
+    comp.wait_stream(h2d)
+    comp.wait_stream(d2h)
+    end.record(comp)
+    torch.cuda.synchronize()
+    barrier()
+    return start.elapsed_time(end) / K
 
 
 # -------------------------------------------------------------- CPU oracle --
@@ -446,6 +514,103 @@ def workload_config(w, args):
     return cfg
 
 
+def kernel_table(prof, peaks, steps):
+    """Per kernel kind: launches, time, share of the step, achieved rate and
+    its roofline fraction, the roofline being max(algorithmic flops / tensor
+    peak, algorithmic bytes / HBM peak) per launch."""
+    total = sum(x["ms"] for x in prof.values())
+    out = {}
+    for kind, rec in prof.items():
+        n = rec["launches"]
+        avg_s = rec["ms"] / 1e3 / n
+        t_flop = rec["flops"] / n / (peaks["bf16_tflops"] * 1e12)
+        t_byte = rec["bytes"] / n / (peaks["hbm_gbs"] * 1e9)
+        e = {"launches_per_step": n / steps, "ms_per_launch": rec["ms"] / n,
+             "share": rec["ms"] / total}
+        if rec["flops"] > 0:
+            e["tflops"] = rec["flops"] / n / avg_s / 1e12
+        if rec["bytes"] > 0:
+            e["gbs"] = rec["bytes"] / n / avg_s / 1e9
+        if t_flop > 0 or t_byte > 0:
+            e["bound"] = "tensor" if (kind in TENSOR_KINDS and t_flop >= t_byte) else "hbm"
+            e["frac"] = max(t_flop, t_byte) / avg_s
+        out[kind] = e
+    return out
+
+
+def roofline_entry(prof, peaks, workload):
+    """The dominant kernel (most time per step) against its roofline."""
+    top = max(prof, key=lambda k: prof[k]["ms"])
+    rec = prof[top]
+    n = rec["launches"]
+    avg_s = rec["ms"] / 1e3 / n
+    t_flop = rec["flops"] / n / (peaks["bf16_tflops"] * 1e12)
+    t_byte = rec["bytes"] / n / (peaks["hbm_gbs"] * 1e9)
+    if top in TENSOR_KINDS and t_flop >= t_byte:
+        roof = {"bound": "tensor", "achieved": rec["flops"] / n / avg_s / 1e12,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+        alg = rec["flops"] / n
+    else:
+        roof = {"bound": "hbm", "achieved": rec["bytes"] / n / avg_s / 1e9,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+        alg = rec["bytes"] / n
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = top
+    roof["peak_source"] = peaks["source"]
+    roof["traffic"] = ncu_traffic(top, workload)
+    roof["algorithmic_per_launch"] = alg
+    return roof
+
+
+def measure(r, args, flush, barrier, torch, G, e2e: bool):
+    """Warm-up, K device-resident steps under the clock sampler, (decode) the
+    same steps without the graph, (e2e) the pipelined end-to-end steps, and a
+    profiled pass of K steps with every kernel bracketed by events."""
+    if r.w.kind == "decode":
+        r.capture_graph()
+    for _ in range(args.warmup):
+        r.run()
+    torch.cuda.synchronize()
+    st = G.gpt2_sync_status(r.ctx)
+    if st != G.GPT2_OK:
+        raise SystemExit(f"{r.w.name}: device error after warm-up: {G.status_string(st)}")
+    out = {}
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        out["times"] = timed_steps(r.run, args.steps, flush, barrier, torch)
+    out["clocks"] = clk.summary()
+    out["ms_eager"] = None
+    if r.graph is not None:
+        t = timed_steps(r.step, args.steps, flush, barrier, torch)
+        out["ms_eager"] = sum(t) / len(t)
+    out["ms_e2e"] = timed_e2e(r, args.steps, flush, barrier, torch) if e2e else None
+    G.gpt2_profile_enable(r.ctx, True)
+    G.gpt2_profile_reset(r.ctx)
+    timed_steps(r.step, args.steps, flush, barrier, torch)
+    out["prof"] = G.gpt2_profile_read(r.ctx)
+    G.gpt2_profile_enable(r.ctx, False)
+    st = G.gpt2_sync_status(r.ctx)
+    if st != G.GPT2_OK:
+        raise SystemExit(f"{r.w.name}: device error in the timed region: {G.status_string(st)}")
+    return out
+
+
+def workload_entry(w, r, m, peaks, args, ws, device):
+    """The summary of one extra configuration for the `workloads` key."""
+    ms, ms_med = reduce_over_ranks([sum(m["times"]) / len(m["times"]),
+                                    statistics.median(m["times"])], device)
+    e = {"config": workload_config(w, args), "ms_per_step": ms, "ms_per_step_median": ms_med,
+         "value": job_throughput(r.tokens, ws, ms), "unit": "tokens/s",
+         "tflops": workload_flops(w) * ws / (ms / 1e3) / 1e12,
+         "e2e_roofline": e2e_roofline(m["prof"], peaks, args.steps, ms),
+         "roofline": roofline_entry(m["prof"], peaks, w.name),
+         "kernels": kernel_table(m["prof"], peaks, args.steps),
+         "gpu_launches": int(round(sum(v["launches"] for v in m["prof"].values()))),
+         "clocks": m["clocks"]}
+    if m["ms_eager"] is not None:
+        e["eager_ms_per_step"] = reduce_over_ranks([m["ms_eager"]], device)[0]
+    return e
+
+
 # --------------------------------------------------------------------- main --
 def main():
     ap = argparse.ArgumentParser()
@@ -453,11 +618,15 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="block_bf16_d768", choices=sorted(S.WORKLOADS))
+    ap.add_argument("--extra", default=",".join(EXTRA_WORKLOADS),
+                    help="comma-separated configurations timed after the main one "
+                         "(default: the full forward, the XL block and decode; '' for none)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     w = S.WORKLOADS[args.workload]
+    extras = [S.WORKLOADS[n] for n in args.extra.split(",") if n and n != w.name]
     ws, rank, local = dist_env()
 
     if args.impl == "reference":
@@ -477,102 +646,60 @@ def main():
         barrier = lambda: dist.barrier()  # noqa: E731
 
     from gpt_pre_norm_gb300 import binding as G
-    r = Runner(w, args.seed + rank, device)
-    if w.kind == "decode":
-        r.capture_graph()
+    pool = ThreadPoolExecutor(max_workers=os.cpu_count() or 4)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-    for _ in range(args.warmup):
-        r.run()
-    torch.cuda.synchronize()
-    st = G.gpt2_sync_status(r.ctx)
-    if st != G.GPT2_OK:
-        raise SystemExit(f"device error after warm-up: {G.status_string(st)}")
+    peaks = load_peaks()
 
-    # Timed region: device-resident inputs.
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        times = timed_steps(r.run, args.steps, flush, barrier, torch)
-    ms = sum(times) / len(times)
-    ms_med = statistics.median(times)
+    r = Runner(w, args.seed + rank, device, pool)
+    m = measure(r, args, flush, barrier, torch, G, e2e=True)
+    times, prof = m["times"], m["prof"]
+    ms, ms_e2e, ms_med = reduce_over_ranks(
+        [sum(times) / len(times), m["ms_e2e"], statistics.median(times)], device)
+    ms_eager = reduce_over_ranks([m["ms_eager"]], device)[0] if m["ms_eager"] is not None else None
+    tokens_rank = r.tokens
+    h2d, d2h = r.e2e_bytes()
+    r.close()
+    del r
+    gc.collect()
+    torch.cuda.empty_cache()
 
-    # A graph-replayed workload (decode) is also timed launching its kernels
-    # one by one, for the graph's gain.
-    ms_eager = None
-    if r.graph is not None:
-        times_eager = timed_steps(r.step, args.steps, flush, barrier, torch)
-        ms_eager = sum(times_eager) / len(times_eager)
-
-    # End to end through the C ABI: pinned host buffers, copies inside the step.
-    times_e2e = timed_steps(r.step_e2e, args.steps, flush, barrier, torch)
-    ms_e2e = sum(times_e2e) / len(times_e2e)
-
-    # Profiled pass: every kernel launch bracketed by events on its stream.
-    G.gpt2_profile_enable(r.ctx, True)
-    G.gpt2_profile_reset(r.ctx)
-    timed_steps(r.step, args.steps, flush, barrier, torch)
-    prof = G.gpt2_profile_read(r.ctx)
-    G.gpt2_profile_enable(r.ctx, False)
-    st = G.gpt2_sync_status(r.ctx)
-    if st != G.GPT2_OK:
-        raise SystemExit(f"device error in the timed region: {G.status_string(st)}")
-
-    ms, ms_e2e, ms_med = reduce_over_ranks([ms, ms_e2e, ms_med], device)
-    if ms_eager is not None:
-        ms_eager = reduce_over_ranks([ms_eager], device)[0]
+    # The other configurations, one after the other (each rank a replica).
+    extra_entries = {}
+    for we in extras:
+        re_ = Runner(we, args.seed + rank, device, pool)
+        me = measure(re_, args, flush, barrier, torch, G, e2e=False)
+        extra_entries[we.name] = workload_entry(we, re_, me, peaks, args, ws, device)
+        re_.close()
+        del re_
+        gc.collect()
+        torch.cuda.empty_cache()
+    pool.shutdown()
     if rank != 0:
         return 0
 
-    peaks = load_peaks()
-    tokens = r.tokens * ws
-    value = job_throughput(r.tokens, ws, ms)
+    value = job_throughput(tokens_rank, ws, ms)
     flops = workload_flops(w)
-    kernels = {}
-    for kind, rec in prof.items():
-        n = rec["launches"]
-        avg_s = rec["ms"] / 1e3 / n
-        entry = {"launches_per_step": n / args.steps, "ms_per_launch": rec["ms"] / n,
-                 "share": rec["ms"] / sum(x["ms"] for x in prof.values())}
-        if kind in TENSOR_KINDS and rec["flops"] > 0:
-            ach = rec["flops"] / n / avg_s / 1e12
-            entry.update(tflops=ach, frac=ach / peaks["bf16_tflops"])
-        elif rec["bytes"] > 0:
-            ach = rec["bytes"] / n / avg_s / 1e9
-            entry.update(gbs=ach, frac=ach / peaks["hbm_gbs"])
-        kernels[kind] = entry
-    top = max(prof, key=lambda k: prof[k]["ms"])
-    rec = prof[top]
-    n = rec["launches"]
-    avg_s = rec["ms"] / 1e3 / n
-    if top in TENSOR_KINDS:
-        achieved = rec["flops"] / n / avg_s / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s"}
-    else:
-        achieved = rec["bytes"] / n / avg_s / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["kernel"] = top
-    roof["peak_source"] = peaks["source"]
-    roof["traffic"] = ncu_traffic(top, w.name)
-    roof["algorithmic_per_launch"] = rec["flops"] / n if top in TENSOR_KINDS else rec["bytes"] / n
-
-    h2d, d2h = r.e2e_bytes()
-    launches = sum(v["launches"] for v in prof.values())
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_median": ms_med,
         "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "vs_baseline": None,
+        "dtype": "bf16/fp16" if w.dtype == "bf16" else "f32",
+        "dtype_detail": DTYPE_DETAIL if w.dtype == "bf16" else "fp32 storage and arithmetic",
+        "data": "synthetic",
         "config": workload_config(w, args),
         "tflops": flops * ws / (ms / 1e3) / 1e12,
         "tflops_frac_of_bf16_peak": flops * ws / (ms / 1e3) / 1e12 / peaks["bf16_tflops"],
-        "roofline": roof,
+        "roofline": roofline_entry(prof, peaks, w.name),
         "e2e_roofline": e2e_roofline(prof, peaks, args.steps, ms),
-        "e2e": {"value": job_throughput(r.tokens, ws, ms_e2e), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": int(round(launches)),
-        "clocks": clk.summary(),
-        "kernels": kernels,
+        "e2e": {"value": job_throughput(tokens_rank, ws, ms_e2e), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "pipelined": "two device buffers; copies on their own streams; "
+                             "L2 flush inside the timed region"},
+        "gpu_launches": int(round(sum(v["launches"] for v in prof.values()))),
+        "clocks": m["clocks"],
+        "kernels": kernel_table(prof, peaks, args.steps),
+        "workloads": extra_entries,
     }
     if ms_eager is not None:
         line["eager_ms_per_step"] = ms_eager  # the same step without the CUDA graph

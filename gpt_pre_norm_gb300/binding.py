@@ -22,6 +22,7 @@ GPT2_ERR_CUDA = 5
 GPT2_ERR_DEVICE_TIMEOUT = 6
 GPT2_ERR_WORKSPACE = 7
 GPT2_ERR_NO_DEVICE = 8
+GPT2_ERR_RANGE = 9
 
 GPT2_BF16 = 0
 GPT2_FP32 = 1
@@ -255,11 +256,14 @@ def gpt2_forward(ctx: Context, ids: torch.Tensor, params: ModelParams, B: int, T
 
 def gpt2_forward_loss(ctx: Context, ids: torch.Tensor, params: ModelParams, B: int, T: int,
                       targets: torch.Tensor | None = None, past: KV | None = None,
-                      present: KV | None = None, want_next: bool = True, stream=None):
+                      present: KV | None = None, want_next: bool = True, stream=None,
+                      loss: torch.Tensor | None = None):
     """(loss [B, T] fp32 or None, next_ids [B, T] int32 or None) without the
-    logits; loss needs targets."""
-    loss = (torch.empty((B, T), dtype=torch.float32, device=ids.device)
-            if targets is not None else None)
+    logits; loss needs targets (written into `loss` when given)."""
+    if targets is None:
+        loss = None
+    elif loss is None:
+        loss = torch.empty((B, T), dtype=torch.float32, device=ids.device)
     nxt = torch.empty((B, T), dtype=torch.int32, device=ids.device) if want_next else None
     ps = past.struct() if past is not None else None
     pr = present.struct() if present is not None else None

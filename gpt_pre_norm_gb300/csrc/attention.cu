@@ -156,11 +156,28 @@ __global__ void __launch_bounds__(kDecThreads)
   }
   if (j < ns) {
     // A wait ran out: the copies still in flight must land before the CTA
-    // exits; nothing is written.
+    // exits, and this (sequence, head)'s result becomes NaN (its output row,
+    // or this split's partial, which makes the combined row NaN), so that a
+    // caller without the error word cannot mistake stale memory for a result.
     if (tid == 0)
       for (int k = j; k < issued; ++k)
         mbar_wait_bounded(&full[k % kDecStages], static_cast<uint32_t>(k / kDecStages) & 1u,
                           nullptr, err);
+    if (warp == 0) {
+      const float nan = __int_as_float(0x7fc00000);
+      if (splits == 1) {
+        *reinterpret_cast<uint32_t*>(out + static_cast<size_t>(bh) * kDh + 2 * lane) =
+            pack_16x2(nan, nan, out_f16 != 0);
+      } else {
+        float* pp = partials + (static_cast<size_t>(bh) * splits + split) * kPartialStride;
+        pp[2 * lane] = nan;
+        pp[2 * lane + 1] = nan;
+        if (lane == 0) {
+          pp[kDh] = nan;
+          pp[kDh + 1] = nan;
+        }
+      }
+    }
     return;
   }
   // Merge the four key groups of the warp (lanes sub, sub+8, sub+16, sub+24).
@@ -316,16 +333,13 @@ int launch_decode_attention_bf16(const bf16* q, const bf16* kv, long long s_batc
                                  float* partials, int splits, cudaStream_t stream,
                                  int* launches, bool out_f16, unsigned* err) {
   if (B <= 0 || h <= 0 || t_len <= 0 || splits <= 0 || splits > 65535) return GPT2_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * h > 65535) return GPT2_ERR_UNSUPPORTED;  // grid.y
   if (splits > 1 && partials == nullptr) return GPT2_ERR_INVALID_ARG;
   const int chunk = (t_len + splits - 1) / splits;
   dim3 grid(splits, B * h);
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(attn_decode_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kDecSmem)) != cudaSuccess)
-      return GPT2_ERR_CUDA;
-    attr_set = true;
-  }
+  if (!ensure_smem_limit(reinterpret_cast<const void*>(&attn_decode_bf16),
+                         static_cast<int>(kDecSmem)))
+    return GPT2_ERR_CUDA;
   cudaError_t e = launch_pdl(attn_decode_bf16, grid, dim3(kDecThreads), kDecSmem, stream, q, kv,
                              s_batch, s_kv, s_head, h, t_len, chunk, static_cast<uint16_t*>(out),
                              partials, out_f16 ? 1 : 0, err);

@@ -464,13 +464,9 @@ int launch_attention_tc(const LaunchEnv& env, const bf16* q, const bf16* kv, lon
   if (!encode(env, &tmQ, q, 3, qd, qs, qb, false) || !encode(env, &tmK, kv, 4, kd, ks, kb, false) ||
       !encode(env, &tmV, kv + s_kv, 4, kd, ks, kb, false))
     return GPT2_ERR_CUDA;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes)) != cudaSuccess)
-      return GPT2_ERR_CUDA;
-    attr_set = true;
-  }
+  if (!ensure_smem_limit(reinterpret_cast<const void*>(&attn_tc_kernel),
+                         static_cast<int>(kSmemBytes)))
+    return GPT2_ERR_CUDA;
   const long long n_work = static_cast<long long>(B) * h * n_qtiles;
   if (n_work > 0x7fffffff) return GPT2_ERR_UNSUPPORTED;
   AttnArgs args{T, t_past, h, n_qtiles, B * h, static_cast<int>(n_work), out_f16 ? 1 : 0, out,

@@ -17,6 +17,7 @@ namespace gpt2 {
 enum : unsigned {
   kErrTimeout = 1u,   // a bounded wait ran out
   kErrBadToken = 2u,  // a token id outside [0, n_vocab)
+  kErrRange = 4u,     // a value outside the fp16 operand range, or not finite
 };
 
 // A wait gives up after this many nanoseconds of %globaltimer.

@@ -173,14 +173,9 @@ __global__ void __launch_bounds__(kWarps * 32)
 template <int KIND>
 cudaError_t launch_kind(dim3 grid, cudaStream_t s, const CUtensorMap& tmX, const CUtensorMap& tmW,
                         const SmallArgs& a) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(gemm_smallm<KIND>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(kSmem));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  if (!ensure_smem_limit(reinterpret_cast<const void*>(&gemm_smallm<KIND>),
+                         static_cast<int>(kSmem)))
+    return cudaErrorInvalidValue;
   return launch_pdl(gemm_smallm<KIND>, grid, dim3(kWarps * 32), kSmem, s, tmX, tmW, a);
 }
 

@@ -993,15 +993,8 @@ int launch_gemm_tc(const LaunchEnv& env, int kind_in, const void* A_in, const vo
                                 ep.kv.s_head);
   }
 
-  // Set once per process (the opt-in limit does not depend on the call), so
-  // later calls make no non-stream CUDA call (safe under stream capture).
-  static bool attr_set[2][kEpiCount] = {};
-  if (!attr_set[cg - 1][kind]) {
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) !=
-        cudaSuccess)
-      return GPT2_ERR_CUDA;
-    attr_set[cg - 1][kind] = true;
-  }
+  // The opt-in limit does not depend on the call: set once per device.
+  if (!ensure_smem_limit(fn, kSmemLimit)) return GPT2_ERR_CUDA;
   const int grid = std::min(args.num_tiles, units) * cg;
   void* params[] = {&tmA, &tmB, &tmO, &tmR, &tmQ, &tmKV, &args};
   cudaLaunchConfig_t cfg = {};

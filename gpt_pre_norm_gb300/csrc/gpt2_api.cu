@@ -427,6 +427,14 @@ int check_mode_shape(const gpt2_hparams& hp) {
   return GPT2_OK;
 }
 
+std::mutex g_smem_attr_mutex;
+struct SmemAttr {
+  int device;
+  const void* fn;
+  int bytes;
+};
+std::vector<SmemAttr> g_smem_attrs;
+
 std::once_flag g_encode_once;
 EncodeTiledFn g_encode = nullptr;
 
@@ -445,6 +453,24 @@ EncodeTiledFn get_encode() {
 }  // namespace
 
 namespace gpt2 {
+
+bool ensure_smem_limit(const void* fn, int bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(g_smem_attr_mutex);
+  for (const SmemAttr& a : g_smem_attrs)
+    if (a.device == dev && a.fn == fn && a.bytes >= bytes) return true;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return false;
+  for (SmemAttr& a : g_smem_attrs)
+    if (a.device == dev && a.fn == fn) {
+      a.bytes = bytes;
+      return true;
+    }
+  g_smem_attrs.push_back(SmemAttr{dev, fn, bytes});
+  return true;
+}
+
 namespace {
 // One thread waits on an mbarrier nothing completes, with the kernels' bounded
 // wait and a short limit: the wait runs out and raises the timeout bit.
@@ -473,6 +499,8 @@ const char* gpt2_status_string(int status) {
     case GPT2_ERR_DEVICE_TIMEOUT: return "a kernel wait timed out";
     case GPT2_ERR_WORKSPACE: return "workspace too small for the request";
     case GPT2_ERR_NO_DEVICE: return "no sm_100-family GPU is current";
+    case GPT2_ERR_RANGE:
+      return "a value outside the fp16 operand range (|v| > 65504) or not finite";
     default: return "unknown status";
   }
 }
@@ -515,6 +543,7 @@ int gpt2_ctx_create(const gpt2_hparams* hp, int max_B, int max_T, void* workspac
   c->env.num_sms = sms;
   c->env.err = c->at<unsigned>(plan.err);
   c->env.encode = enc;
+  c->env.wait_ns = kWaitLimitNs;
   c->prof = false;
   c->extra_kernels = 0;
   c->cache_weights = false;
@@ -559,6 +588,7 @@ int gpt2_sync_status(gpt2_ctx* c, void* stream) {
   if (word != 0 && cudaMemset(c->env.err, 0, sizeof(unsigned)) != cudaSuccess) return GPT2_ERR_CUDA;
   if (word & kErrTimeout) return GPT2_ERR_DEVICE_TIMEOUT;
   if (word & kErrBadToken) return GPT2_ERR_INVALID_ARG;
+  if (word & kErrRange) return GPT2_ERR_RANGE;
   return GPT2_OK;
 }
 

@@ -94,6 +94,7 @@ struct LaunchEnv {
   int num_sms;
   unsigned* err;          // device error word
   EncodeTiledFn encode;   // cuTensorMapEncodeTiled
+  unsigned long long wait_ns;  // limit of every bounded wait in the kernels
 };
 
 // Tensor-core GEMM (16-bit operands, fp32 accumulate in TMEM): C = A[M,K]
@@ -174,6 +175,13 @@ int decode_splits(int B, int h, int t_len, int num_sms);
 int launch_attention_fp32(const float* q, const float* kv, long long kv_s_batch, long long kv_s_kv,
                           long long kv_s_head, int B, int h, int T, int t_past, int d_h,
                           float* out, cudaStream_t stream);
+
+// Raises the dynamic shared-memory limit of kernel `fn` to `bytes` on the
+// current device, the first time it is asked for that (device, kernel, size):
+// the attribute is per device, and later calls make no CUDA call at all (so
+// they are safe inside a stream capture).  Thread-safe.  Returns false when
+// the runtime refuses.
+bool ensure_smem_limit(const void* fn, int bytes);
 
 // Launches `kernel` on `stream` with programmatic stream serialisation (the
 // kernel must call pdl_wait() before touching global memory).

@@ -72,6 +72,8 @@ extern "C" int gpt2_attention_decode_noalloc(const void* q, const void* kv, int 
   if (d_h != 64) return GPT2_ERR_UNSUPPORTED;
   if (T_past + 1 > T_cap) return GPT2_ERR_CTX_OVERFLOW;
   if (!aligned16(q) || !aligned16(kv) || !aligned16(out)) return GPT2_ERR_ALIGNMENT;
+  // One CTA row per (sequence, head) pair: the grid's y extent.
+  if (static_cast<long long>(B) * n_head > 65535) return GPT2_ERR_UNSUPPORTED;
   DeviceSetup* dev = nullptr;
   int st = setup_current_device(&dev);
   if (st) return st;

@@ -65,7 +65,9 @@ typedef enum {
   GPT2_ERR_CUDA = 5,           /* a CUDA runtime call failed */
   GPT2_ERR_DEVICE_TIMEOUT = 6, /* a kernel's bounded wait ran out */
   GPT2_ERR_WORKSPACE = 7,      /* workspace too small for the request */
-  GPT2_ERR_NO_DEVICE = 8       /* no sm_100-family GPU is current */
+  GPT2_ERR_NO_DEVICE = 8,      /* no sm_100-family GPU is current */
+  GPT2_ERR_RANGE = 9           /* (device) a value outside the fp16 operand range
+                                  of the bf16 mode (|v| > 65504), or not finite */
 } gpt2_status;
 
 typedef enum { GPT2_BF16 = 0, GPT2_FP32 = 1 } gpt2_dtype;
@@ -277,9 +279,12 @@ int gpt2_attention(gpt2_ctx *ctx, const void *q, const void *kv, int B, int n_he
  * call's contents; nothing in it has to start at zero, since each call writes
  * every partial result before reading it.  Calls that overlap on the GPU
  * (other streams, other host threads) race on the array.
- * Errors: INVALID_ARG, UNSUPPORTED (d_h != 64), CTX_OVERFLOW (T_past + 1 >
- * T_cap), ALIGNMENT, WORKSPACE (B * h * splits partial results of 66 floats
- * exceed the 1 MiB array), NO_DEVICE, CUDA.                                 */
+ * There is no context and so no device error word: if one of the kernel's
+ * bounded waits runs out (2 s), that (sequence, head)'s output row is
+ * written as NaN instead of being left as it was.
+ * Errors: INVALID_ARG, UNSUPPORTED (d_h != 64, or B * h > 65535),
+ * CTX_OVERFLOW (T_past + 1 > T_cap), ALIGNMENT, WORKSPACE (B * h * splits
+ * partial results of 66 floats exceed the 1 MiB array), NO_DEVICE, CUDA.    */
 int gpt2_attention_decode_noalloc(const void *q, const void *kv, int B, int n_head, int T_past,
                                   int T_cap, int d_h, int splits, void *out, void *stream);
 

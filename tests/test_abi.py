@@ -117,6 +117,9 @@ def test_noalloc_decode_validates_on_the_host(G):
     assert f(a16, a16, 1, 4, 10, 16, 32, 0, a16, None) == G.GPT2_ERR_UNSUPPORTED    # d_h != 64
     assert f(a16, a16, 1, 4, 16, 16, 64, 0, a16, None) == G.GPT2_ERR_CTX_OVERFLOW   # T_past + 1 > T_cap
     assert f(bad, a16, 1, 4, 10, 16, 64, 0, a16, None) == G.GPT2_ERR_ALIGNMENT
+    # One CTA row per (sequence, head): B * h beyond the grid's 65535 rows.
+    assert f(a16, a16, 4096, 16, 10, 16, 64, 1, a16, None) == G.GPT2_ERR_UNSUPPORTED
+    assert f(a16, a16, 1 << 20, 1 << 12, 10, 16, 64, 0, a16, None) == G.GPT2_ERR_UNSUPPORTED
 
 
 def test_profiler_kinds_and_null_context(G):
