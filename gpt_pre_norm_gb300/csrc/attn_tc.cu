@@ -76,6 +76,7 @@ struct AttnArgs {
   int out_f16;  // output fp16 (else bf16)
   void* out;    // [B, T, h * 64]
   unsigned* err;
+  unsigned long long wait_ns;  // limit of each bounded wait
 };
 
 // Work item w: the query tiles with the most keys first, then sequence x head.
@@ -222,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const unsigned long long now = global_timer_ns();
         if (t_idle == 0) {
           t_idle = now;
-        } else if (*abort_flag || now - t_idle > kWaitLimitNs) {
+        } else if (*abort_flag || now - t_idle > a.wait_ns) {
           if (!*abort_flag) raise_error(a.err, kErrTimeout);
           *abort_flag = 1;
           ok = false;
@@ -249,11 +250,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     auto issue_s = [&]() -> bool {
       const int s = sg % kSK, sb = sg & 1;
       if (sj == 0 && !mbar_wait_bounded(&q_full[st & 1], static_cast<uint32_t>(st >> 1) & 1u,
-                                        abort_flag, a.err))
+                                        abort_flag, a.err, a.wait_ns))
         return false;
       // S_{g-2}, the buffer's previous tile, was read before P_{g-2} was
       // published, which this thread has already waited for.
-      if (!mbar_wait_bounded(&k_full[s], static_cast<uint32_t>(sg / kSK) & 1u, abort_flag, a.err))
+      if (!mbar_wait_bounded(&k_full[s], static_cast<uint32_t>(sg / kSK) & 1u, abort_flag, a.err,
+                             a.wait_ns))
         return false;
       tc_fence_after();
       const uint64_t q_desc = sdesc_k_sw128(smem_u32(sQ + (st & 1) * kQBytes));
@@ -281,8 +283,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int j = 0; j < n_kt; ++j, ++g) {
         if (sw < a.n_work && !(ok = issue_s())) break;
         const int pb = g & 1, s = g % kSV;
-        if (!mbar_wait_bounded(&v_full[s], static_cast<uint32_t>(g / kSV) & 1u, abort_flag, a.err) ||
-            !mbar_wait_bounded(&p_full[pb], static_cast<uint32_t>(g >> 1) & 1u, abort_flag, a.err)) {
+        if (!mbar_wait_bounded(&v_full[s], static_cast<uint32_t>(g / kSV) & 1u, abort_flag, a.err,
+                               a.wait_ns) ||
+            !mbar_wait_bounded(&p_full[pb], static_cast<uint32_t>(g >> 1) & 1u, abort_flag, a.err,
+                               a.wait_ns)) {
           ok = false;
           break;
         }
@@ -307,11 +311,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = 0.125f * kLog2e;           // 1/sqrt(64), in log2 units
     bool ok = true;
+    bool bad = false;                            // an output value out of range
     // The product P_t V_t has completed (pv_done of step t; never more than
     // one phase behind when waited for).
     auto wait_pv = [&](int t) -> bool {
       return mbar_wait_bounded(&pv_done[t & 1], static_cast<uint32_t>(t >> 1) & 1u, abort_flag,
-                               a.err);
+                               a.err, a.wait_ns);
     };
     int g = 0;
     for (int t = 0, w = w0; ok && w < a.n_work; w = work(++t)) {
@@ -321,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int j = 0; j < tl.n_kt; ++j) {
         const int gj = g + j, sb = gj & 1;
         if (!mbar_wait_bounded(&s_full[sb], static_cast<uint32_t>(gj >> 1) & 1u, abort_flag,
-                               a.err)) {
+                               a.err, a.wait_ns)) {
           ok = false;
           break;
         }
@@ -335,17 +340,23 @@ __global__ void __launch_bounds__(kThreads, 2)
         // Raw scores; the 1/sqrt(64) scale (in log2 units) is applied to the
         // row maximum and inside the exponent's fused multiply-add.
         const int key0 = j * kKT;
-        float mx = -INFINITY;
-        if (key0 + kKT - 1 > pos) {               // this step crosses the row's diagonal
+        if (__any_sync(0xffffffffu, key0 + kKT - 1 > pos)) {  // a step crossing some row's diagonal
 #pragma unroll
-          for (int c = 0; c < kKT; ++c) {
-            const float x = key0 + c <= pos ? __uint_as_float(sr[c]) : -INFINITY;
-            sr[c] = __float_as_uint(x);
-            mx = fmaxf(mx, x);
-          }
-        } else {
+          for (int c = 0; c < kKT; ++c)
+            if (key0 + c > pos) sr[c] = __float_as_uint(-INFINITY);
+        }
+        // Row maximum over eight independent chains of three-input maxima.
+        float mx;
+        {
+          float m8[8];
 #pragma unroll
-          for (int c = 0; c < kKT; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+          for (int i = 0; i < 8; ++i) m8[i] = __uint_as_float(sr[i]);
+#pragma unroll
+          for (int c = 8; c < kKT; c += 16)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              m8[i] = max3(m8[i], __uint_as_float(sr[c + i]), __uint_as_float(sr[c + 8 + i]));
+          mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
         }
         // A new reference maximum only when this row's passed it by more
         // than kRescaleLog2 (always on the row's first key); O and l scale
@@ -371,16 +382,26 @@ __global__ void __launch_bounds__(kThreads, 2)
           tmem_st_wait();
         }
         const float m_use = m == -INFINITY ? 0.f : m;  // a row with no key yet
-        float lj = 0.f;
+        // Packed pairs: x = s * scale - m for two keys per instruction, the
+        // row sum in four packed accumulators.
+        const uint64_t sl2_2 = f2(sl2, sl2), nm_2 = f2(-m_use, -m_use);
+        uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
         uint32_t pk[kKT / 2];
 #pragma unroll
         for (int c = 0; c < kKT / 2; ++c) {
-          const float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), sl2, -m_use));
-          const float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -m_use));
-          lj += p0 + p1;
+          float x0, x1;
+          f2_split(ffma2(f2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sl2_2,
+                         nm_2),
+                   x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          ls2[c & 3] = fadd2(ls2[c & 3], f2(p0, p1));
           pk[c] = pack_bf16x2(p0, p1);
         }
-        l += lj;
+        {
+          float a0, a1;
+          f2_split(fadd2(fadd2(ls2[0], ls2[1]), fadd2(ls2[2], ls2[3])), a0, a1);
+          l += a0 + a1;
+        }
         // P_g: this row's 64 keys as 32 bf16 pairs in TMEM lane r, in the
         // buffer P_{g-2} V_{g-2} read last.
         if (gj >= 2 && !(ok = wait_pv(gj - 2))) break;
@@ -404,6 +425,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       const float inv = 1.0f / l;
       const int row = tl.q0 + r;
       if (row < a.T) {
+        // fp16 output: values beyond 65504 would become inf; either kind:
+        // nothing non-finite.
+        const float lim = a.out_f16 ? 65504.f : 3.4028235e38f;
         uint4* dst = reinterpret_cast<uint4*>(
             static_cast<uint16_t*>(a.out) +
             (static_cast<size_t>(tl.b) * a.T + row) * (static_cast<size_t>(a.h) * kD) +
@@ -412,13 +436,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int c = 0; c < 8; ++c) {
           uint32_t wv[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            wv[e] = pack_16x2(__uint_as_float(ov[8 * c + 2 * e]) * inv,
-                              __uint_as_float(ov[8 * c + 2 * e + 1]) * inv, a.out_f16 != 0);
+          for (int e = 0; e < 4; ++e) {
+            const float o0 = __uint_as_float(ov[8 * c + 2 * e]) * inv;
+            const float o1 = __uint_as_float(ov[8 * c + 2 * e + 1]) * inv;
+            bad |= !(fabsf(o0) <= lim) || !(fabsf(o1) <= lim);
+            wv[e] = pack_16x2(o0, o1, a.out_f16 != 0);
+          }
           dst[c] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
       }
     }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) raise_error(a.err, kErrRange);
   }
 
   tc_fence_before();
@@ -470,7 +498,7 @@ int launch_attention_tc(const LaunchEnv& env, const bf16* q, const bf16* kv, lon
   const long long n_work = static_cast<long long>(B) * h * n_qtiles;
   if (n_work > 0x7fffffff) return GPT2_ERR_UNSUPPORTED;
   AttnArgs args{T, t_past, h, n_qtiles, B * h, static_cast<int>(n_work), out_f16 ? 1 : 0, out,
-                env.err};
+                env.err, env.wait_ns};
   // Two resident CTAs per SM, each walking the tiles w = blockIdx.x, + grid, ...
   const int grid = static_cast<int>(std::min<long long>(n_work, 2LL * env.num_sms));
   const cudaError_t e = launch_pdl(attn_tc_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream,

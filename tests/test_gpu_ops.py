@@ -149,9 +149,13 @@ def _attn_case(rng, B, h, T, t_past, t_cap, dh=64, bf16=True):
     return q, kv
 
 
+# Query tiles of 128 rows are processed in pairs sharing each 128-key step:
+# T = 256 is one full pair, 384 and 513 end in a pair with one (partly)
+# filled tile, 257 after 63 cached positions puts every tile across two steps.
 @pytest.mark.parametrize("B,h,T,t_past", [(2, 3, 1, 0), (2, 3, 2, 0), (1, 2, 127, 0),
                                           (2, 3, 129, 0), (1, 12, 300, 0), (2, 2, 70, 5),
-                                          (1, 2, 200, 130), (1, 1, 1024, 0)])
+                                          (1, 2, 200, 130), (1, 1, 1024, 0), (1, 2, 256, 0),
+                                          (2, 1, 384, 0), (1, 2, 513, 0), (2, 2, 257, 63)])
 def test_attention_prefill_bf16(G, B, h, T, t_past):
     rng = np.random.default_rng(B * 1000 + T + t_past)
     ctx = _ctx(G, G.GPT2_BF16)
@@ -164,6 +168,26 @@ def test_attention_prefill_bf16(G, B, h, T, t_past):
     ref = O.merge_heads(O.causal_attention(q.astype(np.float64), k, v))
     got = host(out)
     assert_bf16_close(got, ref, what="prefill attention")
+    assert np.max(np.abs(got - ref)) < 3e-2
+
+
+def test_attention_prefill_bf16_growing_scores(G):
+    # Keys grow with their position, so a row's maximum score keeps rising
+    # from step to step by more than the online softmax lets its reference
+    # maximum lag: the kernel must rescale the running output and sum.
+    rng = np.random.default_rng(77)
+    B, h, T = 2, 2, 1024
+    ctx = _ctx(G, G.GPT2_BF16)
+    q, kv = _attn_case(rng, B, h, T, 0, T)
+    q = S.round_to_bf16(2.0 * q)
+    grow = (1.0 + np.arange(T) / 128.0)[None, None, :, None]
+    kv[:, 0] = S.round_to_bf16(kv[:, 0] * grow)
+    out = G.gpt2_attention(ctx, dev(q), dev(kv), 0)
+    assert G.gpt2_sync_status(ctx) == 0
+    ref = O.merge_heads(O.causal_attention(q.astype(np.float64), kv[:, 0].astype(np.float64),
+                                           kv[:, 1].astype(np.float64)))
+    got = host(out)
+    assert_bf16_close(got, ref, what="prefill attention, growing scores")
     assert np.max(np.abs(got - ref)) < 3e-2
 
 
