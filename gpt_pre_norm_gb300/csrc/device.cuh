@@ -523,6 +523,17 @@ __device__ __forceinline__ uint32_t pack_16x2(float lo, float hi, bool f16) {
   return f16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
 }
 
+// Range test of packed fp16 pairs: fp16_max_mag(acc, w) keeps the larger
+// magnitude of each half (unsigned compare of the bits without the signs), and
+// fp16_nonfinite(acc) says whether a half reached the all-ones exponent (an
+// overflow to infinity, or a NaN).
+__device__ __forceinline__ uint32_t fp16_max_mag(uint32_t acc, uint32_t w) {
+  return __vmaxu2(acc, w & 0x7fff7fffu);
+}
+__device__ __forceinline__ bool fp16_nonfinite(uint32_t acc) {
+  return (acc & 0xffffu) >= 0x7c00u || (acc >> 16) >= 0x7c00u;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 

@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   // Epilogue: 512 outputs (16 features x 32 tokens), 4 per thread, the
   // feature index fastest so neighbouring threads write neighbouring columns.
   const EpiParams& ep = a.ep;
+  uint32_t mag = 0u;  // kEpiGelu: largest fp16 output magnitude (bits)
   for (int o = threadIdx.x; o < kFeat * kTok; o += blockDim.x) {
     const int fl = o % kFeat, tok = o / kFeat;
     const int f = f0 + fl;
@@ -147,8 +148,9 @@ __global__ void __launch_bounds__(kWarps * 32)
           atomicAdd(o_, v);  // in place: out == resid, chunks accumulate
         }
       } else if constexpr (KIND == kEpiGelu) {
-        static_cast<__half*>(ep.out)[static_cast<size_t>(tok) * ep.ldo + f] =
-            __float2half_rn(gelu_tanh_approx(v));
+        const __half h = __float2half_rn(gelu_tanh_approx(v));
+        mag = fp16_max_mag(mag, static_cast<uint32_t>(__half_as_ushort(h)));
+        static_cast<__half*>(ep.out)[static_cast<size_t>(tok) * ep.ldo + f] = h;
       } else if constexpr (KIND == kEpiBias) {
         static_cast<__half*>(ep.out)[static_cast<size_t>(tok) * ep.ldo + f] = __float2half_rn(v);
       } else if constexpr (KIND == kEpiQkv) {
@@ -168,6 +170,8 @@ __global__ void __launch_bounds__(kWarps * 32)
       }
     }
   }
+  // An fp16 GELU output past 65504 (or not finite) would feed the next product.
+  if (KIND == kEpiGelu && fp16_nonfinite(mag)) raise_error(a.err, kErrRange);
 }
 
 template <int KIND>

@@ -357,6 +357,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol
     qkv_b = row / ep.T;
     qkv_t = row - qkv_b * ep.T;
   }
+  uint32_t mag = 0u;  // kEpiGelu, fp16 output: largest magnitude (fp16 bits) written
   for (int c = 0; c < seg_end; c += 32) {
     const int col = ncol0 + c;
     uint32_t r[32];
@@ -465,7 +466,10 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol
           // result already in its stored form.
           uint32_t w[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) w[i] = gelu_tanh_f16x2(v[2 * i], v[2 * i + 1]);
+          for (int i = 0; i < 16; ++i) {
+            w[i] = gelu_tanh_f16x2(v[2 * i], v[2 * i + 1]);
+            mag = fp16_max_mag(mag, w[i]);
+          }
           if (tma_store_path) {
             box_write_packed(ob, lane, w);
             fence_proxy_async_smem();
@@ -556,6 +560,11 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol
         }
       }
     }
+  }
+  if constexpr (KIND == kEpiGelu) {
+    // An fp16 GELU output past 65504 (or not finite) would feed the next
+    // product: report it (the rows past M hold zeros).
+    if (__any_sync(0xffffffffu, fp16_nonfinite(mag)) && lane == 0) raise_error(a.err, kErrRange);
   }
 }
 

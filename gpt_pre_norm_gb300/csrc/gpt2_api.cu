@@ -296,7 +296,7 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int slot, int B, int
     *by = static_cast<double>(M) * d * ((x_dtype == GPT2_FP32 ? 4 : 2) + (bf ? 2 : 4)) +
           conversion_bytes(conv);
     return launch_layer_norm(hp.dtype, x_in, x_dtype, p->ln1_g, p->ln1_b, M, d, ln, s, bf,
-                             conv.count ? &conv : nullptr);
+                             conv.count ? &conv : nullptr, c->env.err);
   });
   if (st) return st;
 
@@ -375,7 +375,8 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int slot, int B, int
   st = c->run(kKindLayerNorm, s, [&](double* fl, double* by) {
     *fl = 0;
     *by = static_cast<double>(M) * d * (4 + (bf ? 2 : 4));
-    return launch_layer_norm(hp.dtype, xprime, GPT2_FP32, p->ln2_g, p->ln2_b, M, d, ln, s, bf);
+    return launch_layer_norm(hp.dtype, xprime, GPT2_FP32, p->ln2_g, p->ln2_b, M, d, ln, s, bf,
+                             nullptr, c->env.err);
   });
   if (st) return st;
 
@@ -807,7 +808,7 @@ int forward_trunk(gpt2_ctx* c, const int32_t* ids, int B, int T, const gpt2_para
     *fl = 0;
     *by = static_cast<double>(M) * d * (4 + es) + conversion_bytes(conv);
     return launch_layer_norm(hp.dtype, H, GPT2_FP32, params->lnf_g, params->lnf_b, M, d, ln, s,
-                             bf, conv.count ? &conv : nullptr);
+                             bf, conv.count ? &conv : nullptr, c->env.err);
   });
 }
 

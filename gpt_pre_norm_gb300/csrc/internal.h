@@ -130,10 +130,12 @@ struct ConvSegs {
 // LayerNorm rows of d: x fp32 or bf16 -> y (mode BF16: bf16, or fp16 when
 // y_f16; g, b bf16) or fp32 (mode FP32).  `side`, if given, is a weight
 // conversion done by extra blocks of the same launch (both are memory-bound
-// and too small to fill the GPU's memory pipeline alone).
+// and too small to fill the GPU's memory pipeline alone).  With `err`, an fp16
+// output or converted weight past the fp16 range (or not finite) raises the
+// range bit.
 int launch_layer_norm(int mode, const void* x, int x_dtype, const void* g, const void* b, int rows,
                       int d, void* y, cudaStream_t stream, bool y_f16 = false,
-                      const ConvSegs* side = nullptr);
+                      const ConvSegs* side = nullptr, unsigned* err = nullptr);
 
 
 // Per token t < n_tok: merges the n_vblk partials of kEpiHeadLoss into

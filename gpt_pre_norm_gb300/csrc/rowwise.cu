@@ -12,6 +12,8 @@
 // The embedding follows "GPT-2 Full Forward Pass", "How it works":
 // H0[b, t] = wte[ids[b, t]] + wpe[T_past + t], written in fp32 (the residual
 // stream).  One warp per token, 16-byte loads.
+#include <type_traits>
+
 #include "device.cuh"
 #include "internal.h"
 
@@ -43,6 +45,22 @@ __device__ __forceinline__ void store2(__half* p, float a, float b) {
   *reinterpret_cast<uint32_t*>(p) = pack_f16x2(a, b);
 }
 
+// Stores that also keep the magnitude test of fp16 outputs (the bits of the
+// packed halves, see fp16_max_mag); other output types store only.
+template <typename TY>
+__device__ __forceinline__ void store2c(TY* p, float a, float b, uint32_t&) {
+  store2(p, a, b);
+}
+__device__ __forceinline__ void store2c(__half* p, float a, float b, uint32_t& mag) {
+  const uint32_t w = pack_f16x2(a, b);
+  mag = fp16_max_mag(mag, w);
+  *reinterpret_cast<uint32_t*>(p) = w;
+}
+__device__ __forceinline__ void report_range(uint32_t mag, unsigned* err) {
+  if (__any_sync(0xffffffffu, fp16_nonfinite(mag)) && (threadIdx.x & 31) == 0)
+    raise_error(err, kErrRange);
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
@@ -67,10 +85,12 @@ struct ConvJob {
   long long n[kMaxConvSegs];
   int first[kMaxConvSegs + 1];  // first[count] = blocks in all
   int count;
+  unsigned* err;  // range bit: a value past the fp16 range (the LayerNorm's too)
 };
 
-ConvJob make_conv_job(const ConvSegs* segs) {
+ConvJob make_conv_job(const ConvSegs* segs, unsigned* err) {
   ConvJob j{};
+  j.err = err;
   j.count = segs ? segs->count : 0;
   for (int i = 0; i < j.count; ++i) {
     j.src[i] = segs->src[i];
@@ -84,6 +104,8 @@ ConvJob make_conv_job(const ConvSegs* segs) {
 }
 
 // Block b of a conversion job: all of its loads are issued before any store.
+// A bf16 value whose magnitude exceeds 65504 becomes an fp16 infinity: that
+// raises the range bit (the products would use infinite weights).
 __device__ __forceinline__ void convert_part(const ConvJob& job, int b) {
   int i = 0;
   while (i + 1 < job.count && b >= job.first[i + 1]) ++i;
@@ -97,17 +119,28 @@ __device__ __forceinline__ void convert_part(const ConvJob& job, int b) {
     const long long c = c0 + static_cast<long long>(k) * kRowThreads;
     if (c < n8) v[k] = src[c];
   }
+  uint32_t mag = 0u;
 #pragma unroll
   for (int k = 0; k < kConvChunks; ++k) {
     const long long c = c0 + static_cast<long long>(k) * kRowThreads;
-    if (c < n8) dst[c] = bf16x8_to_f16x8(v[k]);
+    if (c < n8) {
+      const uint4 h = bf16x8_to_f16x8(v[k]);
+      mag = fp16_max_mag(fp16_max_mag(mag, h.x), h.y);
+      mag = fp16_max_mag(fp16_max_mag(mag, h.z), h.w);
+      dst[c] = h;
+    }
   }
   if (b == job.first[i + 1] - 1) {  // the array's last block: its ragged tail
     const bf16* s1 = job.src[i];
     __half* d1 = job.dst[i];
-    for (long long e = n8 * 8 + threadIdx.x; e < n; e += kRowThreads)
-      d1[e] = __float2half_rn(__bfloat162float(s1[e]));
+    for (long long e = n8 * 8 + threadIdx.x; e < n; e += kRowThreads) {
+      const __half h = __float2half_rn(__bfloat162float(s1[e]));
+      mag = fp16_max_mag(mag, static_cast<uint32_t>(__half_as_ushort(h)));
+      d1[e] = h;
+    }
   }
+  if (__any_sync(0xffffffffu, fp16_nonfinite(mag)) && (threadIdx.x & 31) == 0)
+    raise_error(job.err, kErrRange);
 }
 
 // Row held in registers: NP pairs per lane, d <= 64 * NP, d even (the form
@@ -153,6 +186,7 @@ __global__ void __launch_bounds__(kRowThreads)
   const float s = warp_sum(sq) * inv_d;
   const float rstd = rsqrtf(s + kLnEps);
   TY* yr = y + static_cast<size_t>(row) * d;
+  uint32_t mag = 0u;
 #pragma unroll
   for (int i = 0; i < NP; ++i) {
     const int c = 2 * (lane + 32 * i);
@@ -160,9 +194,10 @@ __global__ void __launch_bounds__(kRowThreads)
       float g0, g1, b0, b1;
       load2(g + c, g0, g1);
       load2(b + c, b0, b1);
-      store2(yr + c, (v[2 * i] - u) * rstd * g0 + b0, (v[2 * i + 1] - u) * rstd * g1 + b1);
+      store2c(yr + c, (v[2 * i] - u) * rstd * g0 + b0, (v[2 * i + 1] - u) * rstd * g1 + b1, mag);
     }
   }
+  report_range(mag, side.err);
 }
 
 // Eight consecutive row values <-> registers with 16-byte accesses.
@@ -190,6 +225,17 @@ __device__ __forceinline__ void store8(bf16* p, const float* v) {
 __device__ __forceinline__ void store8(__half* p, const float* v) {
   *reinterpret_cast<uint4*>(p) = make_uint4(pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]),
                                             pack_f16x2(v[4], v[5]), pack_f16x2(v[6], v[7]));
+}
+template <typename TY>
+__device__ __forceinline__ void store8c(TY* p, const float* v, uint32_t&) {
+  store8(p, v);
+}
+__device__ __forceinline__ void store8c(__half* p, const float* v, uint32_t& mag) {
+  const uint4 w = make_uint4(pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]),
+                             pack_f16x2(v[4], v[5]), pack_f16x2(v[6], v[7]));
+  mag = fp16_max_mag(fp16_max_mag(mag, w.x), w.y);
+  mag = fp16_max_mag(fp16_max_mag(mag, w.z), w.w);
+  *reinterpret_cast<uint4*>(p) = w;
 }
 
 // Row held in registers as NC groups of eight values per lane (group
@@ -241,6 +287,7 @@ __global__ void __launch_bounds__(kRowThreads, NC <= 3 ? 6 : (NC <= 4 ? 5 : 3))
   }
   const float rstd = rsqrtf(warp_sum(sq) * inv_d + kLnEps);
   TY* yr = y + static_cast<size_t>(row) * d;
+  uint32_t mag = 0u;
 #pragma unroll
   for (int i = 0; i < NC; ++i) {
     const int gi = lane + 32 * i;
@@ -250,9 +297,10 @@ __global__ void __launch_bounds__(kRowThreads, NC <= 3 ? 6 : (NC <= 4 ? 5 : 3))
       load8(b + 8 * gi, bb);
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] = (v[8 * i + e] - u) * rstd * gg[e] + bb[e];
-      store8(yr + 8 * gi, o);
+      store8c(yr + 8 * gi, o, mag);
     }
   }
+  report_range(mag, side.err);
 }
 
 __device__ __forceinline__ float ld1(const float* p) { return *p; }
@@ -287,7 +335,14 @@ __global__ void __launch_bounds__(kRowThreads)
   }
   const float rstd = rsqrtf(warp_sum(sq) / static_cast<float>(d) + kLnEps);
   TY* yr = y + static_cast<size_t>(row) * d;
-  for (int c = lane; c < d; c += 32) st1(yr + c, (ld1(xr + c) - u) * rstd * ld1(g + c) + ld1(b + c));
+  uint32_t mag = 0u;
+  for (int c = lane; c < d; c += 32) {
+    const float o = (ld1(xr + c) - u) * rstd * ld1(g + c) + ld1(b + c);
+    st1(yr + c, o);
+    if constexpr (sizeof(TY) == 2 && !std::is_same<TY, bf16>::value)
+      mag = fp16_max_mag(mag, static_cast<uint32_t>(__half_as_ushort(__float2half_rn(o))));
+  }
+  report_range(mag, side.err);
 }
 
 __host__ __device__ inline bool aligned16(const void* p) {
@@ -503,10 +558,11 @@ int launch_head_loss_combine(const float* part_m, const float* part_s, const int
 }
 
 int launch_layer_norm(int mode, const void* x, int x_dtype, const void* g, const void* b, int rows,
-                      int d, void* y, cudaStream_t stream, bool y_f16, const ConvSegs* side) {
+                      int d, void* y, cudaStream_t stream, bool y_f16, const ConvSegs* side,
+                      unsigned* err) {
   if (rows <= 0 || d <= 0) return GPT2_ERR_INVALID_ARG;
   if (side && (side->count < 0 || side->count > kMaxConvSegs)) return GPT2_ERR_INVALID_ARG;
-  const ConvJob job = make_conv_job(side);
+  const ConvJob job = make_conv_job(side, err);
   if (mode == GPT2_BF16) {
     if (d % 2 != 0) return GPT2_ERR_UNSUPPORTED;
     const bf16* gg = static_cast<const bf16*>(g);

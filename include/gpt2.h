@@ -24,7 +24,8 @@
  * Conventions common to every entry point:
  *   - Return value: a gpt2_status.  On any validation error nothing is
  *     launched and no memory is touched.  Errors raised inside a kernel
- *     (a bounded wait that ran out) surface at gpt2_sync_status.
+ *     (a bounded wait that ran out, a token id out of range, a value past
+ *     the fp16 operand range) surface at gpt2_sync_status.
  *   - Asynchrony: work is enqueued on `stream` (a cudaStream_t value; NULL is
  *     the legacy default stream) and the call returns before it completes.
  *   - Dtypes: in GPT2_BF16 mode parameters, the block input/output and the KV
@@ -35,7 +36,9 @@
  *     accumulates in fp32 and the residual stream is fp32.  (fp16 operands
  *     carry 3 more mantissa bits than bf16; with bf16 operands the tied-head
  *     argmax of random-weight models agrees with exact arithmetic at only
- *     ~99.1% of positions, with fp16 operands at ~99.7%.)  In GPT2_FP32 mode
+ *     ~99.1% of positions, with fp16 operands at ~99.7%.)  A weight or an
+ *     activation past the fp16 range is reported as GPT2_ERR_RANGE by
+ *     gpt2_sync_status, never rounded to infinity silently.  In GPT2_FP32 mode
  *     everything is fp32.  Logits are always fp32.  Token ids are int32.
  *   - Layouts are dense row-major C order.  Linear weights are [out, in]
  *     (the nn.Linear convention); c_attn rows are Q | K | V, head j taking
@@ -131,8 +134,13 @@ int gpt2_ctx_create(const gpt2_hparams *hp, int max_B, int max_T, void *workspac
 void gpt2_ctx_destroy(gpt2_ctx *ctx);
 
 /* Waits for `stream`, then reads and clears the context's device error
- * word: GPT2_OK, GPT2_ERR_DEVICE_TIMEOUT, or GPT2_ERR_CUDA for a failed
- * launch or an asynchronous CUDA error.                                    */
+ * word: GPT2_OK, GPT2_ERR_DEVICE_TIMEOUT (a bounded wait ran out),
+ * GPT2_ERR_INVALID_ARG (a token id outside [0, n_vocab)), GPT2_ERR_RANGE (in
+ * bf16 mode, a value past the fp16 range of the products' operands: a weight
+ * with |w| > 65504, or a LayerNorm, attention or GELU output beyond 65504 or
+ * not finite; the outputs of that call are not to be trusted), or
+ * GPT2_ERR_CUDA for a failed launch or an asynchronous CUDA error.  When
+ * several bits are set the first of that list is returned.                 */
 int gpt2_sync_status(gpt2_ctx *ctx, void *stream);
 
 /* bf16 mode converts each weight matrix to an fp16 working copy (in the
