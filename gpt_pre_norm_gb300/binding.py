@@ -89,6 +89,7 @@ def _load() -> C.CDLL:
         "gpt2_attention_decode_noalloc": (I, [P, P, I, I, I, I, I, I, P, P]),
         "gpt2_ctx_cache_weights": (I, [P, I]),
         "gpt2_selftest_wait_timeout": (I, [P, I, P]),
+        "gpt2_ctx_set_wait_limit": (I, [P, LL]),
         "gpt2_generate_greedy": (I, [P, P, I, I, C.POINTER(gpt2_params), I, C.POINTER(gpt2_kv), I,
                                      P, P, P]),
         "gpt2_profile_enable": (I, [P, I]),
@@ -357,6 +358,11 @@ def gpt2_selftest_wait_timeout(ctx: Context, limit_us: int, stream=None) -> None
     gpt2_sync_status reports GPT2_ERR_DEVICE_TIMEOUT."""
     _check(LIB.gpt2_selftest_wait_timeout(ctx.handle, limit_us, _stream(stream)),
            "gpt2_selftest_wait_timeout")
+
+
+def gpt2_ctx_set_wait_limit(ctx: Context, limit_ns: int) -> None:
+    """Limit of the kernels' bounded waits (test support; <= 0 restores 2 s)."""
+    _check(LIB.gpt2_ctx_set_wait_limit(ctx.handle, int(limit_ns)), "gpt2_ctx_set_wait_limit")
 
 
 def gpt2_profile_enable(ctx: Context, enable: bool) -> None:

@@ -93,12 +93,29 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Limits below this are a test setting (see gpt2_ctx_set_wait_limit): the
+// wait then polls without blocking, so that the limit is observed even where
+// one blocking try_wait would outlast it.
+constexpr unsigned long long kShortWaitNs = 1000000ull;  // 1 ms
+
 // Waits for the phase of parity `parity` to complete.  Gives up (returns
 // false) when *abort becomes non-zero or after limit_ns (default kWaitLimitNs);
 // on a timeout it sets *abort and the kErrTimeout bit of the error word.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort, unsigned* err,
                                                   unsigned long long limit_ns = kWaitLimitNs) {
+  if (limit_ns < kShortWaitNs) {
+    const unsigned long long t0 = global_timer_ns();
+    for (;;) {
+      if (mbar_test_wait(bar, parity)) return true;
+      if (abort && *abort) return false;
+      if (global_timer_ns() - t0 > limit_ns) {
+        if (abort) *abort = 1;
+        raise_error(err, kErrTimeout);
+        return false;
+      }
+    }
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {

@@ -106,6 +106,7 @@ struct GemmArgs {
   int out_f16;       // 16-bit outputs of kEpiBias / kEpiGelu are fp16 (else bf16)
   uint32_t idesc;    // tcgen05.mma instruction descriptor (operand kind, tile)
   unsigned* err;
+  unsigned long long wait_ns;  // limit of each bounded wait (the drains keep 2 s)
   EpiParams ep;
 };
 
@@ -443,10 +444,12 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int row0, int ncol
       for (int i = 0; i < 4; ++i) unpack8(*reinterpret_cast<const uint4*>(bias_s + c + 8 * i), bv + 8 * i);
       tmem_ld_wait();
       if (tma_resid) {
-        if (mbar_wait_bounded(&rbar[slot], (s.rpar >> slot) & 1u, abort_flag, a.err)) {
-          s.rpar ^= 1u << slot;
-          s.inflight &= ~(1u << slot);
-        }
+        // A wait that runs out ends this tile's epilogue: the load stays
+        // marked in flight, and the CTA's final drain waits for it.
+        if (!mbar_wait_bounded(&rbar[slot], (s.rpar >> slot) & 1u, abort_flag, a.err, a.wait_ns))
+          return;
+        s.rpar ^= 1u << slot;
+        s.inflight &= ~(1u << slot);
         box_read_f32(rb, lane, rv);
         if constexpr (KIND == kEpiResidBf16Out) {
           // The box is free again: fetch the residual of chunk c+2 into it.
@@ -655,7 +658,7 @@ __global__ void __launch_bounds__(epi_threads(KIND), 1)
       const int a_row = m_blk * tile_rows + static_cast<int>(rank) * kBM;
       const int b_row = n_blk * BN + static_cast<int>(rank) * (BN / CG);
       for (int kb = 0; kb < KB; ++kb) {
-        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.err)) {
+        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, args.err, args.wait_ns)) {
           ok = false;
           break;
         }
@@ -679,12 +682,16 @@ __global__ void __launch_bounds__(epi_threads(KIND), 1)
       }
     }
     if (!ok && rank == 0) {
-      // Drain: every copy already issued must land before the CTA exits.  (A
-      // pair's second CTA cannot wait on the first CTA's barriers; after an
-      // abort its copies land long before the closing cluster barrier, which
-      // waits for the first CTA's bounded waits to run out.)
+      // Drain: every copy already issued must land before the CTA exits.
       for (int s = 0; s < S; ++s)
-        if ((issued >> s) & 1u) mbar_wait_bounded(&full[s], (issued_par >> s) & 1u, nullptr, args.err);
+        if ((issued >> s) & 1u)
+          mbar_wait_bounded(&full[s], (issued_par >> s) & 1u, nullptr, args.err);
+    } else if (!ok) {
+      // A pair's second CTA cannot wait on the first CTA's barriers, which
+      // count its copies: it lets 50 us pass (a copy lands within
+      // microseconds) before going on to the closing cluster barrier.
+      const unsigned long long t0 = global_timer_ns();
+      while (global_timer_ns() - t0 < 50000ull) __nanosleep(1000);
     }
   } else if (warp == 1 && lane == 0 && rank == 0) {
     // ------------------------------------------------------- MMA issuer --
@@ -696,11 +703,12 @@ __global__ void __launch_bounds__(epi_threads(KIND), 1)
     for (int tile = first_tile; ok && tile < args.num_tiles; tile += tile_step, ++it) {
       const int acc = it & 1;
       const uint32_t acc_par = static_cast<uint32_t>((it >> 1) & 1);
-      if (!mbar_wait_bounded(&tempty[acc], acc_par ^ 1u, abort_flag, args.err)) break;
+      if (!mbar_wait_bounded(&tempty[acc], acc_par ^ 1u, abort_flag, args.err, args.wait_ns))
+        break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 256);
       for (int kb = 0; kb < KB; ++kb) {
-        if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.err)) {
+        if (!mbar_wait_bounded(&full[stage], phase, abort_flag, args.err, args.wait_ns)) {
           ok = false;
           break;
         }
@@ -763,8 +771,9 @@ __global__ void __launch_bounds__(epi_threads(KIND), 1)
       const int row0 = m_blk * tile_rows + static_cast<int>(rank) * kBM + quarter * 32;
       const int ncol0 = n_blk * BN + half * ncols;
       uint16_t* bias_s = bias_half + (it % kBiasBufs) * (256 / (kEpiWarps / 4));
+      if (*abort_flag) break;  // a wait of this CTA ran out: no new loads
       epilogue_prefetch<KIND>(row0, ncol0, ncols, lane, epi, bias_s, rbar, st, args, &tmR);
-      if (!mbar_wait_bounded(&tfull[acc], acc_par, abort_flag, args.err)) break;
+      if (!mbar_wait_bounded(&tfull[acc], acc_par, abort_flag, args.err, args.wait_ns)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc * 256 + half * ncols);
@@ -980,6 +989,7 @@ int launch_gemm_tc(const LaunchEnv& env, int kind_in, const void* A_in, const vo
   args.out_f16 = out_f16 ? 1 : 0;
   args.idesc = umma_idesc_16(kBM * cg, BN, operands_f16);
   args.err = env.err;
+  args.wait_ns = env.wait_ns;
   args.ep = ep;
   if (kind == kEpiBias || kind == kEpiGelu)
     args.tma_out = encode_box32(env, &tmO, ep.out, false, M, N, ep.ldo, out_f16);

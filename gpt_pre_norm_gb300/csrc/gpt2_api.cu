@@ -578,6 +578,12 @@ int gpt2_selftest_wait_timeout(gpt2_ctx* c, int limit_us, void* stream) {
   return cudaGetLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
+int gpt2_ctx_set_wait_limit(gpt2_ctx* c, long long limit_ns) {
+  if (!c) return GPT2_ERR_INVALID_ARG;
+  c->env.wait_ns = limit_ns > 0 ? static_cast<unsigned long long>(limit_ns) : kWaitLimitNs;
+  return GPT2_OK;
+}
+
 int gpt2_sync_status(gpt2_ctx* c, void* stream) {
   if (!c) return GPT2_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -313,6 +313,18 @@ int gpt2_embed(gpt2_ctx *ctx, const int32_t *ids, const void *wte, const void *w
  * Errors: INVALID_ARG (null ctx, limit_us outside 1 .. 1000000), CUDA.      */
 int gpt2_selftest_wait_timeout(gpt2_ctx *ctx, int limit_us, void *stream);
 
+/* Sets the limit of the bounded waits inside the tensor-core GEMM and the
+ * prefill attention launched through `ctx` (limit_ns > 0), or restores the
+ * default of 2 s (limit_ns <= 0).  Test support, no counterpart on the pages:
+ * a limit of a few nanoseconds makes the first wait that is not already
+ * satisfied run out, so the kernels' failure path (raise the error word,
+ * drain the copies already issued, retire the issued MMAs, free TMEM,
+ * return) runs on real work; the next gpt2_sync_status then reports
+ * GPT2_ERR_DEVICE_TIMEOUT, and with the default restored the context computes
+ * normally again.  The waits that drain copies keep the 2 s limit.
+ * Errors: INVALID_ARG (null ctx).                                          */
+int gpt2_ctx_set_wait_limit(gpt2_ctx *ctx, long long limit_ns);
+
 /* ---------------------------------------------------------- profiling ---- */
 
 /* When enabled, every kernel launch the context makes is bracketed by CUDA

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(G):
 
 
 def test_status_strings(G):
-    for s in range(0, 9):
+    for s in range(0, 10):
         assert G.status_string(s) and G.status_string(s) != "unknown status"
     assert G.status_string(99) == "unknown status"
 
@@ -131,6 +131,7 @@ def test_profiler_kinds_and_null_context(G):
                                    C.byref(d3)) == G.GPT2_ERR_INVALID_ARG
     assert G.LIB.gpt2_profile_reset(None) == G.GPT2_ERR_INVALID_ARG
     assert G.LIB.gpt2_selftest_wait_timeout(None, 1000, None) == G.GPT2_ERR_INVALID_ARG
+    assert G.LIB.gpt2_ctx_set_wait_limit(None, 1000) == G.GPT2_ERR_INVALID_ARG
 
 
 def test_binding_refuses_to_load_without_the_library():
