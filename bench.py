@@ -108,7 +108,8 @@ def source_digest(files):
 
 
 KERNEL_SOURCES = {
-    "gemm": ["gpt_pre_norm_gb300/csrc/gemm_tc.cu", "gpt_pre_norm_gb300/csrc/device.cuh"],
+    "gemm": ["gpt_pre_norm_gb300/csrc/gemm_tc.cu", "gpt_pre_norm_gb300/csrc/gemm_smallm.cu",
+             "gpt_pre_norm_gb300/csrc/device.cuh"],
     "attention": ["gpt_pre_norm_gb300/csrc/attn_tc.cu", "gpt_pre_norm_gb300/csrc/attention.cu",
                   "gpt_pre_norm_gb300/csrc/device.cuh"],
     "row": ["gpt_pre_norm_gb300/csrc/rowwise.cu", "gpt_pre_norm_gb300/csrc/device.cuh"],
