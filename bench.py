@@ -12,18 +12,21 @@ one cached decode step.  The default workload is the GPT-2-small block
 (d=768, 12 heads, B=8, T=1024, bf16 storage, fp32 accumulate).
 
 Timing: W untimed warm-up steps, then K steps each bracketed by CUDA events
-on the launching stream, with L2 flushed (a 256 MiB device write) between
-steps; a barrier and a device synchronize bracket the K steps; the per-step
-time is the maximum over ranks.  Under torchrun each rank runs an independent
+on the launching stream; a barrier and a device synchronize bracket the K
+steps; the per-step time is the maximum over ranks.  No step finds its inputs
+in L2: the inputs of every workload are larger than L2.  The block workloads
+rotate over R copies of their parameters and input (R x (weights + x) >= 2 x
+L2, every copy read once per R steps); the full forward reads 250 MB of
+weights and decode 3.3 GB of cached keys and values per step.  Under torchrun each rank runs an independent
 replica of the workload (the forward has no cross-sequence exchange), so the
 whole-job value is the sum of the ranks' tokens over the slowest rank's time.
 
 One JSON line is printed by rank 0.  Beside the device-timed value it carries:
   e2e         the same metric through the C ABI with pinned host buffers: every
               step copies its input from pinned host memory and its result
-              back; steps are pipelined over two device buffers (copies on
-              their own streams overlap the previous step's compute) and the
-              L2 flush runs inside the timed region;
+              back; steps are pipelined over the device input/result slots
+              (copies on their own streams overlap the neighbouring steps'
+              compute), every copy inside the timed region;
   workloads   the other configurations timed in the same run (the full
               GPT-2-small forward, the GPT-2-XL-shaped block, cached decode
               of the GPT-2-medium shape), each with its step time, tokens/s,
@@ -69,7 +72,7 @@ METRIC = "GPT-2 block/full-forward tokens/s at 1 GB300; achieved TFLOP/s vs bf16
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 TENSOR_KINDS = {"gemm_c_attn", "gemm_c_proj", "gemm_c_fc", "gemm_mlp_c_proj", "gemm_lm_head",
                 "gemm_other", "attention_prefill"}
-L2_FLUSH_BYTES = 256 << 20
+L2_BYTES_FALLBACK = 126 << 20  # GB300
 # Configurations timed beside the default one (the GPT-2-small block).
 EXTRA_WORKLOADS = ("forward_bf16_gpt2_small", "block_bf16_d1600", "decode_bf16_gpt2_medium")
 # What the bf16 path computes in.
@@ -218,6 +221,15 @@ def workload_flops(w: S.Workload) -> float:
     return w.n_layer * per_layer + 2.0 * B * T * d * w.n_vocab
 
 
+def l2_bytes(torch, device) -> int:
+    props = torch.cuda.get_device_properties(device)
+    return int(getattr(props, "L2_cache_size", 0) or L2_BYTES_FALLBACK)
+
+
+def nbytes(tensors) -> int:
+    return sum(t.numel() * t.element_size() for t in tensors)
+
+
 def to_dev_bf16(a: np.ndarray, torch, device):
     bits = S.bf16_bits(a).view(np.int16)
     return torch.from_numpy(bits).to(device).view(torch.bfloat16)
@@ -228,9 +240,14 @@ class Runner:
 
     Host-side generation of the synthetic weights (and of the decode
     workload's 1.6e9-value KV cache) runs on a thread pool: each tensor has
-    its own random stream, so the values do not depend on the pool."""
+    its own random stream, so the values do not depend on the pool.
 
-    def __init__(self, w: S.Workload, seed: int, device, pool: ThreadPoolExecutor):
+    Step i uses input/result slot i % slots.  A block workload's inputs (its
+    weights and x) are smaller than L2, so it keeps `slots` copies of both,
+    enough that all copies together are at least twice the L2 size: a copy
+    is read again only after the others have been, and is gone from L2."""
+
+    def __init__(self, w: S.Workload, seed: int, device, pool: ThreadPoolExecutor, l2: int):
         import torch
         from gpt_pre_norm_gb300 import binding as G
         self.G, self.torch, self.w, self.device = G, torch, w, device
@@ -245,24 +262,35 @@ class Runner:
         self.tokens = w.B * w.T
         self.cache = None
         self.graph = None
-        # Two device buffers for each step input and result, so that the
-        # end-to-end steps can overlap copies with the previous step's compute;
-        # a step replayed from a CUDA graph has fixed buffers (one slot).
+        # At least two device buffers for each step input and result, so that
+        # the end-to-end steps can overlap copies with the neighbouring steps'
+        # compute; a step replayed from a CUDA graph has fixed buffers (one slot).
         self.slots = 2
         if w.kind == "block":
-            p = S.block_params(w, seed)
-            self.params = {k: todev(v) for k, v in p.items()}
+            p = {k: todev(v) for k, v in S.block_params(w, seed).items()}
             x = todev(S.block_input(w, seed))
-            self.inp = [{"x": x}, {"x": torch.empty_like(x)}]
-            self.res = [torch.empty_like(x) for _ in range(2)]
+            per_copy = nbytes(p.values()) + nbytes([x])
+            self.slots = max(2, -(-2 * l2 // per_copy))
+            self.params = [p] + [{k: v.clone() for k, v in p.items()}
+                                 for _ in range(self.slots - 1)]
+            self.inp = [{"x": x}] + [{"x": x.clone()} for _ in range(self.slots - 1)]
+            self.res = [torch.empty_like(x) for _ in range(self.slots)]
             self.inp_host = {"x": x.cpu().pin_memory()}
-            self.res_host = [torch.empty(x.shape, dtype=dt).pin_memory() for _ in range(2)]
+            self.res_host = [torch.empty(x.shape, dtype=dt).pin_memory()
+                             for _ in range(self.slots)]
+            self.l2_note = (f"inputs larger than L2, no flush: {self.slots} copies of the "
+                            f"weights and x ({per_copy / 1e6:.1f} MB each) rotated, "
+                            f"{self.slots * per_copy / 1e6:.0f} MB >= 2 x L2")
             return
         blocks = list(pool.map(lambda layer: S.block_params(w, seed, layer), range(w.n_layer)))
         p = S.embeddings(w, seed)
         tp = {k: todev(p[k]) for k in ("wte", "wpe", "lnf_g", "lnf_b")}
         tp["blocks"] = [{k: todev(v) for k, v in b.items()} for b in blocks]
         self.mp = G.ModelParams(tp)
+        weights = nbytes([tp[k] for k in ("wte", "wpe", "lnf_g", "lnf_b")]) + \
+            sum(nbytes(b.values()) for b in tp["blocks"])
+        self.l2_note = (f"inputs larger than L2, no flush: {weights / 1e6:.0f} MB of weights "
+                        "read every step")
         ids = S.token_ids(w, seed)
         ids_dev = torch.from_numpy(ids).to(device)
         self.inp = [{"ids": ids_dev}, {"ids": torch.empty_like(ids_dev)}]
@@ -297,13 +325,19 @@ class Runner:
 
             list(pool.map(fill, [(b, layer) for b in range(w.B) for layer in range(w.n_layer)]))
             self.cache = G.KV(host.to(device).view(torch.bfloat16), w.t_past)
+            kv_read = 2 * w.B * w.n_layer * 2 * w.n_head * w.t_past * w.d_h
+            self.l2_note = (f"inputs larger than L2, no flush: {kv_read / 1e9:.1f} GB of cached "
+                            f"keys and values and {weights / 1e6:.0f} MB of weights read "
+                            "every step")
 
     # One step on input/result slot `s`, inputs resident on the device.
     def step(self, s: int = 0):
         G, w = self.G, self.w
+        s %= self.slots
         inp, res = self.inp[s], self.res[s]
         if w.kind == "block":
-            G.gpt2_block_forward(self.ctx, inp["x"], self.params, w.B, w.T, w.d, w.n_head, out=res)
+            G.gpt2_block_forward(self.ctx, inp["x"], self.params[s], w.B, w.T, w.d, w.n_head,
+                                 out=res)
         elif w.kind == "forward":
             G.gpt2_forward(self.ctx, inp["ids"], self.mp, w.B, w.T, logits=res)
         elif w.kind == "forward_loss":
@@ -366,29 +400,28 @@ def job_throughput(tokens_per_rank, world_size, ms_per_step):
     return tokens_per_rank * world_size / (ms_per_step / 1e3)
 
 
-def timed_steps(fn, K, flush, barrier, torch):
+def timed_steps(fn, K, barrier, torch):
+    """Per-step times (ms) of K steps fn(0) .. fn(K - 1), back to back."""
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     barrier()
     torch.cuda.synchronize()
     for i in range(K):
-        flush.zero_()
         starts[i].record()
-        fn()
+        fn(i)
         ends[i].record()
     torch.cuda.synchronize()
     barrier()
     return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
-def timed_e2e(r, K, flush, barrier, torch):
+def timed_e2e(r, K, barrier, torch):
     """Mean time of K end-to-end steps: step i copies its input from pinned
     host memory into device slot i % slots (own stream), runs after that copy
-    and after the L2 flush (compute stream), and copies its result back to
-    pinned host memory (own stream); with two slots the copies of one step
-    overlap the compute of its neighbours.  One event pair brackets all K
-    steps, the last result copy included, so every copy and every flush is
-    inside the timed region."""
+    (compute stream), and copies its result back to pinned host memory (own
+    stream); with two or more slots the copies of one step overlap the compute
+    of its neighbours.  One event pair brackets all K steps, the last result
+    copy included, so every copy is inside the timed region."""
     comp = torch.cuda.current_stream()
     h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
     n = r.slots
@@ -410,7 +443,6 @@ def timed_e2e(r, K, flush, barrier, torch):
             ev_in[i].record(h2d)
         if i >= n:
             comp.wait_event(ev_out[i - n])      # slot s's last result copied out
-        flush.zero_()
         comp.wait_event(ev_in[i])
         r.run(s)
         ev_done[i].record(comp)
@@ -494,16 +526,16 @@ def reference_arm(args, w):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
-            "config": workload_config(w, args),
+            "config": workload_config(w, args, "not applicable: host cores"),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
 
-def workload_config(w, args):
+def workload_config(w, args, l2_note):
     cfg = {"workload": w.name, "kind": w.kind, "d": w.d, "n_head": w.n_head, "B": w.B, "T": w.T,
-           "seed": args.seed, "l2": "flushed between steps (256 MiB device write)",
+           "seed": args.seed, "l2": l2_note,
            "parallelism": f"replicas x{args.gpus}"}
     if w.kind != "block":
         cfg.update(n_layer=w.n_layer, n_vocab=w.n_vocab)
@@ -563,30 +595,30 @@ def roofline_entry(prof, peaks, workload):
     return roof
 
 
-def measure(r, args, flush, barrier, torch, G, e2e: bool):
+def measure(r, args, barrier, torch, G, e2e: bool):
     """Warm-up, K device-resident steps under the clock sampler, (decode) the
     same steps without the graph, (e2e) the pipelined end-to-end steps, and a
     profiled pass of K steps with every kernel bracketed by events."""
     if r.w.kind == "decode":
         r.capture_graph()
-    for _ in range(args.warmup):
-        r.run()
+    for i in range(max(args.warmup, r.slots)):
+        r.run(i)
     torch.cuda.synchronize()
     st = G.gpt2_sync_status(r.ctx)
     if st != G.GPT2_OK:
         raise SystemExit(f"{r.w.name}: device error after warm-up: {G.status_string(st)}")
     out = {}
     with ClockSampler(torch.cuda.current_device()) as clk:
-        out["times"] = timed_steps(r.run, args.steps, flush, barrier, torch)
+        out["times"] = timed_steps(r.run, args.steps, barrier, torch)
     out["clocks"] = clk.summary()
     out["ms_eager"] = None
     if r.graph is not None:
-        t = timed_steps(r.step, args.steps, flush, barrier, torch)
+        t = timed_steps(r.step, args.steps, barrier, torch)
         out["ms_eager"] = sum(t) / len(t)
-    out["ms_e2e"] = timed_e2e(r, args.steps, flush, barrier, torch) if e2e else None
+    out["ms_e2e"] = timed_e2e(r, args.steps, barrier, torch) if e2e else None
     G.gpt2_profile_enable(r.ctx, True)
     G.gpt2_profile_reset(r.ctx)
-    timed_steps(r.step, args.steps, flush, barrier, torch)
+    timed_steps(r.step, args.steps, barrier, torch)
     out["prof"] = G.gpt2_profile_read(r.ctx)
     G.gpt2_profile_enable(r.ctx, False)
     st = G.gpt2_sync_status(r.ctx)
@@ -599,7 +631,7 @@ def workload_entry(w, r, m, peaks, args, ws, device):
     """The summary of one extra configuration for the `workloads` key."""
     ms, ms_med = reduce_over_ranks([sum(m["times"]) / len(m["times"]),
                                     statistics.median(m["times"])], device)
-    e = {"config": workload_config(w, args), "ms_per_step": ms, "ms_per_step_median": ms_med,
+    e = {"config": workload_config(w, args, r.l2_note), "ms_per_step": ms, "ms_per_step_median": ms_med,
          "value": job_throughput(r.tokens, ws, ms), "unit": "tokens/s",
          "tflops": workload_flops(w) * ws / (ms / 1e3) / 1e12,
          "e2e_roofline": e2e_roofline(m["prof"], peaks, args.steps, ms),
@@ -648,17 +680,18 @@ def main():
 
     from gpt_pre_norm_gb300 import binding as G
     pool = ThreadPoolExecutor(max_workers=os.cpu_count() or 4)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    l2 = l2_bytes(torch, device)
     peaks = load_peaks()
 
-    r = Runner(w, args.seed + rank, device, pool)
-    m = measure(r, args, flush, barrier, torch, G, e2e=True)
+    r = Runner(w, args.seed + rank, device, pool, l2)
+    m = measure(r, args, barrier, torch, G, e2e=True)
     times, prof = m["times"], m["prof"]
     ms, ms_e2e, ms_med = reduce_over_ranks(
         [sum(times) / len(times), m["ms_e2e"], statistics.median(times)], device)
     ms_eager = reduce_over_ranks([m["ms_eager"]], device)[0] if m["ms_eager"] is not None else None
     tokens_rank = r.tokens
     h2d, d2h = r.e2e_bytes()
+    l2_note, slots = r.l2_note, r.slots
     r.close()
     del r
     gc.collect()
@@ -667,8 +700,8 @@ def main():
     # The other configurations, one after the other (each rank a replica).
     extra_entries = {}
     for we in extras:
-        re_ = Runner(we, args.seed + rank, device, pool)
-        me = measure(re_, args, flush, barrier, torch, G, e2e=False)
+        re_ = Runner(we, args.seed + rank, device, pool, l2)
+        me = measure(re_, args, barrier, torch, G, e2e=False)
         extra_entries[we.name] = workload_entry(we, re_, me, peaks, args, ws, device)
         re_.close()
         del re_
@@ -688,15 +721,15 @@ def main():
         "dtype": "bf16/fp16" if w.dtype == "bf16" else "f32",
         "dtype_detail": DTYPE_DETAIL if w.dtype == "bf16" else "fp32 storage and arithmetic",
         "data": "synthetic",
-        "config": workload_config(w, args),
+        "config": workload_config(w, args, l2_note),
         "tflops": flops * ws / (ms / 1e3) / 1e12,
         "tflops_frac_of_bf16_peak": flops * ws / (ms / 1e3) / 1e12 / peaks["bf16_tflops"],
         "roofline": roofline_entry(prof, peaks, w.name),
         "e2e_roofline": e2e_roofline(prof, peaks, args.steps, ms),
         "e2e": {"value": job_throughput(tokens_rank, ws, ms_e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "pipelined": "two device buffers; copies on their own streams; "
-                             "L2 flush inside the timed region"},
+                "pipelined": f"{slots} device input/result slots; copies on their own "
+                             "streams"},
         "gpu_launches": int(round(sum(v["launches"] for v in prof.values()))),
         "clocks": m["clocks"],
         "kernels": kernel_table(prof, peaks, args.steps),

@@ -17,6 +17,10 @@
 //     epilogue (bias, GELU, residual, Q/K/V split) is applied once;
 //     when K spans several chunks, the chunks add into the fp32 residual with
 //     atomics (in-place residual epilogue only).
+//
+// Early weights: when W was written before the current call began, its loads
+// are issued before the wait on the previous kernel, so the weight stream
+// overlaps that kernel's tail.
 #include "device.cuh"
 #include "internal.h"
 
@@ -39,6 +43,7 @@ struct SmallArgs {
   int M, N, K;
   unsigned* err;
   EpiParams ep;
+  int w_early;  // W may be read before the previous kernel completes
 };
 
 // 16-byte chunk c (0..7) of row r in a 128-byte-swizzled box row.
@@ -78,16 +83,21 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
   __syncthreads();
   pdl_trigger();
-  pdl_wait();
-  // Every box of the CTA at once; boxes past M / N / K read as zero.
+  // Every box of the CTA at once, on one barrier; boxes past M / N / K read
+  // as zero.  W first, and before the wait on the previous kernel when W was
+  // written before this call began (it is not produced by that kernel).
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmX);
     tma_prefetch_desc(&tmW);
-    mbar_arrive_expect_tx(bar, kBoxes * (kXBox + kWBox));
-    for (int j = 0; j < kBoxes; ++j) {
-      tma_load_2d(sX + j * kXBox, &tmX, bar, k0 + j * kBoxK, 0);
-      tma_load_2d(sW + j * kWBox, &tmW, bar, k0 + j * kBoxK, f0);
-    }
+    mbar_arrive_expect_tx(bar, kBoxes * (kWBox + kXBox));
+    if (a.w_early)
+      for (int j = 0; j < kBoxes; ++j) tma_load_2d(sW + j * kWBox, &tmW, bar, k0 + j * kBoxK, f0);
+  }
+  pdl_wait();
+  if (threadIdx.x == 0) {
+    if (!a.w_early)
+      for (int j = 0; j < kBoxes; ++j) tma_load_2d(sW + j * kWBox, &tmW, bar, k0 + j * kBoxK, f0);
+    for (int j = 0; j < kBoxes; ++j) tma_load_2d(sX + j * kXBox, &tmX, bar, k0 + j * kBoxK, 0);
   }
   mbar_wait_bounded(bar, 0, nullptr, a.err);
 
@@ -210,14 +220,14 @@ bool smallm_supported(int kind, int M, int K) {
 
 int launch_gemm_smallm(const LaunchEnv& env, int kind, const __half* X, const __half* W, int M,
                        int N, int K, const EpiParams& ep, cudaStream_t stream, double* flops,
-                       double* bytes) {
+                       double* bytes, bool w_early) {
   if (!smallm_supported(kind, M, K) || N <= 0) return GPT2_ERR_UNSUPPORTED;
   const int chunks = (K + kKChunk - 1) / kKChunk;
   if (chunks > 1 && (kind != kEpiResidF32 || ep.out != ep.resid)) return GPT2_ERR_UNSUPPORTED;
   CUtensorMap tmX, tmW;
   if (!encode_rows_f16(env, &tmX, X, M, K, kTok) || !encode_rows_f16(env, &tmW, W, N, K, kFeat))
     return GPT2_ERR_CUDA;
-  SmallArgs a{M, N, K, env.err, ep};
+  SmallArgs a{M, N, K, env.err, ep, w_early ? 1 : 0};
   const dim3 grid((N + kFeat - 1) / kFeat, chunks);
   cudaError_t e;
   switch (kind) {

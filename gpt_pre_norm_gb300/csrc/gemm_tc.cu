@@ -1023,7 +1023,7 @@ int launch_gemm_tc(const LaunchEnv& env, int kind_in, const void* A_in, const vo
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].val.programmaticStreamSerializationAllowed = take_pdl_permission() ? 1 : 0;
   attr[1].id = cudaLaunchAttributeClusterDimension;
   attr[1].val.clusterDim.x = static_cast<unsigned>(cg);
   attr[1].val.clusterDim.y = 1;

@@ -257,12 +257,14 @@ double conversion_bytes(const ConvSegs& segs) {
 
 // A bf16-mode product with fp16 operands: the weight-streaming kernel for a
 // few rows when it implements the epilogue, else the tensor-core GEMM.
+// w_early: W was made by an earlier call (see request_plain_launch).
 int gemm16(gpt2_ctx* c, int kind, const void* A, const __half* W, int M, int N, int K,
-           const EpiParams& e, bool out_f16, cudaStream_t s, double* fl, double* by) {
+           const EpiParams& e, bool out_f16, cudaStream_t s, double* fl, double* by,
+           bool w_early = false) {
   const bool in_place_ok = kind != kEpiResidF32 || K <= 1024 || e.out == e.resid;
   if (smallm_supported(kind, M, K) && in_place_ok && (kind != kEpiBias || out_f16))
     return launch_gemm_smallm(c->env, kind, static_cast<const __half*>(A), W, M, N, K, e, s, fl,
-                              by);
+                              by, w_early);
   return launch_gemm_tc(c->env, kind, A, W, M, N, K, e, s, fl, by, true, out_f16);
 }
 
@@ -289,6 +291,11 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int slot, int B, int
   BlockW16 w{};
   ConvSegs conv{};
   if (bf) block_weight_conversions(c, slot, p, &w, &conv);
+  // Cached weights (every fp16 copy of this layer made by an earlier call):
+  // the few-row products start their weight streams before waiting on the
+  // previous kernel.  The call asked for a plain first launch (forward_trunk,
+  // gpt2_block_forward), so those copies are complete.
+  const bool w_early = bf && c->cache_weights && conv.count == 0;
 
   // LN1, with the block's weight conversion in the same launch
   st = c->run(kKindLayerNorm, s, [&](double* fl, double* by) {
@@ -314,7 +321,7 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int slot, int B, int
   e.ldo = 3 * d;
   st = c->run(bf ? kKindGemmQkv : kKindSimtFp32, s, [&](double* fl, double* by) {
     if (bf)
-      return gemm16(c, kEpiQkv, ln, w.attn_w, M, 3 * d, d, e, false, s, fl, by);
+      return gemm16(c, kEpiQkv, ln, w.attn_w, M, 3 * d, d, e, false, s, fl, by, w_early);
     return launch_gemm_fp32(c->env, kEpiQkv, static_cast<const float*>(ln),
                             static_cast<const float*>(p->attn_w), M, 3 * d, d, e, dh, s);
   });
@@ -364,7 +371,7 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int slot, int B, int
   st = c->run(bf ? kKindGemmProj : kKindSimtFp32, s, [&](double* fl, double* by) {
     if (bf) {
       const int kind = x_is_stream ? kEpiResidF32 : kEpiResidBf16In;
-      return gemm16(c, kind, attn, w.proj_w, M, d, d, e2, false, s, fl, by);
+      return gemm16(c, kind, attn, w.proj_w, M, d, d, e2, false, s, fl, by, w_early);
     }
     return launch_gemm_fp32(c->env, kEpiResidF32, static_cast<const float*>(attn),
                             static_cast<const float*>(p->proj_w), M, d, d, e2, dh, s);
@@ -387,7 +394,7 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int slot, int B, int
   e3.ldo = 4 * d;
   st = c->run(bf ? kKindGemmFc : kKindSimtFp32, s, [&](double* fl, double* by) {
     if (bf)
-      return gemm16(c, kEpiGelu, ln, w.fc_w, M, 4 * d, d, e3, true, s, fl, by);
+      return gemm16(c, kEpiGelu, ln, w.fc_w, M, 4 * d, d, e3, true, s, fl, by, w_early);
     return launch_gemm_fp32(c->env, kEpiGelu, static_cast<const float*>(ln),
                             static_cast<const float*>(p->fc_w), M, 4 * d, d, e3, dh, s);
   });
@@ -402,7 +409,7 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int slot, int B, int
   st = c->run(bf ? kKindGemmMlpProj : kKindSimtFp32, s, [&](double* fl, double* by) {
     if (bf) {
       const int kind = x_is_stream ? kEpiResidF32 : kEpiResidBf16Out;
-      return gemm16(c, kind, fc, w.mlp_proj_w, M, d, 4 * d, e4, false, s, fl, by);
+      return gemm16(c, kind, fc, w.mlp_proj_w, M, d, 4 * d, e4, false, s, fl, by, w_early);
     }
     return launch_gemm_fp32(c->env, kEpiResidF32, static_cast<const float*>(fc),
                             static_cast<const float*>(p->mlp_proj_w), M, d, 4 * d, e4, dh, s);
@@ -454,6 +461,18 @@ EncodeTiledFn get_encode() {
 }  // namespace
 
 namespace gpt2 {
+
+namespace {
+thread_local bool t_plain_next = false;
+}  // namespace
+
+void request_plain_launch() { t_plain_next = true; }
+
+bool take_pdl_permission() {
+  const bool plain = t_plain_next;
+  t_plain_next = false;
+  return !plain;
+}
 
 bool ensure_smem_limit(const void* fn, int bytes) {
   int dev = 0;
@@ -615,6 +634,9 @@ int gpt2_block_forward(gpt2_ctx* c, const void* x, const gpt2_block_params* para
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int h = n_head, dh = d / h;
   const size_t es = c->hp.dtype == GPT2_BF16 ? 2 : 4;
+  // Cached fp16 weights are read before waits on the previous kernel: the
+  // call's first launch waits for all earlier work (request_plain_launch).
+  if (c->hp.dtype == GPT2_BF16 && c->cache_weights) request_plain_launch();
 
   KvView dst;
   if (present) {
@@ -778,6 +800,9 @@ int forward_trunk(gpt2_ctx* c, const int32_t* ids, int B, int T, const gpt2_para
   const size_t es = bf ? 2 : 4;
   float* H = c->at<float>(c->plan.resid);
 
+  // Cached fp16 weights are read before waits on the previous kernel: the
+  // call's first launch waits for all earlier work (request_plain_launch).
+  if (bf && c->cache_weights) request_plain_launch();
   st = c->run(kKindEmbed, s, [&](double* fl, double* by) {
     *fl = 0;
     *by = static_cast<double>(M) * d * (2.0 * es + 4.0) + 4.0 * M;

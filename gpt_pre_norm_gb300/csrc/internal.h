@@ -109,9 +109,11 @@ int launch_gemm_tc(const LaunchEnv& env, int kind, const void* A, const void* W,
 // W [N, K], fp32 accumulate, epilogues kEpiQkv / kEpiGelu / kEpiBias (fp16
 // out) / kEpiResidF32 (K > 1024 only in place, out == resid).
 bool smallm_supported(int kind, int M, int K);
+// w_early: W was written before the current call's first launch, so its loads
+// may start before the previous kernel completes.
 int launch_gemm_smallm(const LaunchEnv& env, int kind, const __half* X, const __half* W, int M,
                        int N, int K, const EpiParams& ep, cudaStream_t stream, double* flops,
-                       double* bytes);
+                       double* bytes, bool w_early = false);
 
 // fp32 SIMT GEMM with the same epilogues (fp32 storage throughout).
 int launch_gemm_fp32(const LaunchEnv& env, int kind, const float* A, const float* W, int M, int N,
@@ -185,6 +187,15 @@ int launch_attention_fp32(const float* q, const float* kv, long long kv_s_batch,
 // the runtime refuses.
 bool ensure_smem_limit(const void* fn, int bytes);
 
+// Overlap with the previous kernel of the stream.  Every launch may overlap
+// it unless the calling thread asked for one plain launch: an API call whose
+// kernels read cached weights before waiting on their predecessor asks for it
+// before its first launch, which then starts only once all earlier work in the
+// stream has finished; every later launch of the call starts after that one,
+// so weights written by earlier calls are complete when they are read.
+void request_plain_launch();
+bool take_pdl_permission();  // false once after request_plain_launch()
+
 // Launches `kernel` on `stream` with programmatic stream serialisation (the
 // kernel must call pdl_wait() before touching global memory).
 template <typename... KArgs, typename... Args>
@@ -197,7 +208,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].val.programmaticStreamSerializationAllowed = take_pdl_permission() ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
