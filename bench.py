@@ -39,7 +39,10 @@ One JSON line is printed by rank 0.  Beside the device-timed value it carries:
   ms_per_step_median  the median of the K step times (ms_per_step is their
               mean);
   eager_ms_per_step  for the graph-replayed decode step, the same step with
-              its kernels launched one by one.
+              its kernels launched one by one;
+  cached_weights  for the block workloads, the same step with the fp16
+              working copies of the weights made by an earlier call (what the
+              per-call conversion from bf16 costs).
 --impl reference times the oracle itself as the reference arm.
 """
 from __future__ import annotations
@@ -348,6 +351,14 @@ class Runner:
             G.gpt2_forward(self.ctx, inp["ids"], self.mp, w.B, w.T, past=self.cache,
                            present=self.cache, logits=res)
 
+    # The block step on one weight set whose fp16 working copies an earlier call
+    # made (the context's weight cache on): what the per-call conversion costs.
+    def step_cached(self, s: int = 0):
+        G, w = self.G, self.w
+        s %= self.slots
+        G.gpt2_block_forward(self.ctx, self.inp[s]["x"], self.params[0], w.B, w.T, w.d, w.n_head,
+                             out=self.res[s])
+
     def capture_graph(self):
         torch = self.torch
         self.step()  # first call outside capture
@@ -616,6 +627,13 @@ def measure(r, args, barrier, torch, G, e2e: bool):
         t = timed_steps(r.step, args.steps, barrier, torch)
         out["ms_eager"] = sum(t) / len(t)
     out["ms_e2e"] = timed_e2e(r, args.steps, barrier, torch) if e2e else None
+    out["ms_cached"] = None
+    if r.w.kind == "block" and r.w.dtype == "bf16":
+        G.gpt2_ctx_cache_weights(r.ctx, True)
+        r.step_cached(0)  # makes the copies
+        t = timed_steps(r.step_cached, args.steps, barrier, torch)
+        out["ms_cached"] = sum(t) / len(t)
+        G.gpt2_ctx_cache_weights(r.ctx, False)
     G.gpt2_profile_enable(r.ctx, True)
     G.gpt2_profile_reset(r.ctx)
     timed_steps(r.step, args.steps, barrier, torch)
@@ -641,7 +659,17 @@ def workload_entry(w, r, m, peaks, args, ws, device):
          "clocks": m["clocks"]}
     if m["ms_eager"] is not None:
         e["eager_ms_per_step"] = reduce_over_ranks([m["ms_eager"]], device)[0]
+    if m["ms_cached"] is not None:
+        e["cached_weights"] = cached_entry(r, m, ws, device)
     return e
+
+
+def cached_entry(r, m, ws, device):
+    ms = reduce_over_ranks([m["ms_cached"]], device)[0]
+    return {"ms_per_step": ms, "value": job_throughput(r.tokens, ws, ms), "unit": "tokens/s",
+            "note": "the same step on one weight set whose fp16 working copies an earlier call "
+                    "made (weight cache on; x still rotated): the difference from ms_per_step is "
+                    "the per-call bf16 -> fp16 weight conversion"}
 
 
 # --------------------------------------------------------------------- main --
@@ -691,6 +719,7 @@ def main():
     ms_eager = reduce_over_ranks([m["ms_eager"]], device)[0] if m["ms_eager"] is not None else None
     tokens_rank = r.tokens
     h2d, d2h = r.e2e_bytes()
+    cached = cached_entry(r, m, ws, device) if m["ms_cached"] is not None else None
     l2_note, slots = r.l2_note, r.slots
     r.close()
     del r
@@ -737,6 +766,8 @@ def main():
     }
     if ms_eager is not None:
         line["eager_ms_per_step"] = ms_eager  # the same step without the CUDA graph
+    if cached is not None:
+        line["cached_weights"] = cached
     if not args.no_cpu_baseline and ws == 1:
         line["cpu_baseline"] = time_oracle(w, args.seed)
     print(json.dumps(line), flush=True)

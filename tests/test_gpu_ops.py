@@ -33,9 +33,9 @@ def _rand(rng, shape, std=1.0, bf16=True):
 # ------------------------------------------------------------- LayerNorm ----
 @pytest.mark.parametrize("d", [64, 768, 1024, 1600, 100])
 @pytest.mark.parametrize("x_fp32", [True, False])
-def test_layer_norm_bf16(G, d, x_fp32):
-    rng = np.random.default_rng(d)
-    rows = 1000
+@pytest.mark.parametrize("rows", [1000, 2049])  # one row per warp; two (an odd count)
+def test_layer_norm_bf16(G, d, x_fp32, rows):
+    rng = np.random.default_rng(d + rows)
     x = (2.0 * rng.standard_normal((rows, d)) + 0.5).astype(np.float32)
     if not x_fp32:
         x = S.round_to_bf16(x)
@@ -52,10 +52,10 @@ def test_layer_norm_bf16(G, d, x_fp32):
     assert np.max(np.abs(got - ref) / (np.abs(ref) + 1e-2)) < 2 ** -7
 
 
-@pytest.mark.parametrize("d", [64, 15, 768])
-def test_layer_norm_fp32(G, d):
+@pytest.mark.parametrize("d,rows", [(64, 37), (15, 37), (768, 37), (768, 4095)])
+def test_layer_norm_fp32(G, d, rows):
     rng = np.random.default_rng(7 + d)
-    x = _rand(rng, (37, d), 3.0, bf16=False) - 1.0
+    x = _rand(rng, (rows, d), 3.0, bf16=False) - 1.0
     g = _rand(rng, (d,), 0.2, bf16=False) + 1.0
     b = _rand(rng, (d,), 0.2, bf16=False)
     y = G.gpt2_layer_norm(G.GPT2_FP32, dev(x, torch.float32), dev(g, torch.float32),
