@@ -1,5 +1,8 @@
 // gemm_tc.cu -- tensor-core GEMM for sm_103a: C[M,N] = A[M,K] * W[N,K]^T,
-// bf16 operands, fp32 accumulation in tensor memory, fused epilogues.
+// 16-bit operands (fp16 for the products of the bf16 forward, whose
+// activations are written as fp16 and weights converted from bf16; bf16 when
+// a caller passes bf16 operands), fp32 accumulation in tensor memory, fused
+// epilogues.
 //
 // It computes the five Linear products of the GPT-2 forward ("GPT-2 Full
 // Forward Pass", "How it works": fused c_attn d->3d, attention c_proj, c_fc

@@ -65,15 +65,17 @@ def test_cached_decode_matches_oracle(G, B, d, h):
 
 
 def test_cached_equals_uncached_decode(G):
-    """The same arithmetic runs with and without the cache.  The logits agree
-    to far inside the oracle tolerance; not bit for bit, because the K chunks of
-    the 4096-wide mlp c_proj add into the residual with atomics, in any order."""
+    """The same arithmetic runs with and without the cache.  Not bit for bit:
+    the K chunks of the 4096-wide mlp c_proj add into the fp32 residual with
+    atomics, in any order, and an fp16 activation that then rounds the other
+    way moves by 2^-11 of itself; measured run to run about 1e-4 of the logits
+    (relative L2).  The bound, 1e-3, is ten times below the oracle's."""
     w = _model(8, 1024, 16)
     p = S.model_params(w, seed=22)
     ids = S.token_ids(w, seed=22, T=22)
     cached = _decode(G, w, p, ids, 20, cache_weights=True)
     plain = _decode(G, w, p, ids, 20, cache_weights=False)
-    assert_bf16_close(cached, plain, tol=1e-4, what="cached vs uncached decode")
+    assert_bf16_close(cached, plain, tol=1e-3, what="cached vs uncached decode")
 
 
 def test_cached_block_decode(G):
