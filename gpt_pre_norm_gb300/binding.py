@@ -82,6 +82,8 @@ def _load() -> C.CDLL:
                              C.POINTER(gpt2_kv), P, P]),
         "gpt2_forward_loss": (I, [P, P, P, I, I, C.POINTER(gpt2_params), I, C.POINTER(gpt2_kv),
                                   C.POINTER(gpt2_kv), P, P, P]),
+        "gpt2_forward_topk": (I, [P, P, I, I, C.POINTER(gpt2_params), I, C.POINTER(gpt2_kv),
+                                  C.POINTER(gpt2_kv), I, P, P, P, P]),
         "gpt2_layer_norm": (I, [I, P, I, P, P, I, I, P, P]),
         "gpt2_linear": (I, [P, I, P, P, P, P, P, I, I, I, P]),
         "gpt2_attention": (I, [P, P, P, I, I, I, I, I, I, P, P]),
@@ -275,6 +277,25 @@ def gpt2_forward_loss(ctx: Context, ids: torch.Tensor, params: ModelParams, B: i
     if present is not None:
         present.T_len = pr.T_len
     return loss, nxt
+
+
+def gpt2_forward_topk(ctx: Context, ids: torch.Tensor, params: ModelParams, B: int, T: int,
+                      k: int, past: KV | None = None, present: KV | None = None,
+                      want_lse: bool = True, stream=None):
+    """(top_logits [B, T, k] fp32, top_ids [B, T, k] int32, lse [B, T] fp32 or
+    None) without the logits."""
+    tv = torch.empty((B, T, k), dtype=torch.float32, device=ids.device)
+    ti = torch.empty((B, T, k), dtype=torch.int32, device=ids.device)
+    lse = torch.empty((B, T), dtype=torch.float32, device=ids.device) if want_lse else None
+    ps = past.struct() if past is not None else None
+    pr = present.struct() if present is not None else None
+    _check(LIB.gpt2_forward_topk(ctx.handle, _ptr(ids), B, T, C.byref(params.struct),
+                                 params.n_layer, C.byref(ps) if ps is not None else None,
+                                 C.byref(pr) if pr is not None else None, k, _ptr(tv), _ptr(ti),
+                                 _ptr(lse), _stream(stream)), "gpt2_forward_topk")
+    if present is not None:
+        present.T_len = pr.T_len
+    return tv, ti, lse
 
 
 def gpt2_generate_greedy(ctx: Context, ids: torch.Tensor, params: ModelParams, n_new: int,

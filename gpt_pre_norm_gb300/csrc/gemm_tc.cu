@@ -52,7 +52,7 @@ constexpr int kBK = 64;                       // one 128-byte swizzle row of bf1
 // GPT-2-XL shape 80 -> 70 us with four; the in-place fp32 residual epilogue
 // is faster with eight).
 __host__ __device__ constexpr int epi_warps(int k) {
-  return k == kEpiResidBf16Out || k == kEpiHeadLoss ? 4 : 8;
+  return k == kEpiResidBf16Out || k == kEpiHeadLoss || k == kEpiHeadTopK ? 4 : 8;
 }
 __host__ __device__ constexpr int epi_threads(int k) { return 128 + 32 * epi_warps(k); }
 constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB per A slot
@@ -86,11 +86,13 @@ __host__ __device__ constexpr int slot_bytes(int k) {
 __host__ __device__ constexpr int epi_warp_bytes(int k) {
   return k == kEpiLogits ? 32 * kLogitsLd * 4
          : k == kEpiLogitsT ? 0
-         : k == kEpiHeadLoss ? 0
+         : k == kEpiHeadLoss || k == kEpiHeadTopK ? 0
                              : 2 * slot_bytes(k);
 }
 __host__ __device__ constexpr int epi_bias_bytes(int k) {
-  return k == kEpiLogits || k == kEpiLogitsT || k == kEpiHeadLoss ? 0 : kBiasBytes;
+  return k == kEpiLogits || k == kEpiLogitsT || k == kEpiHeadLoss || k == kEpiHeadTopK
+             ? 0
+             : kBiasBytes;
 }
 
 struct GemmArgs {
@@ -228,7 +230,8 @@ __device__ __forceinline__ void epilogue_prefetch(int row0, int ncol0, int ncols
                                                   uint8_t* epi, uint16_t* bias_s, uint64_t* rbar,
                                                   EpiState& s, const GemmArgs& a,
                                                   const CUtensorMap* tmR) {
-  if constexpr (KIND != kEpiLogits && KIND != kEpiLogitsT && KIND != kEpiHeadLoss) {
+  if constexpr (KIND != kEpiLogits && KIND != kEpiLogitsT && KIND != kEpiHeadLoss &&
+                KIND != kEpiHeadTopK) {
     const int N = a.N;
     for (int j = 4 * lane; j < ncols; j += 128) {
       const int col = ncol0 + j;
@@ -339,6 +342,83 @@ __device__ __forceinline__ void head_loss_rows(uint32_t tbase, int row0, int nco
     ep.part_m[o] = m;
     ep.part_s[o] = sum;
     ep.part_i[o] = idx;
+  }
+}
+
+// kEpiHeadTopK, one warp's share of a tile of the head, laid out as for
+// head_loss_rows: each thread owns token row0 + lane and the tile's
+// kHeadLossBlock vocabulary entries from ncol0.  It keeps the kTopKMax largest
+// in a sorted register list (an entry enters when it beats the last one,
+// strictly, then bubbles up past smaller ones: the scan runs in index order,
+// so among equal values the lower index stays first; NaN never enters), and
+// the block's maximum and sum of 2^((z - max) log2 e) for the logsumexp.
+__device__ __forceinline__ void head_topk_rows(uint32_t tbase, int row0, int ncol0, int lane,
+                                               const GemmArgs& a) {
+  constexpr float kL2e = 1.4426950408889634f;
+  const EpiParams& ep = a.ep;
+  const int n_tok = a.M, V = a.N;
+  const int row = row0 + lane;
+  if (ncol0 >= V) return;  // a half tile past the vocabulary (warp-uniform)
+  float tv[kTopKMax];
+  int ti[kTopKMax];
+#pragma unroll
+  for (int j = 0; j < kTopKMax; ++j) {
+    tv[j] = -INFINITY;
+    ti[j] = 0x7fffffff;
+  }
+  float m = -INFINITY, sum = 0.f;
+  for (int c = 0; c < kHeadLossBlock; c += 32) {
+    const int col0 = ncol0 + c;
+    if (col0 >= V) break;  // warp-uniform
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), r);
+    tmem_ld_wait();
+    if (col0 + 32 > V) {  // the vocabulary's ragged end: entries past it do not count
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (col0 + i >= V) r[i] = __float_as_uint(-INFINITY);
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float v = __uint_as_float(r[i]);
+      if (v > tv[kTopKMax - 1]) {
+        tv[kTopKMax - 1] = v;
+        ti[kTopKMax - 1] = col0 + i;
+#pragma unroll
+        for (int j = kTopKMax - 1; j > 0; --j)
+          if (tv[j] > tv[j - 1]) {
+            const float fv = tv[j];
+            tv[j] = tv[j - 1];
+            tv[j - 1] = fv;
+            const int fi = ti[j];
+            ti[j] = ti[j - 1];
+            ti[j - 1] = fi;
+          }
+      }
+    }
+    // The block's running maximum and rescaled sum (as head_loss_rows).
+    float cm = __uint_as_float(r[0]);
+#pragma unroll
+    for (int i = 1; i < 32; ++i) cm = fmaxf(cm, __uint_as_float(r[i]));
+    if (cm > m) {
+      sum = m == -INFINITY ? 0.f : sum * ex2((m - cm) * kL2e);
+      m = cm;
+    }
+    const float ml = m * kL2e;
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 32; ++i) s4[i & 3] += ex2(fmaf(__uint_as_float(r[i]), kL2e, -ml));
+    sum += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+  }
+  if (row < n_tok) {
+    const size_t vb = static_cast<size_t>(ncol0 / kHeadLossBlock);
+    ep.part_m[vb * n_tok + row] = m;
+    ep.part_s[vb * n_tok + row] = sum;
+#pragma unroll
+    for (int j = 0; j < kTopKMax; ++j) {
+      ep.topk_v[(vb * kTopKMax + j) * n_tok + row] = tv[j];
+      ep.topk_i[(vb * kTopKMax + j) * n_tok + row] = ti[j];
+    }
   }
 }
 
@@ -782,6 +862,8 @@ __global__ void __launch_bounds__(epi_threads(KIND), 1)
                              static_cast<uint32_t>(acc * 256 + half * ncols);
       if constexpr (KIND == kEpiHeadLoss) {
         head_loss_rows(tbase, row0, ncol0, lane, args);
+      } else if constexpr (KIND == kEpiHeadTopK) {
+        head_topk_rows(tbase, row0, ncol0, lane, args);
       } else {
         epilogue_tile<KIND>(tbase, row0, ncol0, ncols, lane, epi, bias_s, rbar, st, args, &tmO,
                             &tmR, &tmQ, &tmKV, abort_flag);
@@ -834,6 +916,7 @@ void* kernel_for(int kind, int cg) {
     case kEpiLogits: return kernel_ptr<kEpiLogits>(cg);
     case kEpiLogitsT: return kernel_ptr<kEpiLogitsT>(cg);
     case kEpiHeadLoss: return kernel_ptr<kEpiHeadLoss>(cg);
+    case kEpiHeadTopK: return kernel_ptr<kEpiHeadTopK>(cg);
     case kEpiQkv: return kernel_ptr<kEpiQkv>(cg);
     default: return nullptr;
   }
@@ -927,7 +1010,8 @@ int launch_gemm_tc(const LaunchEnv& env, int kind_in, const void* A_in, const vo
       kind_in >= kEpiCount)
     return GPT2_ERR_INVALID_ARG;
   if (K % 8 != 0) return GPT2_ERR_UNSUPPORTED;
-  if (kind_in != kEpiLogits && kind_in != kEpiHeadLoss && (N_in % 2 != 0))
+  const bool reduced_head = kind_in == kEpiHeadLoss || kind_in == kEpiHeadTopK;
+  if (kind_in != kEpiLogits && !reduced_head && (N_in % 2 != 0))
     return GPT2_ERR_UNSUPPORTED;
   if (kind_in == kEpiQkv && (ep.d % 64 != 0 || N_in != 3 * ep.d)) return GPT2_ERR_UNSUPPORTED;
   // The tied head that writes logits runs transposed, logits^T = W_e H^T:
@@ -941,7 +1025,7 @@ int launch_gemm_tc(const LaunchEnv& env, int kind_in, const void* A_in, const vo
   const void* A = A_in;
   const void* W = W_in;
   const bool transposed = kind_in == kEpiLogits;
-  const bool head = transposed || kind_in == kEpiHeadLoss;
+  const bool head = transposed || reduced_head;
   if (transposed) {
     if (kind_in == kEpiLogits) kind = kEpiLogitsT;
     std::swap(A, W);
@@ -959,7 +1043,7 @@ int launch_gemm_tc(const LaunchEnv& env, int kind_in, const void* A_in, const vo
 
   const int units = cg == 2 ? env.num_sms / 2 : env.num_sms;
   // The loss epilogue's partials cover one whole tile's kHeadLossBlock entries.
-  const int BN = kind == kEpiHeadLoss ? kHeadLossBlock : choose_bn(M, N, kBM * cg, units);
+  const int BN = reduced_head ? kHeadLossBlock : choose_bn(M, N, kBM * cg, units);
   int stages = kMaxStages;
   while (stages > 2 && smem_bytes_for(kind, BN, stages, cg) > static_cast<size_t>(kSmemLimit))
     --stages;
@@ -1046,6 +1130,7 @@ int launch_gemm_tc(const LaunchEnv& env, int kind_in, const void* A_in, const vo
       case kEpiResidBf16Out: b += 6.0 * mn + 2.0 * N; break;
       case kEpiLogits: b += 4.0 * mn; break;
       case kEpiHeadLoss: b += 12.0 * mn / kHeadLossBlock; break;  // the per-block partials
+      case kEpiHeadTopK: b += (8.0 + 8.0 * kTopKMax) * mn / kHeadLossBlock; break;
     }
     *bytes = b;
   }

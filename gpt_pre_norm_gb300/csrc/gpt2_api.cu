@@ -39,7 +39,7 @@ struct ProfRec {
 
 // Offsets (bytes) of the workspace regions.
 struct WsPlan {
-  size_t err, ln, q, kv, attn, resid, fc, partials, wconv, ids, hloss, total;
+  size_t err, ln, q, kv, attn, resid, fc, partials, wconv, ids, hloss, htopk, total;
 };
 
 // Vocabulary blocks of the fused head's per-token partials (kHeadLossBlock
@@ -84,6 +84,11 @@ WsPlan plan_workspace(const gpt2_hparams& hp, int max_B, int max_T) {
   // maxima, sums and indices [vocab blocks][M]
   p.hloss = take(hp.dtype == GPT2_BF16
                      ? M * 4 * (1 + 3 * static_cast<size_t>(loss_vblocks(hp)))
+                     : 0);
+  // top-k head (bf16 mode): kTopKMax candidate logits and indices per (vocabulary
+  // block, token); its maxima and sums share the loss partials' arrays
+  p.htopk = take(hp.dtype == GPT2_BF16
+                     ? M * 8 * static_cast<size_t>(kTopKMax) * loss_vblocks(hp)
                      : 0);
   p.total = off;
   return p;
@@ -906,6 +911,46 @@ int gpt2_forward_loss(gpt2_ctx* c, const int32_t* ids, const int32_t* targets, i
     *by = 12.0 * nvb * M + 12.0 * M;
     return launch_head_loss_combine(pm, ps, pi, nvb, M, V, loss ? targets : nullptr, tl, loss,
                                     next_ids, c->env.err, s);
+  });
+  if (st) return st;
+  if (present) present->T_len = t_past + T;
+  return GPT2_OK;
+}
+
+int gpt2_forward_topk(gpt2_ctx* c, const int32_t* ids, int B, int T, const gpt2_params* params,
+                      int L, const gpt2_kv* past, gpt2_kv* present, int k, float* top_logits,
+                      int32_t* top_ids, float* lse, void* stream) {
+  if (!c || !top_logits || !top_ids) return GPT2_ERR_INVALID_ARG;
+  if (k < 1 || k > kTopKMax || k > c->hp.n_vocab) return GPT2_ERR_INVALID_ARG;
+  if (c->hp.dtype != GPT2_BF16) return GPT2_ERR_UNSUPPORTED;
+  if (!aligned16(top_logits) || !aligned16(top_ids) || (lse && !aligned16(lse)))
+    return GPT2_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const __half* wte16 = nullptr;
+  int t_past = 0;
+  int st = forward_trunk(c, ids, B, T, params, L, past, present, s, &wte16, &t_past);
+  if (st) return st;
+  const gpt2_hparams& hp = c->hp;
+  const int d = hp.n_embd, V = hp.n_vocab, M = B * T;
+  const int nvb = loss_vblocks(hp);
+  float* pm = c->at<float>(c->plan.hloss) + M;
+  float* ps = pm + static_cast<size_t>(nvb) * M;
+  float* tv = c->at<float>(c->plan.htopk);
+  int32_t* ti = reinterpret_cast<int32_t*>(tv + static_cast<size_t>(nvb) * kTopKMax * M);
+  EpiParams e{};
+  e.part_m = pm;
+  e.part_s = ps;
+  e.topk_v = tv;
+  e.topk_i = ti;
+  st = c->run(kKindGemmLogits, s, [&](double* fl, double* by) {
+    return launch_gemm_tc(c->env, kEpiHeadTopK, c->ws + c->plan.ln, wte16, M, V, d, e, s, fl,
+                          by, true, false);
+  });
+  if (st) return st;
+  st = c->run(kKindLossCombine, s, [&](double* fl, double* by) {
+    *fl = 0;
+    *by = static_cast<double>(nvb) * M * (8.0 + 8.0 * k) + 8.0 * M * k + 4.0 * M;
+    return launch_head_topk_combine(pm, ps, tv, ti, nvb, M, k, top_logits, top_ids, lse, s);
   });
   if (st) return st;
   if (present) present->T_len = t_past + T;

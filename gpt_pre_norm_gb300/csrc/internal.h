@@ -45,6 +45,7 @@ enum EpiKind : int {
   kEpiQkv,            // acc + bias scattered to Q [B,h,T,64] and the K/V cache
   kEpiLogitsT,        // (internal) kEpiLogits computed as W A^T: TMEM lanes = vocabulary
   kEpiHeadLoss,       // the tied head (tokens on TMEM lanes) reduced to per-token partials
+  kEpiHeadTopK,       // the tied head reduced to per-token top-k candidates and logsumexp partials
   kEpiCount
 };
 
@@ -61,6 +62,8 @@ struct KvDst {
 // Vocabulary entries per partial of the head reduced to the loss (one
 // 256-wide tile of the head per token).
 constexpr int kHeadLossBlock = 256;
+// Candidates the top-k head keeps per (token, vocabulary block): the largest k allowed.
+constexpr int kTopKMax = 8;
 
 struct EpiParams {
   const void* bias;         // [N], mode dtype
@@ -82,6 +85,12 @@ struct EpiParams {
   float* part_m;
   float* part_s;
   int32_t* part_i;
+  // kEpiHeadTopK: part_m, part_s as above, and the block's kTopKMax largest
+  // logits in descending order (among equal values the lower index first; NaN
+  // never taken) topk_v[(j * kTopKMax + i) * n_tok + t] with their indices
+  // topk_i[..] (-inf and 0x7fffffff where the block has fewer candidates).
+  float* topk_v;
+  int32_t* topk_i;
 };
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -144,6 +153,12 @@ int launch_layer_norm(int mode, const void* x, int x_dtype, const void* g, const
 // logsumexp L and the argmax; loss[t] = L - tgt_logit[t] for 0 <= tgt[t] < V,
 // 0 for tgt[t] < 0 (NaN and the bad-token error bit for tgt[t] >= V);
 // next[t] = the argmax.  loss, next and tgt may be null.
+// Top-k of every token from the top-k head's partials: top_v[t * k + i],
+// top_i[..] for i < k (descending, lower index first among equal values; -1 where
+// fewer than k finite logits exist), lse[t] = logsumexp (NULL to skip).
+int launch_head_topk_combine(const float* part_m, const float* part_s, const float* topk_v,
+                             const int32_t* topk_i, int n_vblk, int n_tok, int k, float* top_v,
+                             int32_t* top_i, float* lse, cudaStream_t stream);
 int launch_head_loss_combine(const float* part_m, const float* part_s, const int32_t* part_i,
                              int n_vblk, int n_tok, int V, const int32_t* tgt,
                              const float* tgt_logit, float* loss, int32_t* next, unsigned* err,

@@ -543,7 +543,110 @@ __global__ void __launch_bounds__(32 * kLossSlices)
   }
 }
 
+// (v1, i1) ranks before (v2, i2): larger value, or equal value and lower index.
+__device__ __forceinline__ bool topk_before(float v1, int i1, float v2, int i2) {
+  return v1 > v2 || (v1 == v2 && i1 < i2);
+}
+
+// Top-k from the top-k head's partials: one warp per token.  Lane l merges
+// the candidates of vocabulary blocks l, l + 32, ... into its own sorted list
+// of kTopKMax and their (max, sum) pairs into a logsumexp; then k rounds in
+// which the warp finds the best head of all lanes' lists (a butterfly on
+// (value, index)) and the lane holding it drops it.  Indices are unique, so
+// exactly one lane pops per round (or, once every list holds only empty
+// slots, all lanes alike, which ends the useful output: -1 from there on).
+__global__ void __launch_bounds__(256)
+    head_topk_combine(const float* __restrict__ pm, const float* __restrict__ ps,
+                      const float* __restrict__ cv, const int32_t* __restrict__ ci, int n_vblk,
+                      int n_tok, int k, float* __restrict__ top_v, int32_t* __restrict__ top_i,
+                      float* __restrict__ lse) {
+  pdl_trigger();
+  pdl_wait();
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= n_tok) return;  // warp-uniform
+  float tv[kTopKMax];
+  int ti[kTopKMax];
+#pragma unroll
+  for (int j = 0; j < kTopKMax; ++j) {
+    tv[j] = -INFINITY;
+    ti[j] = 0x7fffffff;
+  }
+  float m = -INFINITY, sum = 0.f;
+  int dummy = 0;
+  for (int b = lane; b < n_vblk; b += 32) {
+    const size_t o = static_cast<size_t>(b) * n_tok + t;
+    lse_merge_rw(m, sum, dummy, pm[o], ps[o], 0);
+    for (int j = 0; j < k; ++j) {
+      const size_t oj = (static_cast<size_t>(b) * kTopKMax + j) * n_tok + t;
+      const float v = cv[oj];
+      const int id = ci[oj];
+      if (!topk_before(v, id, tv[kTopKMax - 1], ti[kTopKMax - 1])) break;  // the block's list is sorted
+      tv[kTopKMax - 1] = v;
+      ti[kTopKMax - 1] = id;
+#pragma unroll
+      for (int q = kTopKMax - 1; q > 0; --q)
+        if (topk_before(tv[q], ti[q], tv[q - 1], ti[q - 1])) {
+          const float fv = tv[q];
+          tv[q] = tv[q - 1];
+          tv[q - 1] = fv;
+          const int fi = ti[q];
+          ti[q] = ti[q - 1];
+          ti[q - 1] = fi;
+        }
+    }
+  }
+  for (int r = 0; r < k; ++r) {
+    float bv = tv[0];
+    int bi = ti[0];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (topk_before(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (tv[0] == bv && ti[0] == bi) {  // this lane's head was taken
+#pragma unroll
+      for (int q = 0; q < kTopKMax - 1; ++q) {
+        tv[q] = tv[q + 1];
+        ti[q] = ti[q + 1];
+      }
+      tv[kTopKMax - 1] = -INFINITY;
+      ti[kTopKMax - 1] = 0x7fffffff;
+    }
+    if (lane == 0) {
+      const bool real = bi != 0x7fffffff;
+      top_v[static_cast<size_t>(t) * k + r] = bv;
+      top_i[static_cast<size_t>(t) * k + r] = real ? bi : -1;
+    }
+  }
+  if (lse) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+      const float s2 = __shfl_xor_sync(0xffffffffu, sum, off);
+      lse_merge_rw(m, sum, dummy, m2, s2, 0);
+    }
+    if (lane == 0) lse[t] = m + logf(sum);
+  }
+}
+
 }  // namespace
+
+int launch_head_topk_combine(const float* part_m, const float* part_s, const float* topk_v,
+                             const int32_t* topk_i, int n_vblk, int n_tok, int k, float* top_v,
+                             int32_t* top_i, float* lse, cudaStream_t stream) {
+  if (n_vblk <= 0 || n_tok <= 0 || k < 1 || k > kTopKMax || !part_m || !part_s || !topk_v ||
+      !topk_i || !top_v || !top_i)
+    return GPT2_ERR_INVALID_ARG;
+  const cudaError_t e =
+      launch_pdl(head_topk_combine, dim3((n_tok + 7) / 8), dim3(256), 0, stream, part_m, part_s,
+                 topk_v, topk_i, n_vblk, n_tok, k, top_v, top_i, lse);
+  return e == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+}
 
 int launch_head_loss_combine(const float* part_m, const float* part_s, const int32_t* part_i,
                              int n_vblk, int n_tok, int V, const int32_t* tgt,

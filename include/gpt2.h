@@ -216,6 +216,25 @@ int gpt2_forward_loss(gpt2_ctx *ctx, const int32_t *ids, const int32_t *targets,
                       const gpt2_params *params, int L, const gpt2_kv *past, gpt2_kv *present,
                       float *loss, int32_t *next_ids, void *stream);
 
+/* The k most likely next tokens of every position, without the logits: the
+ * candidates a top-k sampler draws from ("GPT-2 Full Forward Pass", "How it
+ * works": the logits give the next token's distribution; greedy decoding takes
+ * its argmax, k = 1).  Runs as gpt2_forward up to LN_f, then reduces the tied
+ * head on the fly, per position t of [B, T]:
+ *   top_logits[t, i], top_ids[t, i] for i < k: the k largest z[t, v] in
+ *     descending order with their ids (among equal values the lower id
+ *     first; NaN logits are never chosen; -1 ids fill slots beyond the finite
+ *     logits);
+ *   lse[t] = logsumexp_v z[t, v], so that top_logits[t, i] - lse[t] are the
+ *     log-probabilities of the candidates (NaN when a logit is NaN).
+ * 1 <= k <= 8 and k <= n_vocab (INVALID_ARG otherwise).  top_logits: device
+ * fp32 [B, T, k]; top_ids: device int32 [B, T, k]; lse: device fp32 [B, T] or
+ * NULL; each 16-byte aligned.  bf16 mode only (UNSUPPORTED in fp32 mode).
+ * Other errors: as gpt2_forward.                                             */
+int gpt2_forward_topk(gpt2_ctx *ctx, const int32_t *ids, int B, int T, const gpt2_params *params,
+                      int L, const gpt2_kv *past, gpt2_kv *present, int k, float *top_logits,
+                      int32_t *top_ids, float *lse, void *stream);
+
 /* Greedy generation: the model's consumer ("GPT-2 Full Forward Pass": the
  * logits of the last position give the next token; greedy takes their
  * argmax, the lowest index among equal maxima).  Runs the prompt ids [B,

@@ -289,3 +289,26 @@ def next_token_loss(logits: np.ndarray, targets: np.ndarray):
     zy = np.take_along_axis(z, safe[..., None], axis=-1)[..., 0]
     loss = np.where(y >= 0, lse - zy, 0.0)
     return loss, np.argmax(z, axis=-1)
+
+
+def top_k(logits: np.ndarray, k: int):
+    """Per position: the k largest logits in descending order with their ids,
+    the lower id first among equal values (the greedy choice argmax is the
+    first of them, k = 1), and logsumexp(z), which turns them into
+    log-probabilities ([FF] "How it works": the logits give the next token's
+    distribution; a sampler draws from its most likely candidates).  NaN
+    logits are never chosen.  logits [..., V] with V >= k.
+    Returns (values [..., k], ids [..., k], lse [...])."""
+    z = np.asarray(logits, np.float64)
+    V = z.shape[-1]
+    flat = z.reshape(-1, V)
+    ids = np.empty((flat.shape[0], k), np.int64)
+    for r in range(flat.shape[0]):
+        key = np.where(np.isnan(flat[r]), -np.inf, flat[r])
+        order = np.lexsort((np.arange(V), -key))  # by value descending, then id ascending
+        ids[r] = order[:k]
+    ids = ids.reshape(z.shape[:-1] + (k,))
+    vals = np.take_along_axis(z, ids, axis=-1)
+    m = z.max(axis=-1)
+    lse = m + np.log(np.exp(z - m[..., None]).sum(axis=-1))
+    return vals, ids, lse

@@ -81,6 +81,8 @@ def test_null_arguments_rejected_without_launch(G):
     assert G.LIB.gpt2_block_forward_postnorm(None, None, None, 1, 1, 768, 12, None, None) == 1
     assert G.LIB.gpt2_forward_loss(None, None, None, 1, 1, None, 12, None, None, None, None,
                                    None) == 1
+    assert G.LIB.gpt2_forward_topk(None, None, 1, 1, None, 12, None, None, 4, None, None, None,
+                                   None) == 1
     assert G.LIB.gpt2_layer_norm(0, None, 0, None, None, 1, 768, None, None) == 1
     assert G.LIB.gpt2_sync_status(None, None) == 1
     assert G.LIB.gpt2_linear(None, 0, None, None, None, None, None, 1, 1, 1, None) == 1

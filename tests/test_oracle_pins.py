@@ -599,3 +599,76 @@ def test_loss_shift_invariance_and_library_special_case():
                           reduction="none").numpy().reshape(4, 5)
     np.testing.assert_allclose(loss, ref, rtol=1e-12, atol=1e-12)
     np.testing.assert_array_equal(am, torch.from_numpy(z).argmax(-1).numpy())
+
+
+# ------------------------------------------------------------------- top-k ----
+def test_top_k_hand_example_ties_and_nan():
+    """Worked by hand: values 3 (ids 4 and 1), 5, NaN, 3 again at id 7: the order is
+    5 (id 2), then the 3s by id (1, 4, 7); NaN (id 0) is never chosen."""
+    z = np.array([[np.nan, 3.0, 5.0, -1.0, 3.0, 0.5, -2.0, 3.0]])
+    vals, ids, _ = O.top_k(z, 4)
+    assert ids.tolist() == [[2, 1, 4, 7]]
+    assert vals.tolist() == [[5.0, 3.0, 3.0, 3.0]]
+
+
+def test_top_k_first_is_argmax_and_set_is_the_k_largest():
+    """k = 1 is numpy's argmax (lowest index among equal maxima); for any k the
+    chosen values are the k largest of the row (as a sorted multiset), sorted
+    descending, the ids distinct and pointing at those values."""
+    rng = _rng(41)
+    z = np.round(4.0 * rng.standard_normal((6, 7, 97)), 1)  # rounding makes ties common
+    v1, i1, _ = O.top_k(z, 1)
+    np.testing.assert_array_equal(i1[..., 0], np.argmax(z, axis=-1))
+    for k in (3, 8):
+        vals, ids, _ = O.top_k(z, k)
+        np.testing.assert_array_equal(vals, -np.sort(-z, axis=-1)[..., :k])
+        np.testing.assert_array_equal(np.take_along_axis(z, ids, axis=-1), vals)
+        assert all(len(set(r)) == k for r in ids.reshape(-1, k).tolist())
+        # among equal values the lower id comes first
+        same = vals[..., 1:] == vals[..., :-1]
+        assert np.all(ids[..., 1:][same] > ids[..., :-1][same])
+
+
+def test_top_k_lse_matches_the_loss_and_torch():
+    """logsumexp ties the top-k output to the cross-entropy: lse - z[y] is the
+    loss of target y; and it equals torch's logsumexp.  Shifting a row by a
+    constant shifts its values and lse and keeps its ids."""
+    rng = _rng(42)
+    z = 3.0 * rng.standard_normal((4, 5, 60))
+    y = rng.integers(0, 60, size=(4, 5))
+    vals, ids, lse = O.top_k(z, 5)
+    loss, _ = O.next_token_loss(z, y)
+    np.testing.assert_allclose(lse - np.take_along_axis(z, y[..., None], -1)[..., 0], loss,
+                               rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, torch.logsumexp(torch.from_numpy(z), dim=-1).numpy(),
+                               rtol=1e-12, atol=1e-12)
+    c = 100.0 * rng.standard_normal((4, 5, 1))
+    vals2, ids2, lse2 = O.top_k(z + c, 5)
+    np.testing.assert_array_equal(ids2, ids)
+    np.testing.assert_allclose(vals2, vals + c, rtol=1e-12, atol=1e-9)
+    np.testing.assert_allclose(lse2, lse + c[..., 0], rtol=1e-12, atol=1e-9)
+
+
+def _topk_higher_id_first(logits, k):
+    z = np.asarray(logits, np.float64)
+    V = z.shape[-1]
+    flat = np.where(np.isnan(z), -np.inf, z).reshape(-1, V)
+    ids = np.stack([np.lexsort((-np.arange(V), -r))[:k] for r in flat]).reshape(z.shape[:-1] + (k,))
+    m = z.max(-1)
+    return np.take_along_axis(z, ids, -1), ids, m + np.log(np.exp(z - m[..., None]).sum(-1))
+
+
+def _topk_nan_as_largest(logits, k):
+    z = np.asarray(logits, np.float64)
+    V = z.shape[-1]
+    flat = np.where(np.isnan(z), np.inf, z).reshape(-1, V)
+    ids = np.stack([np.lexsort((np.arange(V), -r))[:k] for r in flat]).reshape(z.shape[:-1] + (k,))
+    m = np.nanmax(z, -1)
+    return np.take_along_axis(z, ids, -1), ids, m
+
+
+@pytest.mark.parametrize("bad", [_topk_higher_id_first, _topk_nan_as_largest])
+def test_planted_top_k_mistake_is_caught(monkeypatch, bad):
+    monkeypatch.setattr(O, "top_k", bad)
+    with pytest.raises(AssertionError):
+        test_top_k_hand_example_ties_and_nan()
