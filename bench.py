@@ -76,6 +76,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 TENSOR_KINDS = {"gemm_c_attn", "gemm_c_proj", "gemm_c_fc", "gemm_mlp_c_proj", "gemm_lm_head",
                 "gemm_other", "attention_prefill"}
 L2_BYTES_FALLBACK = 126 << 20  # GB300
+TOPK = 8  # candidates per position of the top-k workload
 # Configurations timed beside the default one (the GPT-2-small block).
 EXTRA_WORKLOADS = ("forward_bf16_gpt2_small", "block_bf16_d1600", "decode_bf16_gpt2_medium")
 # What the bf16 path computes in.
@@ -307,6 +308,10 @@ class Runner:
             self.inp_host["targets"] = tg_dev.cpu().pin_memory()
             self.res = [torch.empty((w.B, w.T), dtype=torch.float32, device=device)
                         for _ in range(2)]
+        elif w.kind == "forward_topk":
+            # [0]: the k largest logits, [1]: their ids (int32 bits)
+            self.res = [torch.empty((2, w.B, w.T, TOPK), dtype=torch.float32, device=device)
+                        for _ in range(2)]
         else:
             n_res = 1 if w.kind == "decode" else 2
             self.res = [torch.empty((w.B, w.T, w.n_vocab), dtype=torch.float32, device=device)
@@ -343,6 +348,9 @@ class Runner:
                                  out=res)
         elif w.kind == "forward":
             G.gpt2_forward(self.ctx, inp["ids"], self.mp, w.B, w.T, logits=res)
+        elif w.kind == "forward_topk":
+            G.gpt2_forward_topk(self.ctx, inp["ids"], self.mp, w.B, w.T, TOPK, want_lse=False,
+                                top_logits=res[0], top_ids=res[1].view(self.torch.int32))
         elif w.kind == "forward_loss":
             G.gpt2_forward_loss(self.ctx, inp["ids"], self.mp, w.B, w.T, targets=inp["targets"],
                                 want_next=False, loss=res)
@@ -481,10 +489,12 @@ def oracle_sample(w: S.Workload, seed: int, T_sample: int):
         return (lambda: O.block_forward(x, p, w.n_head)), T_sample
     p = S.model_params(w, seed)
     ids = S.token_ids(w, seed)[:1]
-    if w.kind in ("forward", "forward_loss"):
+    if w.kind in ("forward", "forward_loss", "forward_topk"):
         ids = ids[:, :T_sample]
         if w.kind == "forward":
             return (lambda: O.forward(ids, p, w.n_head)), T_sample
+        if w.kind == "forward_topk":
+            return (lambda: O.top_k(O.forward(ids, p, w.n_head)[0], TOPK)), T_sample
         tg = np.concatenate([ids[:, 1:], np.full((1, 1), -1, ids.dtype)], axis=1)
         return (lambda: O.next_token_loss(O.forward(ids, p, w.n_head)[0], tg)), T_sample
     past = np.stack([S.past_kv(w, seed, 0, layer) for layer in range(w.n_layer)])[None]

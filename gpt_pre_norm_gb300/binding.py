@@ -281,11 +281,14 @@ def gpt2_forward_loss(ctx: Context, ids: torch.Tensor, params: ModelParams, B: i
 
 def gpt2_forward_topk(ctx: Context, ids: torch.Tensor, params: ModelParams, B: int, T: int,
                       k: int, past: KV | None = None, present: KV | None = None,
-                      want_lse: bool = True, stream=None):
+                      want_lse: bool = True, stream=None, top_logits: torch.Tensor | None = None,
+                      top_ids: torch.Tensor | None = None):
     """(top_logits [B, T, k] fp32, top_ids [B, T, k] int32, lse [B, T] fp32 or
-    None) without the logits."""
-    tv = torch.empty((B, T, k), dtype=torch.float32, device=ids.device)
-    ti = torch.empty((B, T, k), dtype=torch.int32, device=ids.device)
+    None) without the logits (written into top_logits / top_ids when given)."""
+    tv = top_logits if top_logits is not None else \
+        torch.empty((B, T, k), dtype=torch.float32, device=ids.device)
+    ti = top_ids if top_ids is not None else \
+        torch.empty((B, T, k), dtype=torch.int32, device=ids.device)
     lse = torch.empty((B, T), dtype=torch.float32, device=ids.device) if want_lse else None
     ps = past.struct() if past is not None else None
     pr = present.struct() if present is not None else None

@@ -86,7 +86,8 @@ __host__ __device__ constexpr int slot_bytes(int k) {
 __host__ __device__ constexpr int epi_warp_bytes(int k) {
   return k == kEpiLogits ? 32 * kLogitsLd * 4
          : k == kEpiLogitsT ? 0
-         : k == kEpiHeadLoss || k == kEpiHeadTopK ? 0
+         : k == kEpiHeadLoss ? 0
+         : k == kEpiHeadTopK ? 32 * 33 * 4
                              : 2 * slot_bytes(k);
 }
 __host__ __device__ constexpr int epi_bias_bytes(int k) {
@@ -347,18 +348,45 @@ __device__ __forceinline__ void head_loss_rows(uint32_t tbase, int row0, int nco
 
 // kEpiHeadTopK, one warp's share of a tile of the head, laid out as for
 // head_loss_rows: each thread owns token row0 + lane and the tile's
-// kHeadLossBlock vocabulary entries from ncol0.  It keeps the kTopKMax largest
-// in a sorted register list (an entry enters when it beats the last one,
-// strictly, then bubbles up past smaller ones: the scan runs in index order,
-// so among equal values the lower index stays first; NaN never enters), and
-// the block's maximum and sum of 2^((z - max) log2 e) for the logsumexp.
+// kHeadLossBlock vocabulary entries from ncol0.  Every lane is another token,
+// so inserting entries one by one into a sorted list would make the warp run
+// the insertion at nearly every entry.  Instead, in two passes over TMEM:
+//   1. each 32-entry chunk's maximum: the largest is the block's maximum (the
+//      base of the logsumexp sum, so no rescaling is needed) and the smallest
+//      is a floor under the block's top kTopKMax (the chunk maxima are
+//      kTopKMax entries at least that large);
+//   2. the sum of 2^((z - max) log2 e), and the entries at or above the floor
+//      as a bit mask (about one in twenty on random logits); when any lane of
+//      the warp has some, the chunk goes to shared memory (rows padded to 33
+//      floats: conflict-free), and each lane inserts its candidates, in index
+//      order, into its sorted list of kTopKMax with a branch-free network
+//      (strict comparisons: among equal values the lower index stays first).
+// NaN and -inf entries are never candidates (the entries past V are -inf).
 __device__ __forceinline__ void head_topk_rows(uint32_t tbase, int row0, int ncol0, int lane,
-                                               const GemmArgs& a) {
+                                               const GemmArgs& a, float* stage) {
   constexpr float kL2e = 1.4426950408889634f;
   const EpiParams& ep = a.ep;
   const int n_tok = a.M, V = a.N;
   const int row = row0 + lane;
   if (ncol0 >= V) return;  // a half tile past the vocabulary (warp-uniform)
+  const int n_chunks = min(kHeadLossBlock, V - ncol0 + 31) / 32;  // chunks with entries < V
+  float* srow = stage + lane * 33;
+  // Pass 1: chunk maxima.
+  float m = -INFINITY, thr = INFINITY;
+  for (int c = 0; c < n_chunks; ++c) {
+    const int col0 = ncol0 + 32 * c;
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(32 * c), r);
+    tmem_ld_wait();
+    float cm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (col0 + i < V) cm = fmaxf(cm, __uint_as_float(r[i]));
+    m = fmaxf(m, cm);
+    thr = fminf(thr, cm);
+  }
+  if (n_chunks < kTopKMax) thr = -INFINITY;  // fewer chunks than candidates: no floor
+  // Pass 2: the sum, and the candidates.
   float tv[kTopKMax];
   int ti[kTopKMax];
 #pragma unroll
@@ -366,54 +394,48 @@ __device__ __forceinline__ void head_topk_rows(uint32_t tbase, int row0, int nco
     tv[j] = -INFINITY;
     ti[j] = 0x7fffffff;
   }
-  float m = -INFINITY, sum = 0.f;
-  for (int c = 0; c < kHeadLossBlock; c += 32) {
-    const int col0 = ncol0 + c;
-    if (col0 >= V) break;  // warp-uniform
+  const float ml = m * kL2e;
+  float s4[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int c = 0; c < n_chunks; ++c) {
+    const int col0 = ncol0 + 32 * c;
     uint32_t r[32];
-    tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(c), r);
+    tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(32 * c), r);
     tmem_ld_wait();
-    if (col0 + 32 > V) {  // the vocabulary's ragged end: entries past it do not count
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (col0 + i >= V) r[i] = __float_as_uint(-INFINITY);
-    }
+    uint32_t mask = 0u;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const float v = __uint_as_float(r[i]);
-      if (v > tv[kTopKMax - 1]) {
-        tv[kTopKMax - 1] = v;
-        ti[kTopKMax - 1] = col0 + i;
+      const bool live = col0 + i < V;
+      if (live) s4[i & 3] += ex2(fmaf(v, kL2e, -ml));
+      if (live && v >= thr && v > -INFINITY) mask |= 1u << i;
+    }
+    if (__any_sync(0xffffffffu, mask != 0u)) {
 #pragma unroll
-        for (int j = kTopKMax - 1; j > 0; --j)
-          if (tv[j] > tv[j - 1]) {
-            const float fv = tv[j];
-            tv[j] = tv[j - 1];
-            tv[j - 1] = fv;
-            const int fi = ti[j];
-            ti[j] = ti[j - 1];
-            ti[j - 1] = fi;
-          }
+      for (int i = 0; i < 32; ++i) srow[i] = __uint_as_float(r[i]);
+      __syncwarp();
+      while (mask) {
+        const int i = __ffs(mask) - 1;
+        mask &= mask - 1u;
+        const float v = srow[i];
+        const int id = col0 + i;
+        bool gt[kTopKMax];
+#pragma unroll
+        for (int j = 0; j < kTopKMax; ++j) gt[j] = v > tv[j];
+#pragma unroll
+        for (int j = kTopKMax - 1; j > 0; --j) {
+          tv[j] = gt[j] ? (gt[j - 1] ? tv[j - 1] : v) : tv[j];
+          ti[j] = gt[j] ? (gt[j - 1] ? ti[j - 1] : id) : ti[j];
+        }
+        tv[0] = gt[0] ? v : tv[0];
+        ti[0] = gt[0] ? id : ti[0];
       }
+      __syncwarp();  // the stage is read before the next chunk overwrites it
     }
-    // The block's running maximum and rescaled sum (as head_loss_rows).
-    float cm = __uint_as_float(r[0]);
-#pragma unroll
-    for (int i = 1; i < 32; ++i) cm = fmaxf(cm, __uint_as_float(r[i]));
-    if (cm > m) {
-      sum = m == -INFINITY ? 0.f : sum * ex2((m - cm) * kL2e);
-      m = cm;
-    }
-    const float ml = m * kL2e;
-    float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int i = 0; i < 32; ++i) s4[i & 3] += ex2(fmaf(__uint_as_float(r[i]), kL2e, -ml));
-    sum += (s4[0] + s4[1]) + (s4[2] + s4[3]);
   }
   if (row < n_tok) {
     const size_t vb = static_cast<size_t>(ncol0 / kHeadLossBlock);
     ep.part_m[vb * n_tok + row] = m;
-    ep.part_s[vb * n_tok + row] = sum;
+    ep.part_s[vb * n_tok + row] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
 #pragma unroll
     for (int j = 0; j < kTopKMax; ++j) {
       ep.topk_v[(vb * kTopKMax + j) * n_tok + row] = tv[j];
@@ -863,7 +885,7 @@ __global__ void __launch_bounds__(epi_threads(KIND), 1)
       if constexpr (KIND == kEpiHeadLoss) {
         head_loss_rows(tbase, row0, ncol0, lane, args);
       } else if constexpr (KIND == kEpiHeadTopK) {
-        head_topk_rows(tbase, row0, ncol0, lane, args);
+        head_topk_rows(tbase, row0, ncol0, lane, args, reinterpret_cast<float*>(epi));
       } else {
         epilogue_tile<KIND>(tbase, row0, ncol0, ncols, lane, epi, bias_s, rbar, st, args, &tmO,
                             &tmR, &tmQ, &tmKV, abort_flag);

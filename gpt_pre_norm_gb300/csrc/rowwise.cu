@@ -548,23 +548,40 @@ __device__ __forceinline__ bool topk_before(float v1, int i1, float v2, int i2) 
   return v1 > v2 || (v1 == v2 && i1 < i2);
 }
 
-// Top-k from the top-k head's partials: one warp per token.  Lane l merges
-// the candidates of vocabulary blocks l, l + 32, ... into its own sorted list
-// of kTopKMax and their (max, sum) pairs into a logsumexp; then k rounds in
-// which the warp finds the best head of all lanes' lists (a butterfly on
-// (value, index)) and the lane holding it drops it.  Indices are unique, so
-// exactly one lane pops per round (or, once every list holds only empty
-// slots, all lanes alike, which ends the useful output: -1 from there on).
-__global__ void __launch_bounds__(256)
+// Inserts (v, i) into the sorted list tv / ti (descending by topk_before)
+// when it ranks before the last entry: a branch-free network (the entries
+// ranking before (v, i) keep their places, the others move down one).
+__device__ __forceinline__ void topk_insert(float (&tv)[kTopKMax], int (&ti)[kTopKMax], float v,
+                                            int i) {
+  bool gt[kTopKMax];
+#pragma unroll
+  for (int j = 0; j < kTopKMax; ++j) gt[j] = topk_before(v, i, tv[j], ti[j]);
+#pragma unroll
+  for (int j = kTopKMax - 1; j > 0; --j) {
+    tv[j] = gt[j] ? (gt[j - 1] ? tv[j - 1] : v) : tv[j];
+    ti[j] = gt[j] ? (gt[j - 1] ? ti[j - 1] : i) : ti[j];
+  }
+  tv[0] = gt[0] ? v : tv[0];
+  ti[0] = gt[0] ? i : ti[0];
+}
+
+// Top-k from the top-k head's partials: 32 tokens per block (one per lane),
+// kLossSlices warps each merging every kLossSlices-th vocabulary block (reads
+// of 32 consecutive tokens' candidates), then the warps' lists and logsumexp
+// partials in shared memory.  A block's candidates are sorted, so the scan of
+// a block stops at the first one that does not enter the list.
+__global__ void __launch_bounds__(32 * kLossSlices)
     head_topk_combine(const float* __restrict__ pm, const float* __restrict__ ps,
                       const float* __restrict__ cv, const int32_t* __restrict__ ci, int n_vblk,
                       int n_tok, int k, float* __restrict__ top_v, int32_t* __restrict__ top_i,
                       float* __restrict__ lse) {
   pdl_trigger();
   pdl_wait();
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (t >= n_tok) return;  // warp-uniform
+  __shared__ float sv[kLossSlices][kTopKMax][32];
+  __shared__ int si[kLossSlices][kTopKMax][32];
+  __shared__ float sm[kLossSlices][32], ss[kLossSlices][32];
+  const int lane = threadIdx.x & 31, slice = threadIdx.x >> 5;
+  const int t = blockIdx.x * 32 + lane;
   float tv[kTopKMax];
   int ti[kTopKMax];
 #pragma unroll
@@ -574,64 +591,53 @@ __global__ void __launch_bounds__(256)
   }
   float m = -INFINITY, sum = 0.f;
   int dummy = 0;
-  for (int b = lane; b < n_vblk; b += 32) {
-    const size_t o = static_cast<size_t>(b) * n_tok + t;
-    lse_merge_rw(m, sum, dummy, pm[o], ps[o], 0);
+  if (t < n_tok) {
+    for (int b = slice; b < n_vblk; b += kLossSlices) {
+      // All of the block's loads first (one round trip), then the merge.
+      const size_t o = static_cast<size_t>(b) * n_tok + t;
+      const float bm = pm[o], bs = ps[o];
+      float cvv[kTopKMax];
+      int cii[kTopKMax];
+#pragma unroll
+      for (int j = 0; j < kTopKMax; ++j) {
+        const size_t oj = (static_cast<size_t>(b) * kTopKMax + j) * n_tok + t;
+        cvv[j] = j < k ? cv[oj] : -INFINITY;
+        cii[j] = j < k ? ci[oj] : 0x7fffffff;
+      }
+      lse_merge_rw(m, sum, dummy, bm, bs, 0);
+#pragma unroll
+      for (int j = 0; j < kTopKMax; ++j) {
+        if (!topk_before(cvv[j], cii[j], tv[kTopKMax - 1], ti[kTopKMax - 1])) break;
+        topk_insert(tv, ti, cvv[j], cii[j]);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kTopKMax; ++j) {
+    sv[slice][j][lane] = tv[j];
+    si[slice][j][lane] = ti[j];
+  }
+  sm[slice][lane] = m;
+  ss[slice][lane] = sum;
+  __syncthreads();
+  if (slice != 0 || t >= n_tok) return;
+  for (int w = 1; w < kLossSlices; ++w) {
+    lse_merge_rw(m, sum, dummy, sm[w][lane], ss[w][lane], 0);
     for (int j = 0; j < k; ++j) {
-      const size_t oj = (static_cast<size_t>(b) * kTopKMax + j) * n_tok + t;
-      const float v = cv[oj];
-      const int id = ci[oj];
-      if (!topk_before(v, id, tv[kTopKMax - 1], ti[kTopKMax - 1])) break;  // the block's list is sorted
-      tv[kTopKMax - 1] = v;
-      ti[kTopKMax - 1] = id;
-#pragma unroll
-      for (int q = kTopKMax - 1; q > 0; --q)
-        if (topk_before(tv[q], ti[q], tv[q - 1], ti[q - 1])) {
-          const float fv = tv[q];
-          tv[q] = tv[q - 1];
-          tv[q - 1] = fv;
-          const int fi = ti[q];
-          ti[q] = ti[q - 1];
-          ti[q - 1] = fi;
-        }
+      const float v = sv[w][j][lane];
+      const int id = si[w][j][lane];
+      if (!topk_before(v, id, tv[kTopKMax - 1], ti[kTopKMax - 1])) break;
+      topk_insert(tv, ti, v, id);
     }
   }
-  for (int r = 0; r < k; ++r) {
-    float bv = tv[0];
-    int bi = ti[0];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (topk_before(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if (tv[0] == bv && ti[0] == bi) {  // this lane's head was taken
-#pragma unroll
-      for (int q = 0; q < kTopKMax - 1; ++q) {
-        tv[q] = tv[q + 1];
-        ti[q] = ti[q + 1];
-      }
-      tv[kTopKMax - 1] = -INFINITY;
-      ti[kTopKMax - 1] = 0x7fffffff;
-    }
-    if (lane == 0) {
-      const bool real = bi != 0x7fffffff;
-      top_v[static_cast<size_t>(t) * k + r] = bv;
-      top_i[static_cast<size_t>(t) * k + r] = real ? bi : -1;
+  for (int j = 0; j < kTopKMax; ++j) {
+    if (j < k) {
+      top_v[static_cast<size_t>(t) * k + j] = tv[j];
+      top_i[static_cast<size_t>(t) * k + j] = ti[j] == 0x7fffffff ? -1 : ti[j];
     }
   }
-  if (lse) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-      const float s2 = __shfl_xor_sync(0xffffffffu, sum, off);
-      lse_merge_rw(m, sum, dummy, m2, s2, 0);
-    }
-    if (lane == 0) lse[t] = m + logf(sum);
-  }
+  if (lse) lse[t] = m + logf(sum);
 }
 
 }  // namespace
@@ -643,8 +649,8 @@ int launch_head_topk_combine(const float* part_m, const float* part_s, const flo
       !topk_i || !top_v || !top_i)
     return GPT2_ERR_INVALID_ARG;
   const cudaError_t e =
-      launch_pdl(head_topk_combine, dim3((n_tok + 7) / 8), dim3(256), 0, stream, part_m, part_s,
-                 topk_v, topk_i, n_vblk, n_tok, k, top_v, top_i, lse);
+      launch_pdl(head_topk_combine, dim3((n_tok + 31) / 32), dim3(32 * kLossSlices), 0, stream,
+                 part_m, part_s, topk_v, topk_i, n_vblk, n_tok, k, top_v, top_i, lse);
   return e == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 

@@ -85,6 +85,11 @@ WORKLOADS = {
     "forward_loss_bf16_gpt2_small": Workload("forward_loss_bf16_gpt2_small", "forward_loss",
                                              "bf16", d=768, n_head=12, B=8, T=1024, n_layer=12,
                                              resid_scale_layers=12),
+    # The same forward ending in each position's 8 most likely next tokens and
+    # the logsumexp instead of the logits.
+    "forward_topk_bf16_gpt2_small": Workload("forward_topk_bf16_gpt2_small", "forward_topk",
+                                             "bf16", d=768, n_head=12, B=8, T=1024, n_layer=12,
+                                             resid_scale_layers=12),
     # GPT-2-XL-shaped block.
     "block_bf16_d1600": Workload("block_bf16_d1600", "block", "bf16", d=1600, n_head=25, B=4,
                                  T=1024, resid_scale_layers=48),

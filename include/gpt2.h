@@ -223,8 +223,8 @@ int gpt2_forward_loss(gpt2_ctx *ctx, const int32_t *ids, const int32_t *targets,
  * head on the fly, per position t of [B, T]:
  *   top_logits[t, i], top_ids[t, i] for i < k: the k largest z[t, v] in
  *     descending order with their ids (among equal values the lower id
- *     first; NaN logits are never chosen; -1 ids fill slots beyond the finite
- *     logits);
+ *     first; NaN and -inf logits are never chosen: id -1 and value -inf fill
+ *     slots beyond the other entries);
  *   lse[t] = logsumexp_v z[t, v], so that top_logits[t, i] - lse[t] are the
  *     log-probabilities of the candidates (NaN when a logit is NaN).
  * 1 <= k <= 8 and k <= n_vocab (INVALID_ARG otherwise).  top_logits: device

@@ -296,19 +296,20 @@ def top_k(logits: np.ndarray, k: int):
     the lower id first among equal values (the greedy choice argmax is the
     first of them, k = 1), and logsumexp(z), which turns them into
     log-probabilities ([FF] "How it works": the logits give the next token's
-    distribution; a sampler draws from its most likely candidates).  NaN
-    logits are never chosen.  logits [..., V] with V >= k.
+    distribution; a sampler draws from its most likely candidates).  NaN and
+    -inf logits are never chosen: slots beyond the other entries hold id -1
+    and value -inf.  logits [..., V].
     Returns (values [..., k], ids [..., k], lse [...])."""
     z = np.asarray(logits, np.float64)
     V = z.shape[-1]
     flat = z.reshape(-1, V)
-    ids = np.empty((flat.shape[0], k), np.int64)
+    ids = np.full((flat.shape[0], k), -1, np.int64)
+    vals = np.full((flat.shape[0], k), -np.inf)
     for r in range(flat.shape[0]):
-        key = np.where(np.isnan(flat[r]), -np.inf, flat[r])
-        order = np.lexsort((np.arange(V), -key))  # by value descending, then id ascending
-        ids[r] = order[:k]
-    ids = ids.reshape(z.shape[:-1] + (k,))
-    vals = np.take_along_axis(z, ids, axis=-1)
+        ok = np.nonzero(~np.isnan(flat[r]) & (flat[r] > -np.inf))[0]
+        order = ok[np.lexsort((ok, -flat[r][ok]))][:k]  # by value descending, then id ascending
+        ids[r, :len(order)] = order
+        vals[r, :len(order)] = flat[r][order]
     m = z.max(axis=-1)
     lse = m + np.log(np.exp(z - m[..., None]).sum(axis=-1))
-    return vals, ids, lse
+    return vals.reshape(z.shape[:-1] + (k,)), ids.reshape(z.shape[:-1] + (k,)), lse

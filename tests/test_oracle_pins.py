@@ -602,13 +602,18 @@ def test_loss_shift_invariance_and_library_special_case():
 
 
 # ------------------------------------------------------------------- top-k ----
-def test_top_k_hand_example_ties_and_nan():
+def test_top_k_hand_example_ties_nan_and_short_rows():
     """Worked by hand: values 3 (ids 4 and 1), 5, NaN, 3 again at id 7: the order is
-    5 (id 2), then the 3s by id (1, 4, 7); NaN (id 0) is never chosen."""
+    5 (id 2), then the 3s by id (1, 4, 7); NaN (id 0) is never chosen.  A row
+    with only two entries above -inf gives them, then id -1 with -inf."""
     z = np.array([[np.nan, 3.0, 5.0, -1.0, 3.0, 0.5, -2.0, 3.0]])
     vals, ids, _ = O.top_k(z, 4)
     assert ids.tolist() == [[2, 1, 4, 7]]
     assert vals.tolist() == [[5.0, 3.0, 3.0, 3.0]]
+    z2 = np.array([[-np.inf, 1.0, -np.inf, np.nan, 2.0]])
+    vals2, ids2, _ = O.top_k(z2, 3)
+    assert ids2.tolist() == [[4, 1, -1]]
+    assert vals2.tolist() == [[2.0, 1.0, -np.inf]]
 
 
 def test_top_k_first_is_argmax_and_set_is_the_k_largest():
@@ -671,4 +676,4 @@ def _topk_nan_as_largest(logits, k):
 def test_planted_top_k_mistake_is_caught(monkeypatch, bad):
     monkeypatch.setattr(O, "top_k", bad)
     with pytest.raises(AssertionError):
-        test_top_k_hand_example_ties_and_nan()
+        test_top_k_hand_example_ties_nan_and_short_rows()
