@@ -26,7 +26,9 @@ One JSON line is printed by rank 0.  Beside the device-timed value it carries:
               step copies its input from pinned host memory and its result
               back; steps are pipelined over the device input/result slots
               (copies on their own streams overlap the neighbouring steps'
-              compute), every copy inside the timed region;
+              compute), every copy inside the timed region; with it, the
+              host link as this run's copies see it (GB/s each way and the
+              copy time of one step) and the host's time to enqueue a step;
   workloads   the other configurations timed in the same run (the full
               GPT-2-small forward, the GPT-2-XL-shaped block, cached decode
               of the GPT-2-medium shape), each with its step time, tokens/s,
@@ -453,6 +455,7 @@ def timed_e2e(r, K, barrier, torch):
     start.record(comp)
     h2d.wait_stream(comp)
     d2h.wait_stream(comp)
+    t_host = time.perf_counter()
     for i in range(K):
         s = i % n
         with torch.cuda.stream(h2d):
@@ -472,9 +475,44 @@ def timed_e2e(r, K, barrier, torch):
     comp.wait_stream(h2d)
     comp.wait_stream(d2h)
     end.record(comp)
+    t_host = time.perf_counter() - t_host
     torch.cuda.synchronize()
     barrier()
-    return start.elapsed_time(end) / K
+    return start.elapsed_time(end) / K, t_host * 1e3 / K
+
+
+def link_probe(r, torch, reps=5):
+    """The host link as this run's end-to-end copies see it: the step's input
+    copy (pinned host -> slot 0) alone, its result copy (slot 0 -> pinned
+    host) alone, and the two at once on separate streams, each repeated reps
+    times and timed with events.  Returns GB/s per direction and the copy time
+    of one step at the concurrent rate, to set beside the device step time."""
+    h2d_b, d2h_b = r.e2e_bytes()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(use_in, use_out):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(s_in)
+        s_out.wait_event(a)
+        for _ in range(reps):
+            if use_in:
+                with torch.cuda.stream(s_in):
+                    r.stage_input(0)
+            if use_out:
+                with torch.cuda.stream(s_out):
+                    r.fetch_result(0)
+        s_in.wait_stream(s_out)
+        b.record(s_in)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / 1e3 / reps  # seconds per repetition
+
+    timed(True, True)  # first touch of the buffers
+    t_in, t_out, t_both = timed(True, False), timed(False, True), timed(True, True)
+    out = {"h2d_gbs": h2d_b / t_in / 1e9, "d2h_gbs": d2h_b / t_out / 1e9,
+           "both_gbs_per_direction": max(h2d_b, d2h_b) / t_both / 1e9,
+           "copy_ms_per_step": t_both * 1e3}
+    return out
 
 
 # -------------------------------------------------------------- CPU oracle --
@@ -629,6 +667,13 @@ def measure(r, args, barrier, torch, G, e2e: bool):
     if st != G.GPT2_OK:
         raise SystemExit(f"{r.w.name}: device error after warm-up: {G.status_string(st)}")
     out = {}
+    # The end-to-end steps run before the clock sampler's nvidia-smi starts:
+    # host-memory copies issued just after such a process exits were held up
+    # for 1-30 ms (4 of 40 end-to-end runs that followed one, 1 of 80
+    # otherwise), while kernels ran at their usual speed.
+    out["ms_e2e"], out["host_ms_e2e"] = timed_e2e(r, args.steps, barrier, torch) if e2e \
+        else (None, None)
+    out["link"] = link_probe(r, torch) if e2e else None
     with ClockSampler(torch.cuda.current_device()) as clk:
         out["times"] = timed_steps(r.run, args.steps, barrier, torch)
     out["clocks"] = clk.summary()
@@ -636,7 +681,6 @@ def measure(r, args, barrier, torch, G, e2e: bool):
     if r.graph is not None:
         t = timed_steps(r.step, args.steps, barrier, torch)
         out["ms_eager"] = sum(t) / len(t)
-    out["ms_e2e"] = timed_e2e(r, args.steps, barrier, torch) if e2e else None
     out["ms_cached"] = None
     if r.w.kind == "block" and r.w.dtype == "bf16":
         G.gpt2_ctx_cache_weights(r.ctx, True)
@@ -768,7 +812,9 @@ def main():
         "e2e": {"value": job_throughput(tokens_rank, ws, ms_e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "pipelined": f"{slots} device input/result slots; copies on their own "
-                             "streams"},
+                             "streams",
+                "link": m["link"],
+                "host_enqueue_ms_per_step": m["host_ms_e2e"]},
         "gpu_launches": int(round(sum(v["launches"] for v in prof.values()))),
         "clocks": m["clocks"],
         "kernels": kernel_table(prof, peaks, args.steps),
