@@ -50,10 +50,15 @@ constexpr int kBK = 64;                       // one 128-byte swizzle row of bf1
 // columns), or one for the bf16 block output made from the fp32 residual
 // (measured on GB300 for the block's mlp c_proj: GPT-2-small 43.3 -> 41.2 us,
 // GPT-2-XL shape 80 -> 70 us with four; the in-place fp32 residual epilogue
-// is faster with eight).
+// is faster with eight).  The top-k head has eight in two groups of four, one
+// group per accumulator: each warp reduces whole rows of 256 entries, and the
+// two groups drain alternate tiles at the same time.
 __host__ __device__ constexpr int epi_warps(int k) {
-  return k == kEpiResidBf16Out || k == kEpiHeadLoss || k == kEpiHeadTopK ? 4 : 8;
+  return k == kEpiResidBf16Out || k == kEpiHeadLoss ? 4 : 8;
 }
+// Epilogue groups that each own one accumulator (else every epilogue warp
+// takes part in every tile).
+__host__ __device__ constexpr bool acc_groups(int k) { return k == kEpiHeadTopK; }
 __host__ __device__ constexpr int epi_threads(int k) { return 128 + 32 * epi_warps(k); }
 constexpr uint32_t kABytes = kBM * kBK * 2;   // 16 KB per A slot
 constexpr int kMaxStages = 8;
@@ -346,46 +351,101 @@ __device__ __forceinline__ void head_loss_rows(uint32_t tbase, int row0, int nco
   }
 }
 
+// min with NaN propagation (min.NaN): a NaN entry must not pass for a second
+// largest value (fminf would return the other operand).
+__device__ __forceinline__ float fmin_nan(float a, float b) {
+  float r;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// Sorts 16 values in descending order (bitonic network, fixed indices).
+__device__ __forceinline__ void sort16_desc(float (&v)[16]) {
+#pragma unroll
+  for (int ks = 1; ks <= 4; ++ks) {
+    const int k = 1 << ks;
+#pragma unroll
+    for (int js = ks - 1; js >= 0; --js) {
+      const int j = 1 << js;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int l = i ^ j;
+        if (l > i) {
+          const float hi = fmaxf(v[i], v[l]), lo = fminf(v[i], v[l]);
+          const bool desc = (i & k) == 0;
+          v[i] = desc ? hi : lo;
+          v[l] = desc ? lo : hi;
+        }
+      }
+    }
+  }
+}
+
 // kEpiHeadTopK, one warp's share of a tile of the head, laid out as for
 // head_loss_rows: each thread owns token row0 + lane and the tile's
 // kHeadLossBlock vocabulary entries from ncol0.  Every lane is another token,
 // so inserting entries one by one into a sorted list would make the warp run
 // the insertion at nearly every entry.  Instead, in two passes over TMEM:
-//   1. each 32-entry chunk's maximum: the largest is the block's maximum (the
-//      base of the logsumexp sum, so no rescaling is needed) and the smallest
-//      is a floor under the block's top kTopKMax (the chunk maxima are
-//      kTopKMax entries at least that large);
+//   1. each 32-entry chunk's largest and second largest entry (NaN and the
+//      entries past V left out): the largest of all is the block's maximum
+//      (the base of the logsumexp sum, so no rescaling is needed), and the
+//      k-th largest of these 16 values is a floor under the block's top k
+//      (they are k distinct entries at least that large);
 //   2. the sum of 2^((z - max) log2 e), and the entries at or above the floor
-//      as a bit mask (about one in twenty on random logits); when any lane of
+//      as a bit mask (about one in nine on random logits); when any lane of
 //      the warp has some, the chunk goes to shared memory (rows padded to 33
 //      floats: conflict-free), and each lane inserts its candidates, in index
 //      order, into its sorted list of kTopKMax with a branch-free network
 //      (strict comparisons: among equal values the lower index stays first).
-// NaN and -inf entries are never candidates (the entries past V are -inf).
+// The first k entries of the list are the block's top k; the floor is kept
+// above -inf, so NaN and -inf entries are never candidates.
 __device__ __forceinline__ void head_topk_rows(uint32_t tbase, int row0, int ncol0, int lane,
                                                const GemmArgs& a, float* stage) {
   constexpr float kL2e = 1.4426950408889634f;
+  constexpr int kChunks = kHeadLossBlock / 32;
+  static_assert(2 * kChunks == 16 && kTopKMax <= 16, "floor from 16 chunk values");
   const EpiParams& ep = a.ep;
   const int n_tok = a.M, V = a.N;
   const int row = row0 + lane;
   if (ncol0 >= V) return;  // a half tile past the vocabulary (warp-uniform)
-  const int n_chunks = min(kHeadLossBlock, V - ncol0 + 31) / 32;  // chunks with entries < V
+  const int n_live = min(kHeadLossBlock, V - ncol0);  // entries below V
+  const int n_chunks = (n_live + 31) / 32;
   float* srow = stage + lane * 33;
-  // Pass 1: chunk maxima.
-  float m = -INFINITY, thr = INFINITY;
+  // Pass 1: the chunks' two largest entries, shifted in at the front.
+  float top[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) top[j] = -INFINITY;
   for (int c = 0; c < n_chunks; ++c) {
-    const int col0 = ncol0 + 32 * c;
     uint32_t r[32];
     tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(32 * c), r);
     tmem_ld_wait();
-    float cm = -INFINITY;
+    float m1 = -INFINITY, m2 = -INFINITY;
+    if (32 * c + 32 <= n_live) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (col0 + i < V) cm = fmaxf(cm, __uint_as_float(r[i]));
-    m = fmaxf(m, cm);
-    thr = fminf(thr, cm);
+      for (int i = 0; i < 32; ++i) {
+        const float v = __uint_as_float(r[i]);
+        m2 = fmaxf(m2, fmin_nan(m1, v));
+        m1 = fmaxf(m1, v);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float v = 32 * c + i < n_live ? __uint_as_float(r[i]) : -INFINITY;
+        m2 = fmaxf(m2, fmin_nan(m1, v));
+        m1 = fmaxf(m1, v);
+      }
+    }
+#pragma unroll
+    for (int j = 15; j >= 2; --j) top[j] = top[j - 2];
+    top[0] = m1;
+    top[1] = m2;
   }
-  if (n_chunks < kTopKMax) thr = -INFINITY;  // fewer chunks than candidates: no floor
+  sort16_desc(top);
+  const float m = top[0];
+  float thr = top[0];  // top[k - 1], as the least of the first k (no indexed read)
+#pragma unroll
+  for (int j = 1; j < kTopKMax; ++j) thr = j < ep.topk_k ? fminf(thr, top[j]) : thr;
+  thr = fmaxf(thr, -3.402823466e38f);  // never -inf: -inf entries are no candidates
   // Pass 2: the sum, and the candidates.
   float tv[kTopKMax];
   int ti[kTopKMax];
@@ -402,12 +462,21 @@ __device__ __forceinline__ void head_topk_rows(uint32_t tbase, int row0, int nco
     tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(32 * c), r);
     tmem_ld_wait();
     uint32_t mask = 0u;
+    if (32 * c + 32 <= n_live) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float v = __uint_as_float(r[i]);
-      const bool live = col0 + i < V;
-      if (live) s4[i & 3] += ex2(fmaf(v, kL2e, -ml));
-      if (live && v >= thr && v > -INFINITY) mask |= 1u << i;
+      for (int i = 0; i < 32; ++i) {
+        const float v = __uint_as_float(r[i]);
+        s4[i & 3] += ex2(fmaf(v, kL2e, -ml));
+        mask |= (v >= thr ? 1u : 0u) << i;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float v = __uint_as_float(r[i]);
+        const bool live = 32 * c + i < n_live;
+        if (live) s4[i & 3] += ex2(fmaf(v, kL2e, -ml));
+        mask |= (live && v >= thr ? 1u : 0u) << i;
+      }
     }
     if (__any_sync(0xffffffffu, mask != 0u)) {
 #pragma unroll
@@ -722,7 +791,7 @@ __global__ void __launch_bounds__(epi_threads(KIND), 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], kEpiWarps * CG);
+      mbar_init(&tempty[i], (acc_groups(KIND) ? 4 : kEpiWarps) * CG);
     }
     mbar_init(mma_done, 1);
     for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(&rbars[i], 1);
@@ -847,12 +916,15 @@ __global__ void __launch_bounds__(epi_threads(KIND), 1)
   } else if (warp >= 4) {
     // --------------------------------------------------------- epilogue --
     // Warp w may read TMEM lanes 32*(w%4) .. +31; the two warps of a lane
-    // quarter split the tile's columns in halves.  What does not depend on the
-    // accumulator is fetched before waiting for it.
+    // quarter split the tile's columns in halves, or (accumulator groups)
+    // each takes every other tile, all its columns.  What does not depend on
+    // the accumulator is fetched before waiting for it.
+    constexpr bool kGroups = acc_groups(KIND);
     const int e = warp - 4;
     const int quarter = warp & 3;
-    const int half = e >> 2;                   // column segment
-    const int ncols = BN / (kEpiWarps / 4);
+    const int half = kGroups ? 0 : e >> 2;     // column segment
+    const int group = kGroups ? e >> 2 : 0;    // accumulator (tiles it, it % 2 == group)
+    const int ncols = kGroups ? BN : BN / (kEpiWarps / 4);
     uint8_t* epi = sEpi + static_cast<size_t>(e) * epi_warp_bytes(KIND);
     uint16_t* bias_half = reinterpret_cast<uint16_t*>(sEpi + kEpiWarps * epi_warp_bytes(KIND)) +
                           half * kBiasBufs * (256 / (kEpiWarps / 4));
@@ -867,8 +939,10 @@ __global__ void __launch_bounds__(epi_threads(KIND), 1)
     }
     // The accumulator-drained barrier lives in the pair's first CTA.
     const uint32_t tempty_addr = CG == 2 ? mapa_shared(smem_u32(tempty), 0u) : 0u;
-    int it = 0;
-    for (int tile = first_tile; tile < args.num_tiles; tile += tile_step, ++it) {
+    const int it_step = kGroups ? 2 : 1;
+    int it = group;
+    for (int tile = first_tile + group * tile_step; tile < args.num_tiles;
+         tile += it_step * tile_step, it += it_step) {
       const int acc = it & 1;
       const uint32_t acc_par = static_cast<uint32_t>((it >> 1) & 1);
       int m_blk, n_blk;

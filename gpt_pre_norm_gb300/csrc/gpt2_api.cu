@@ -942,6 +942,7 @@ int gpt2_forward_topk(gpt2_ctx* c, const int32_t* ids, int B, int T, const gpt2_
   e.part_s = ps;
   e.topk_v = tv;
   e.topk_i = ti;
+  e.topk_k = k;
   st = c->run(kKindGemmLogits, s, [&](double* fl, double* by) {
     return launch_gemm_tc(c->env, kEpiHeadTopK, c->ws + c->plan.ln, wte16, M, V, d, e, s, fl,
                           by, true, false);

@@ -85,12 +85,15 @@ struct EpiParams {
   float* part_m;
   float* part_s;
   int32_t* part_i;
-  // kEpiHeadTopK: part_m, part_s as above, and the block's kTopKMax largest
+  // kEpiHeadTopK: part_m, part_s as above, and the block's topk_k largest
   // logits in descending order (among equal values the lower index first; NaN
-  // never taken) topk_v[(j * kTopKMax + i) * n_tok + t] with their indices
-  // topk_i[..] (-inf and 0x7fffffff where the block has fewer candidates).
+  // and -inf never taken) in the first topk_k of kTopKMax slots
+  // topk_v[(j * kTopKMax + i) * n_tok + t], with their indices topk_i[..]
+  // (-inf and 0x7fffffff where the block has fewer; the later slots hold
+  // some of the next largest, and are not read).
   float* topk_v;
   int32_t* topk_i;
+  int topk_k;
 };
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,

@@ -113,3 +113,26 @@ def test_topk_argument_errors(G):
         G.gpt2_forward_topk(c2, dev(np.zeros((1, 4), np.int32), torch.int32),
                             G.ModelParams(model_to_device(ps)), 1, 4, 6)  # k > V
     assert G.gpt2_sync_status(ctx) == G.GPT2_OK
+
+
+@pytest.mark.parametrize("k", [8, 3])
+def test_topk_ties_take_the_lower_ids(G, k):
+    """Embedding rows repeating with period 97: each logit value of a row is
+    shared by 10 or 11 vocabulary entries spread over every 256-entry block
+    (V = 1000, ragged last block), so a position's top k is a run of equal
+    values: its ids must be the lowest ids of the largest values, the rule of
+    the oracle's top_k applied to the library's own logits."""
+    w = _model(1000, B=2, T=40)
+    p = S.model_params(w, seed=35)
+    p["wte"] = np.ascontiguousarray(p["wte"][np.arange(w.n_vocab) % 97])
+    ids = S.token_ids(w, seed=35)
+    ctx = G.Context(w.n_vocab, w.n_ctx, w.d, w.n_head, w.n_layer, G.GPT2_BF16, w.B, w.T)
+    mp = G.ModelParams(model_to_device(p))
+    ids_d = dev(ids, torch.int32)
+    z = host(G.gpt2_forward(ctx, ids_d, mp, w.B, w.T))
+    vals, tid, lse = G.gpt2_forward_topk(ctx, ids_d, mp, w.B, w.T, k)
+    assert G.gpt2_sync_status(ctx) == G.GPT2_OK
+    tid = tid.cpu().numpy()
+    _, ref_ids, _ = O.top_k(z, k)
+    np.testing.assert_array_equal(tid, ref_ids)
+    assert np.all(tid[..., 1:] % 97 == tid[..., :1] % 97)  # one run of equal values
