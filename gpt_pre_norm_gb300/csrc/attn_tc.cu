@@ -345,17 +345,23 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int c = 0; c < kKT; ++c)
             if (key0 + c > pos) sr[c] = __float_as_uint(-INFINITY);
         }
-        // Row maximum over eight independent chains of three-input maxima.
+        // Row maximum over eight independent chains (keys i, i + 8, ..., i + 56):
+        // three-input maxima over keys 0..55, a two-input one for 56..63.
         float mx;
         {
+          static_assert(kKT == 64, "the chains below cover 64 keys");
           float m8[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) m8[i] = __uint_as_float(sr[i]);
+          for (int i = 0; i < 8; ++i)
+            m8[i] = max3(__uint_as_float(sr[i]), __uint_as_float(sr[8 + i]),
+                         __uint_as_float(sr[16 + i]));
 #pragma unroll
-          for (int c = 8; c < kKT; c += 16)
+          for (int c = 24; c < 56; c += 16)
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               m8[i] = max3(m8[i], __uint_as_float(sr[c + i]), __uint_as_float(sr[c + 8 + i]));
+#pragma unroll
+          for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], __uint_as_float(sr[56 + i]));
           mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
         }
         // A new reference maximum only when this row's passed it by more
