@@ -5,7 +5,9 @@ logsumexp without them: the k ids must be a top-k of those logits (within the
 few fp32 ulps by which the two head layouts' sums may differ), in descending
 order, with their values and the logsumexp matching the logits; k = 1 must
 equal the greedy choice of gpt2_forward_loss bit for bit (the same head
-layout); and the top choice and logsumexp must agree with the fp64 oracle.
+layout); and the logsumexp must agree with the fp64 oracle, and the top choice
+wherever the oracle's top two logits are further apart than the library's
+logit error (elsewhere it must be within that error of the maximum).
 Vocabularies with a ragged last 256-entry block, one block only, and the
 GPT-2 size; a cached decode step; argument errors."""
 import numpy as np
@@ -50,6 +52,23 @@ def _check_against_logits(z, vals, ids, lse, k):
     np.testing.assert_allclose(lse.reshape(-1), ref_lse, rtol=1e-5, atol=1e-4)
 
 
+def _check_top_choice(z, ref, got, rv, ri):
+    """The top choice against the fp64 oracle, position by position.  Where
+    the oracle's two largest logits are further apart than twice the
+    library's logit error on that row (measured on its own logits z, plus the
+    few ulps between the two head layouts), the choice is decided at this
+    precision and must be the oracle's; elsewhere it must be a logit within
+    that error of the oracle's maximum.  Most positions must be decided."""
+    zf = z.astype(np.float64)
+    err = np.abs(zf - ref).max(axis=-1) + 1e-4 * np.maximum(1.0, np.abs(zf).max(axis=-1))
+    decided = rv[..., 0] - rv[..., 1] > 2 * err
+    # 0.93-0.99 of the 260 positions on these inputs
+    assert np.mean(decided) >= 0.85, f"decided at only {np.mean(decided):.3f} of positions"
+    np.testing.assert_array_equal(got[decided], ri[..., 0][decided])
+    chosen = np.take_along_axis(ref, got[..., None].astype(np.int64), axis=-1)[..., 0]
+    assert np.all(chosen >= rv[..., 0] - 2 * err)
+
+
 @pytest.mark.parametrize("V,k", [(1000, 8), (1000, 1), (200, 5), (50257, 4)])
 def test_topk_matches_the_logits_and_the_oracle(G, V, k):
     """V = 1000: a ragged last block (232 entries); V = 200: a single block;
@@ -69,8 +88,8 @@ def test_topk_matches_the_logits_and_the_oracle(G, V, k):
     _check_against_logits(z, vals, tid, lse, k)
     np.testing.assert_array_equal(tid[..., 0], nxt.cpu().numpy())  # same head layout as the loss
     ref = O.forward(ids, p, w.n_head)[0]
-    rv, ri, rlse = O.top_k(ref, k)
-    assert np.mean(tid[..., 0] == ri[..., 0]) >= ARGMAX_AGREE
+    rv, ri, rlse = O.top_k(ref, max(k, 2))
+    _check_top_choice(z, ref, tid[..., 0], rv, ri)
     np.testing.assert_allclose(lse, rlse, rtol=2e-3, atol=2e-3)
     np.testing.assert_allclose(vals[..., 0], rv[..., 0], rtol=1e-2, atol=2e-2)
 
@@ -93,7 +112,7 @@ def test_topk_after_a_cached_prefix(G):
     assert cache.T_len == 41
     ref = O.forward(ids, p, w.n_head, positions=[40])[0]
     rv, ri, rlse = O.top_k(ref, 6)
-    assert np.mean(tid.cpu().numpy()[..., 0] == ri[..., 0]) >= ARGMAX_AGREE
+    assert np.mean(tid.cpu().numpy()[..., 0] == ri[..., 0]) >= ARGMAX_AGREE  # 3 positions: all
     np.testing.assert_allclose(host(lse), rlse, rtol=2e-3, atol=2e-3)
 
 
