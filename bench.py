@@ -119,8 +119,10 @@ def source_digest(files):
 KERNEL_SOURCES = {
     "gemm": ["gpt_pre_norm_gb300/csrc/gemm_tc.cu", "gpt_pre_norm_gb300/csrc/gemm_smallm.cu",
              "gpt_pre_norm_gb300/csrc/device.cuh"],
-    "attention": ["gpt_pre_norm_gb300/csrc/attn_tc.cu", "gpt_pre_norm_gb300/csrc/attention.cu",
-                  "gpt_pre_norm_gb300/csrc/device.cuh"],
+    "attention_prefill": ["gpt_pre_norm_gb300/csrc/attn_tc.cu",
+                          "gpt_pre_norm_gb300/csrc/device.cuh"],
+    "attention_decode": ["gpt_pre_norm_gb300/csrc/attention.cu",
+                         "gpt_pre_norm_gb300/csrc/device.cuh"],
     "row": ["gpt_pre_norm_gb300/csrc/rowwise.cu", "gpt_pre_norm_gb300/csrc/device.cuh"],
 }
 
@@ -128,8 +130,10 @@ KERNEL_SOURCES = {
 def kernel_family(kind: str) -> str:
     if kind.startswith("gemm"):
         return "gemm"
+    if kind.startswith("attention_decode"):
+        return "attention_decode"
     if kind.startswith("attention"):
-        return "attention"
+        return "attention_prefill"
     return "row"
 
 
