@@ -42,6 +42,9 @@ One JSON line is printed by rank 0.  Beside the device-timed value it carries:
               mean);
   eager_ms_per_step  for the graph-replayed decode step, the same step with
               its kernels launched one by one;
+  graph_ms_per_step  for the other steps, launched one by one for the
+              headline, the same steps replayed from CUDA graphs (one per
+              input slot);
   cached_weights  for the block workloads, the same step with the fp16
               working copies of the weights made by an earlier call (what the
               per-call conversion from bf16 costs).
@@ -382,6 +385,19 @@ class Runner:
             self.step()
         self.graph = g
 
+    def capture_slot_graphs(self):
+        """One CUDA graph of the step per input/result slot (the same launches
+        as step(s), replayed without host work)."""
+        torch = self.torch
+        graphs = []
+        for s in range(self.slots):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.step(s)
+            graphs.append(g)
+        torch.cuda.synchronize()
+        return graphs
+
     def run(self, s: int = 0):
         if self.graph is not None:
             self.graph.replay()
@@ -682,9 +698,16 @@ def measure(r, args, barrier, torch, G, e2e: bool):
         out["times"] = timed_steps(r.run, args.steps, barrier, torch)
     out["clocks"] = clk.summary()
     out["ms_eager"] = None
+    out["ms_graph"] = None
     if r.graph is not None:
         t = timed_steps(r.step, args.steps, barrier, torch)
         out["ms_eager"] = sum(t) / len(t)
+    else:
+        # The same steps replayed from CUDA graphs, one per slot.
+        graphs = r.capture_slot_graphs()
+        t = timed_steps(lambda i: graphs[i % len(graphs)].replay(), args.steps, barrier, torch)
+        out["ms_graph"] = sum(t) / len(t)
+        del graphs
     out["ms_cached"] = None
     if r.w.kind == "block" and r.w.dtype == "bf16":
         G.gpt2_ctx_cache_weights(r.ctx, True)
@@ -717,6 +740,8 @@ def workload_entry(w, r, m, peaks, args, ws, device):
          "clocks": m["clocks"]}
     if m["ms_eager"] is not None:
         e["eager_ms_per_step"] = reduce_over_ranks([m["ms_eager"]], device)[0]
+    if m["ms_graph"] is not None:
+        e["graph_ms_per_step"] = reduce_over_ranks([m["ms_graph"]], device)[0]
     if m["ms_cached"] is not None:
         e["cached_weights"] = cached_entry(r, m, ws, device)
     return e
@@ -775,6 +800,7 @@ def main():
     ms, ms_e2e, ms_med = reduce_over_ranks(
         [sum(times) / len(times), m["ms_e2e"], statistics.median(times)], device)
     ms_eager = reduce_over_ranks([m["ms_eager"]], device)[0] if m["ms_eager"] is not None else None
+    ms_graph = reduce_over_ranks([m["ms_graph"]], device)[0] if m["ms_graph"] is not None else None
     tokens_rank = r.tokens
     h2d, d2h = r.e2e_bytes()
     cached = cached_entry(r, m, ws, device) if m["ms_cached"] is not None else None
@@ -826,6 +852,8 @@ def main():
     }
     if ms_eager is not None:
         line["eager_ms_per_step"] = ms_eager  # the same step without the CUDA graph
+    if ms_graph is not None:
+        line["graph_ms_per_step"] = ms_graph  # the same steps replayed from CUDA graphs
     if cached is not None:
         line["cached_weights"] = cached
     if not args.no_cpu_baseline and ws == 1:
