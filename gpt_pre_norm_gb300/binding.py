@@ -89,6 +89,8 @@ def _load() -> C.CDLL:
         "gpt2_attention": (I, [P, P, P, I, I, I, I, I, I, P, P]),
         "gpt2_embed": (I, [P, P, P, P, I, I, I, P, P]),
         "gpt2_attention_decode_noalloc": (I, [P, P, I, I, I, I, I, I, P, P]),
+        "gpt2_attention_decode_noalloc_status": (I, [P]),
+        "gpt2_attention_decode_noalloc_set_wait_limit": (I, [LL]),
         "gpt2_ctx_cache_weights": (I, [P, I]),
         "gpt2_selftest_wait_timeout": (I, [P, I, P]),
         "gpt2_ctx_set_wait_limit": (I, [P, LL]),
@@ -365,6 +367,18 @@ def gpt2_attention_decode_noalloc(q: torch.Tensor, kv: torch.Tensor, T_past: int
                                              splits, _ptr(out), _stream(stream)),
            "gpt2_attention_decode_noalloc")
     return out
+
+
+def gpt2_attention_decode_noalloc_status(stream=None) -> int:
+    """The no-allocation decode entry point's device error word: synchronises
+    the stream, returns the status (OK or DEVICE_TIMEOUT) and clears it."""
+    return LIB.gpt2_attention_decode_noalloc_status(_stream(stream))
+
+
+def gpt2_attention_decode_noalloc_set_wait_limit(limit_ns: int) -> None:
+    """Test support: the no-allocation decode kernel's wait limit (<= 0: default)."""
+    _check(LIB.gpt2_attention_decode_noalloc_set_wait_limit(limit_ns),
+           "gpt2_attention_decode_noalloc_set_wait_limit")
 
 
 def gpt2_embed(ctx: Context, ids: torch.Tensor, wte: torch.Tensor, wpe: torch.Tensor,

@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(kDecThreads)
     attn_decode_bf16(const bf16* __restrict__ q, const bf16* __restrict__ kv, long long s_batch,
                      long long s_kv, long long s_head, int h, int t_len, int chunk,
                      uint16_t* __restrict__ out, float* __restrict__ partials, int out_f16,
-                     unsigned* err) {
+                     unsigned* err, unsigned long long wait_ns) {
   extern __shared__ __align__(128) uint8_t dsm[];
   uint8_t* sK = dsm;                                             // [stages][64 rows]
   uint8_t* sV = dsm + kDecStages * kDecStageKeys * kDecRowBytes;  // [stages][64 rows]
@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(kDecThreads)
   for (; j < ns; ++j) {
     const int slot = j % kDecStages;
     const bool got = mbar_wait_bounded(&full[slot], static_cast<uint32_t>(j / kDecStages) & 1u,
-                                       &s_abort, err);
+                                       &s_abort, err, wait_ns);
     if (got) {
       const int nk = min(kDecStageKeys, n_keys - j * kDecStageKeys);
       const uint8_t* kb = sK + slot * kDecStageKeys * kDecRowBytes;
@@ -331,7 +331,8 @@ int decode_splits(int B, int h, int t_len, int num_sms) {
 int launch_decode_attention_bf16(const bf16* q, const bf16* kv, long long s_batch, long long s_kv,
                                  long long s_head, int B, int h, int t_len, void* out,
                                  float* partials, int splits, cudaStream_t stream,
-                                 int* launches, bool out_f16, unsigned* err) {
+                                 int* launches, bool out_f16, unsigned* err,
+                                 unsigned long long wait_ns) {
   if (B <= 0 || h <= 0 || t_len <= 0 || splits <= 0 || splits > 65535) return GPT2_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * h > 65535) return GPT2_ERR_UNSUPPORTED;  // grid.y
   if (splits > 1 && partials == nullptr) return GPT2_ERR_INVALID_ARG;
@@ -342,7 +343,7 @@ int launch_decode_attention_bf16(const bf16* q, const bf16* kv, long long s_batc
     return GPT2_ERR_CUDA;
   cudaError_t e = launch_pdl(attn_decode_bf16, grid, dim3(kDecThreads), kDecSmem, stream, q, kv,
                              s_batch, s_kv, s_head, h, t_len, chunk, static_cast<uint16_t*>(out),
-                             partials, out_f16 ? 1 : 0, err);
+                             partials, out_f16 ? 1 : 0, err, wait_ns ? wait_ns : kWaitLimitNs);
   if (e != cudaSuccess) return GPT2_ERR_CUDA;
   int n = 1;
   if (splits > 1) {

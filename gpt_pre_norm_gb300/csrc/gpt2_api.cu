@@ -343,7 +343,7 @@ int block_sequence(gpt2_ctx* c, const gpt2_block_params* p, int slot, int B, int
       const int r = launch_decode_attention_bf16(
           static_cast<const bf16*>(q), reinterpret_cast<const bf16*>(kv.base), kv.s_batch,
           kv.s_kv, kv.s_head, B, h, t_len, attn, c->at<float>(c->plan.partials), splits, s, &nl,
-          true, c->env.err);
+          true, c->env.err, c->env.wait_ns);
       c->extra_kernels = nl - 1;
       return r;
     });
@@ -1049,7 +1049,7 @@ int gpt2_attention(gpt2_ctx* c, const void* q, const void* kv, int B, int n_head
       const int r = launch_decode_attention_bf16(
           static_cast<const bf16*>(q), reinterpret_cast<const bf16*>(v.base), v.s_batch, v.s_kv,
           v.s_head, B, n_head, t_len, out, c->at<float>(c->plan.partials), splits, s, &nl, false,
-          c->env.err);
+          c->env.err, c->env.wait_ns);
       c->extra_kernels = nl - 1;
       return r;
     });

@@ -189,7 +189,8 @@ int launch_attention_tc(const LaunchEnv& env, const bf16* q, const bf16* kv, lon
 int launch_decode_attention_bf16(const bf16* q, const bf16* kv, long long kv_s_batch,
                                  long long kv_s_kv, long long kv_s_head, int B, int h, int t_len,
                                  void* out, float* partials, int splits, cudaStream_t stream,
-                                 int* launches, bool out_f16 = false, unsigned* err = nullptr);
+                                 int* launches, bool out_f16 = false, unsigned* err = nullptr,
+                                 unsigned long long wait_ns = 0);  // 0: the default limit
 size_t decode_partials_floats(int B, int h, int splits);
 int decode_splits(int B, int h, int t_len, int num_sms);
 

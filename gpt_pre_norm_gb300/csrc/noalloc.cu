@@ -12,6 +12,7 @@
 // library holds it (1 MiB) until the process exits.  In host code its name is
 // only a host-side stand-in, so its device address is looked up once per
 // device, with that device current, by cudaGetSymbolAddress.
+#include <atomic>
 #include <mutex>
 
 #include "device.cuh"
@@ -25,12 +26,19 @@ constexpr size_t kScratchFloats = kScratchBytes / sizeof(float);
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) float g_decode_scratch[kScratchFloats];
+// The entry point's device error word (a bounded wait that ran out), read and
+// cleared by gpt2_attention_decode_noalloc_status.
+static __device__ unsigned g_decode_err;
 
 struct DeviceSetup {
   bool done = false;
   float* scratch = nullptr;
+  unsigned* err = nullptr;
   int num_sms = 0;
 };
+
+// Limit of the kernel's bounded waits, for every device (0: the default 2 s).
+std::atomic<unsigned long long> g_wait_ns{0};
 
 std::mutex g_setup_mutex;
 DeviceSetup g_setup[kMaxDevices];
@@ -45,11 +53,15 @@ int setup_current_device(DeviceSetup** out) {
   DeviceSetup& s = g_setup[dev];
   if (!s.done) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return GPT2_ERR_CUDA;
+    void* e = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess ||
+        cudaGetSymbolAddress(&e, g_decode_err) != cudaSuccess)
+      return GPT2_ERR_CUDA;
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return GPT2_ERR_CUDA;
     s.scratch = static_cast<float*>(p);
+    s.err = static_cast<unsigned*>(e);
     s.num_sms = sms;
     s.done = true;
   }
@@ -87,5 +99,23 @@ extern "C" int gpt2_attention_decode_noalloc(const void* q, const void* kv, int 
   return launch_decode_attention_bf16(static_cast<const bf16*>(q), static_cast<const bf16*>(kv),
                                       2 * s_kv, s_kv, s_head, B, n_head, t_len,
                                       static_cast<bf16*>(out), dev->scratch, splits,
-                                      static_cast<cudaStream_t>(stream), nullptr);
+                                      static_cast<cudaStream_t>(stream), nullptr, false, dev->err,
+                                      g_wait_ns.load());
+}
+
+extern "C" int gpt2_attention_decode_noalloc_status(void* stream) {
+  DeviceSetup* dev = nullptr;
+  const int st = setup_current_device(&dev);
+  if (st) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GPT2_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, dev->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GPT2_ERR_CUDA;
+  if (word != 0 && cudaMemset(dev->err, 0, sizeof(unsigned)) != cudaSuccess) return GPT2_ERR_CUDA;
+  return (word & kErrTimeout) ? GPT2_ERR_DEVICE_TIMEOUT : GPT2_OK;
+}
+
+extern "C" int gpt2_attention_decode_noalloc_set_wait_limit(long long limit_ns) {
+  g_wait_ns.store(limit_ns > 0 ? static_cast<unsigned long long>(limit_ns) : 0ull);
+  return GPT2_OK;
 }

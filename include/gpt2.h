@@ -306,14 +306,31 @@ int gpt2_attention(gpt2_ctx *ctx, const void *q, const void *kv, int B, int n_he
  * call's contents; nothing in it has to start at zero, since each call writes
  * every partial result before reading it.  Calls that overlap on the GPU
  * (other streams, other host threads) race on the array.
- * There is no context and so no device error word: if one of the kernel's
- * bounded waits runs out (2 s), that (sequence, head)'s output row is
- * written as NaN instead of being left as it was.
+ * If one of the kernel's bounded waits runs out (2 s by default), that
+ * (sequence, head)'s output row is written as NaN instead of being left as
+ * it was, and the timeout bit of the entry point's own device error word is
+ * set: gpt2_attention_decode_noalloc_status reports it.
  * Errors: INVALID_ARG, UNSUPPORTED (d_h != 64, or B * h > 65535),
  * CTX_OVERFLOW (T_past + 1 > T_cap), ALIGNMENT, WORKSPACE (B * h * splits
  * partial results of 66 floats exceed the 1 MiB array), NO_DEVICE, CUDA.    */
 int gpt2_attention_decode_noalloc(const void *q, const void *kv, int B, int n_head, int T_past,
                                   int T_cap, int d_h, int splits, void *out, void *stream);
+
+/* The device error word of gpt2_attention_decode_noalloc on the current
+ * device: synchronises `stream`, reads the word and clears it.  Returns
+ * DEVICE_TIMEOUT if a call since the last read had a bounded wait run out
+ * (its NaN rows are the ones affected), else OK; NO_DEVICE or CUDA when
+ * the device or the runtime fails.  Like the entry point it uses no context
+ * and allocates nothing (the word is compiled into the library, one per
+ * device).                                                                  */
+int gpt2_attention_decode_noalloc_status(void *stream);
+
+/* Test support: the limit of gpt2_attention_decode_noalloc's bounded waits,
+ * for all devices of the process, in nanoseconds; limit_ns <= 0 restores the
+ * 2 s default.  A limit of a few nanoseconds makes the first wait that is
+ * not already satisfied run out on ordinary work, so the timeout path can be
+ * tested without a fault.  Returns OK.                                      */
+int gpt2_attention_decode_noalloc_set_wait_limit(long long limit_ns);
 
 /* Embedding: H[b, t] = wte[ids[b, t]] + wpe[T_past + t] (fp32 out [B, T, d]).
  * wte [n_vocab, d], wpe [n_ctx, d] in the mode dtype.                      */
