@@ -505,11 +505,15 @@ __device__ __forceinline__ void head_topk_rows(uint32_t tbase, int row0, int nco
     const size_t vb = static_cast<size_t>(ncol0 / kHeadLossBlock);
     ep.part_m[vb * n_tok + row] = m;
     ep.part_s[vb * n_tok + row] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-#pragma unroll
-    for (int j = 0; j < kTopKMax; ++j) {
-      ep.topk_v[(vb * kTopKMax + j) * n_tok + row] = tv[j];
-      ep.topk_i[(vb * kTopKMax + j) * n_tok + row] = ti[j];
-    }
+    // The token's kTopKMax candidates contiguous (32 bytes each for values and
+    // ids): the warp's 32 tokens write 1 KB runs.
+    static_assert(kTopKMax == 8, "two 16-byte stores per list");
+    float4* dv = reinterpret_cast<float4*>(ep.topk_v + (vb * n_tok + row) * kTopKMax);
+    int4* di = reinterpret_cast<int4*>(ep.topk_i + (vb * n_tok + row) * kTopKMax);
+    dv[0] = make_float4(tv[0], tv[1], tv[2], tv[3]);
+    dv[1] = make_float4(tv[4], tv[5], tv[6], tv[7]);
+    di[0] = make_int4(ti[0], ti[1], ti[2], ti[3]);
+    di[1] = make_int4(ti[4], ti[5], ti[6], ti[7]);
   }
 }
 

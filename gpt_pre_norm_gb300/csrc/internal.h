@@ -88,7 +88,7 @@ struct EpiParams {
   // kEpiHeadTopK: part_m, part_s as above, and the block's topk_k largest
   // logits in descending order (among equal values the lower index first; NaN
   // and -inf never taken) in the first topk_k of kTopKMax slots
-  // topk_v[(j * kTopKMax + i) * n_tok + t], with their indices topk_i[..]
+  // topk_v[(j * n_tok + t) * kTopKMax + i], with their indices topk_i[..]
   // (-inf and 0x7fffffff where the block has fewer; the later slots hold
   // some of the next largest, and are not read).
   float* topk_v;

@@ -566,9 +566,9 @@ __device__ __forceinline__ void topk_insert(float (&tv)[kTopKMax], int (&ti)[kTo
 }
 
 // Top-k from the top-k head's partials: 32 tokens per block (one per lane),
-// kLossSlices warps each merging every kLossSlices-th vocabulary block (reads
-// of 32 consecutive tokens' candidates), then the warps' lists and logsumexp
-// partials in shared memory.  A block's candidates are sorted, so the scan of
+// kLossSlices warps each merging every kLossSlices-th vocabulary block (the
+// 32 consecutive tokens' candidate lists: 1 KB runs of values and of ids),
+// then the warps' lists and logsumexp partials in shared memory.  A block's candidates are sorted, so the scan of
 // a block stops at the first one that does not enter the list.
 __global__ void __launch_bounds__(32 * kLossSlices)
     head_topk_combine(const float* __restrict__ pm, const float* __restrict__ ps,
@@ -596,13 +596,18 @@ __global__ void __launch_bounds__(32 * kLossSlices)
       // All of the block's loads first (one round trip), then the merge.
       const size_t o = static_cast<size_t>(b) * n_tok + t;
       const float bm = pm[o], bs = ps[o];
-      float cvv[kTopKMax];
-      int cii[kTopKMax];
+      // The token's candidates: 32 contiguous bytes of values and of ids.
+      static_assert(kTopKMax == 8, "two 16-byte loads per list");
+      const float4* sv4 = reinterpret_cast<const float4*>(cv + o * kTopKMax);
+      const int4* si4 = reinterpret_cast<const int4*>(ci + o * kTopKMax);
+      const float4 v0 = sv4[0], v1 = sv4[1];
+      const int4 i0 = si4[0], i1 = si4[1];
+      float cvv[kTopKMax] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      int cii[kTopKMax] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
 #pragma unroll
       for (int j = 0; j < kTopKMax; ++j) {
-        const size_t oj = (static_cast<size_t>(b) * kTopKMax + j) * n_tok + t;
-        cvv[j] = j < k ? cv[oj] : -INFINITY;
-        cii[j] = j < k ? ci[oj] : 0x7fffffff;
+        cvv[j] = j < k ? cvv[j] : -INFINITY;
+        cii[j] = j < k ? cii[j] : 0x7fffffff;
       }
       lse_merge_rw(m, sum, dummy, bm, bs, 0);
 #pragma unroll
