@@ -89,3 +89,25 @@ def test_traffic_figure_needs_the_sources_it_was_taken_from(tmp_path, monkeypatc
     assert bench.ncu_traffic("gemm_c_proj", "block_bf16_d768") is None  # stale digest
     (tmp_path / bench.KERNEL_SOURCES["gemm"][0]).write_text("// changed\n")
     assert bench.ncu_traffic("gemm_c_fc", "block_bf16_d768") is None
+
+
+def test_prefill_and_decode_attention_are_keyed_by_their_own_sources(tmp_path, monkeypatch):
+    """A change to the prefill attention's source voids only the prefill
+    figure: the decode attention (and its combine) are keyed by theirs."""
+    assert bench.kernel_family("attention_prefill") == "attention_prefill"
+    assert bench.kernel_family("attention_decode") == "attention_decode"
+    assert bench.kernel_family("attention_decode_combine") == "attention_decode"
+    for rel in {f for files in bench.KERNEL_SOURCES.values() for f in files}:
+        p = tmp_path / rel
+        p.parent.mkdir(parents=True, exist_ok=True)
+        p.write_text("// " + rel + "\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    dp = bench.source_digest(bench.KERNEL_SOURCES["attention_prefill"])
+    dd = bench.source_digest(bench.KERNEL_SOURCES["attention_decode"])
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "ncu_traffic.txt").write_text(
+        f"attention_prefill block_bf16_d768 100 {dp}\n"
+        f"attention_decode decode_bf16_gpt2_medium 200 {dd}\n")
+    (tmp_path / "gpt_pre_norm_gb300/csrc/attn_tc.cu").write_text("// changed\n")
+    assert bench.ncu_traffic("attention_prefill", "block_bf16_d768") is None
+    assert bench.ncu_traffic("attention_decode", "decode_bf16_gpt2_medium") == 200.0
