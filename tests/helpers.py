@@ -74,3 +74,20 @@ def model_to_device(p: dict, dtype=torch.bfloat16) -> dict:
     out = {k: dev(p[k], dtype) for k in ("wte", "wpe", "lnf_g", "lnf_b")}
     out["blocks"] = [block_to_device(b, dtype) for b in p["blocks"]]
     return out
+
+
+def check_top_choice(z, ref, got, rv, ri):
+    """The top choice against the fp64 oracle, position by position.  Where
+    the oracle's two largest logits are further apart than twice the
+    library's logit error on that row (measured on its own logits z, plus the
+    few ulps between the two head layouts), the choice is decided at this
+    precision and must be the oracle's; elsewhere it must be a logit within
+    that error of the oracle's maximum.  Most positions must be decided."""
+    zf = z.astype(np.float64)
+    err = np.abs(zf - ref).max(axis=-1) + 1e-4 * np.maximum(1.0, np.abs(zf).max(axis=-1))
+    decided = rv[..., 0] - rv[..., 1] > 2 * err
+    # 0.93-0.99 of the positions on the random-weight models of the GPU tests
+    assert np.mean(decided) >= 0.85, f"decided at only {np.mean(decided):.3f} of positions"
+    np.testing.assert_array_equal(got[decided], ri[..., 0][decided])
+    chosen = np.take_along_axis(ref, got[..., None].astype(np.int64), axis=-1)[..., 0]
+    assert np.all(chosen >= rv[..., 0] - 2 * err)

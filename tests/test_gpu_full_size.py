@@ -9,7 +9,7 @@ import torch
 from oracle import gpt2_oracle as O
 from gpt_pre_norm_gb300 import synthetic as S
 from tests.helpers import (ARGMAX_AGREE, argmax_agreement, assert_bf16_close, block_to_device,
-                           dev, host, model_to_device)
+                           check_top_choice, dev, host, model_to_device)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -96,6 +96,42 @@ def test_forward_loss_full_size(G):
     ref_logits, _ = O.forward(ids[b:b + 1], p, w.n_head)
     ref_loss, _ = O.next_token_loss(ref_logits, targets[b:b + 1])
     np.testing.assert_allclose(loss[b], ref_loss[0], rtol=2e-3, atol=5e-3)
+
+
+def test_forward_topk_full_size(G):
+    """The fused head reduced to each position's top 8 at the benchmark's
+    configuration (B=8, T=1024, V=50257): every position against this
+    library's own logits (a valid top 8 in descending order, values at their
+    ids, logsumexp as torch's), and sequence 3 against the oracle (the top
+    choice wherever it is decided at this precision, the logsumexp)."""
+    w = S.WORKLOADS["forward_topk_bf16_gpt2_small"]
+    k = 8
+    seed = 0
+    p = S.model_params(w, seed)
+    ids = S.token_ids(w, seed)
+    ctx = G.Context(w.n_vocab, w.n_ctx, w.d, w.n_head, w.n_layer, G.GPT2_BF16, w.B, w.T)
+    mp = G.ModelParams(model_to_device(p))
+    ids_d = dev(ids, torch.int32)
+    vals, tid, lse = G.gpt2_forward_topk(ctx, ids_d, mp, w.B, w.T, k)
+    logits = G.gpt2_forward(ctx, ids_d, mp, w.B, w.T)
+    assert G.gpt2_sync_status(ctx) == G.GPT2_OK
+    tol = 1e-4 * torch.clamp(logits.abs().amax(-1), min=1.0)           # [B, T]
+    ti = tid.long()
+    assert bool(((ti >= 0) & (ti < w.n_vocab)).all())
+    assert bool((ti.sort(-1).values.diff(dim=-1) != 0).all())          # k distinct ids
+    assert bool((logits.gather(-1, ti) - vals).abs().le(tol[..., None]).all())
+    assert bool((vals[..., 1:] <= vals[..., :-1]).all())                 # descending
+    kth = logits.topk(k, dim=-1).values[..., -1]
+    assert bool((vals[..., -1] >= kth - tol).all())                      # nothing better left out
+    torch.testing.assert_close(lse, torch.logsumexp(logits.double(), -1).float(), rtol=1e-5,
+                               atol=1e-4)
+    b = 3
+    z = logits[b].cpu().numpy()
+    del logits
+    ref, _ = O.forward(ids[b:b + 1], p, w.n_head)
+    rv, ri, rlse = O.top_k(ref[0], k)
+    check_top_choice(z, ref[0], tid[b, :, 0].cpu().numpy(), rv, ri)
+    np.testing.assert_allclose(host(lse[b]), rlse, rtol=2e-3, atol=2e-3)
 
 
 def test_decode_full_size(G):

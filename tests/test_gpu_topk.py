@@ -16,7 +16,7 @@ import torch
 
 from oracle import gpt2_oracle as O
 from gpt_pre_norm_gb300 import synthetic as S
-from tests.helpers import ARGMAX_AGREE, dev, host, model_to_device
+from tests.helpers import ARGMAX_AGREE, check_top_choice, dev, host, model_to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -52,23 +52,6 @@ def _check_against_logits(z, vals, ids, lse, k):
     np.testing.assert_allclose(lse.reshape(-1), ref_lse, rtol=1e-5, atol=1e-4)
 
 
-def _check_top_choice(z, ref, got, rv, ri):
-    """The top choice against the fp64 oracle, position by position.  Where
-    the oracle's two largest logits are further apart than twice the
-    library's logit error on that row (measured on its own logits z, plus the
-    few ulps between the two head layouts), the choice is decided at this
-    precision and must be the oracle's; elsewhere it must be a logit within
-    that error of the oracle's maximum.  Most positions must be decided."""
-    zf = z.astype(np.float64)
-    err = np.abs(zf - ref).max(axis=-1) + 1e-4 * np.maximum(1.0, np.abs(zf).max(axis=-1))
-    decided = rv[..., 0] - rv[..., 1] > 2 * err
-    # 0.93-0.99 of the 260 positions on these inputs
-    assert np.mean(decided) >= 0.85, f"decided at only {np.mean(decided):.3f} of positions"
-    np.testing.assert_array_equal(got[decided], ri[..., 0][decided])
-    chosen = np.take_along_axis(ref, got[..., None].astype(np.int64), axis=-1)[..., 0]
-    assert np.all(chosen >= rv[..., 0] - 2 * err)
-
-
 @pytest.mark.parametrize("V,k", [(1000, 8), (1000, 1), (200, 5), (50257, 4)])
 def test_topk_matches_the_logits_and_the_oracle(G, V, k):
     """V = 1000: a ragged last block (232 entries); V = 200: a single block;
@@ -89,7 +72,7 @@ def test_topk_matches_the_logits_and_the_oracle(G, V, k):
     np.testing.assert_array_equal(tid[..., 0], nxt.cpu().numpy())  # same head layout as the loss
     ref = O.forward(ids, p, w.n_head)[0]
     rv, ri, rlse = O.top_k(ref, max(k, 2))
-    _check_top_choice(z, ref, tid[..., 0], rv, ri)
+    check_top_choice(z, ref, tid[..., 0], rv, ri)
     np.testing.assert_allclose(lse, rlse, rtol=2e-3, atol=2e-3)
     np.testing.assert_allclose(vals[..., 0], rv[..., 0], rtol=1e-2, atol=2e-2)
 
