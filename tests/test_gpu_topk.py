@@ -52,7 +52,7 @@ def _check_against_logits(z, vals, ids, lse, k):
     np.testing.assert_allclose(lse.reshape(-1), ref_lse, rtol=1e-5, atol=1e-4)
 
 
-@pytest.mark.parametrize("V,k", [(1000, 8), (1000, 1), (200, 5), (50257, 4)])
+@pytest.mark.parametrize("V,k", [(1000, 8), (1000, 1), (200, 5), (50257, 4), (1000, 2), (50257, 7)])
 def test_topk_matches_the_logits_and_the_oracle(G, V, k):
     """V = 1000: a ragged last block (232 entries); V = 200: a single block;
     V = 50257: the GPT-2 vocabulary."""
